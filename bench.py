@@ -1,0 +1,519 @@
+#!/usr/bin/env python3
+"""Benchmark: K-draft MTP verification over GatedDeltaNet layers on GB300.
+
+One step = one decode-only transaction of the workload: host plan
+(plan_transaction) -> gdn_verify for every layer -> mtp_greedy_accept ->
+gdn_commit -> the one device-to-host read of accept lengths / bonus / emitted
+tokens -> slot-pool release.  The metric is verified tokens per second
+(sum over requests of accepted drafts + 1) and the HBM bandwidth of
+verify + commit from algorithmic bytes.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload paged256]
+    python bench.py --impl reference ...   # the CPU oracle on the host cores
+
+Multi-GPU (torchrun): requests are independent, so every rank runs its own
+copy of the workload (weak scaling); the only collective is the barrier and
+the max of the timed region.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import gdnsynth as sy  # noqa: E402
+
+S_ROW_IO = lambda d: (2 * d.h_qk * d.d_k * 2 + 2 * d.h_v * d.d_v * 2 + 2 * d.h_v * 4)  # q,k,v,o bf16; g,beta fp32
+
+WORKLOADS = {
+    "paged256": sy.SPECS["paged256"],
+    "cb16": sy.SPECS["cb16"],
+    "batch1": sy.SPECS["batch1"],
+    "tiny": sy.SPECS["tiny"],
+    # a small case for ncu captures: 32 requests, 64 slots, 2 layers (inputs still larger than L2)
+    "small": sy.Spec("small", sy.DIMS_FULL, 2, 32, 3, 3, 20, sy.VOCAB_FULL, 2.0, 0.85, 64, 0, 2, 40),
+}
+
+WORKLOAD_TEXT = {
+    "paged256": "paged large batch: 256 requests in a pool of 1024 FP32 state slots (seeded permutation, 16 "
+                "requests share a prefix slot, copy-on-write), 30 GDN layers, H_qk=16, H_v=32, d_k=d_v=128, K=3, "
+                "acceptance Bernoulli 0.85, vocab 151936 bf16 logits",
+    "cb16": "continuous batch: 16 requests x 30 GDN layers, K ~ U{0..3} per step, ragged rows, Bernoulli 0.85",
+    "batch1": "batch-1 verify: 1 request, 1 GDN layer, K=3, vocab 151936",
+    "tiny": "tiny: 1 request, 1 layer, 2 heads, d=16, K=3, vocab 64",
+    "small": "ncu case: 32 requests, 64 slots, 2 layers, K=3",
+}
+
+# DRAM traffic of one gdn_verify launch from an ncu capture (dram__bytes_read.sum + dram__bytes_write.sum),
+# valid only while the kernel source is unchanged.  Filled from profiles/ summaries.
+TRAFFIC = {}
+
+
+def src_digest(path):
+    with open(path, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+# ---------------------------------------------------------------------------
+# clocks sampled during the timed region
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.idx = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "--query-gpu=" + self.Q, "--format=csv,noheader,nounits",
+                                          "-lms", "200", "-i", str(self.idx)], stdout=subprocess.PIPE,
+                                         stderr=subprocess.DEVNULL, text=True)
+            self.th = threading.Thread(target=self._read, daemon=True)
+            self.th.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# workload set-up (device)
+# ---------------------------------------------------------------------------
+
+class Bench:
+    def __init__(self, spec: sy.Spec, dev, rank=0):
+        from speculative_decoding_hybrid_gb300 import binding as gs
+        from speculative_decoding_hybrid_gb300.step import DecodeLoop, LayerRows, VerifyStep
+        self.gs, self.spec, self.dev = gs, spec, dev
+        d = spec.dims
+        self.d = d
+        self.cap = spec.batch * (spec.k_max + 1)
+        slot_of, free, ref = sy.initial_slots(spec)
+        order = []
+        for s in slot_of:
+            if s not in order:
+                order.append(s)
+        order += list(free)
+        self.pool_c = gs.Pool(spec.num_slots, order)
+        seen = set()
+        for s in slot_of:
+            if s in seen:
+                self.pool_c.share(s)
+            else:
+                self.pool_c.alloc()
+                seen.add(s)
+        pool = torch.empty((spec.num_slots, spec.layers, d.h_v, d.d_v, d.d_k), dtype=torch.float32, device=dev)
+        sy.pool_state(spec, dev, out=pool)
+        self.vs = VerifyStep(gs.dims(d.h_qk, d.h_v, d.d_k, d.d_v), spec.layers, spec.num_slots, self.cap,
+                             spec.batch, spec.vocab, dev, pool=pool)
+        self.loop = DecodeLoop(self.vs, slot_of, self.pool_c, k_max=spec.k_max)
+        self.rows = []
+        self.logits, self.targets = [], []
+        for i in range(spec.ring):
+            rl = []
+            for l in range(spec.layers):
+                r = sy.ring_rows(spec, l, i, self.cap, dev)
+                rl.append(LayerRows(r.q, r.k, r.v, r.g, r.beta))
+            self.rows.append(rl)
+            lg, tgt = sy.ring_logits(spec, i, self.cap, dev)
+            self.logits.append(lg)
+            self.targets.append(tgt.tolist())
+        self.ks = sy.k_table(spec, 100000 if spec.k_fixed is not None else spec.steps)
+        self.tok_h = torch.zeros(self.cap, dtype=torch.int32).pin_memory()
+        self.tok_d = torch.zeros(self.cap, dtype=torch.int32, device=dev)
+        self.step_no = 0
+        self.verified = 0
+        self.last_plan = None
+
+    def prepare(self, s):
+        """Host part of a step: plan, drafts, table upload."""
+        p = self.loop.plan_step(self.ks[s % self.ks.shape[0]].tolist())
+        ring = s % self.spec.ring
+        drafts = sy.step_drafts(self.spec, s, p.k, self.targets[ring])
+        toks = [t for dr in drafts for t in dr]
+        self.tok_h[:len(toks)] = torch.tensor(toks, dtype=torch.int32)
+        self.tok_d.copy_(self.tok_h, non_blocking=True)
+        self.loop.upload_tables()
+        self.last_plan = p
+        return ring, p
+
+    def step(self, ev=None):
+        s = self.step_no
+        ring, p = self.prepare(s)
+        vs, loop = self.vs, self.loop
+        vs.txn = (vs.txn + 1) & 0xFFFFFFFF
+        for l in range(self.spec.layers):
+            if ev is not None:
+                ev["verify"][0].append(torch.cuda.Event(enable_timing=True))
+                ev["verify"][0][-1].record()
+            vs.verify_layer(l, loop.B, loop.cu_rows, loop.src_slot, self.rows[ring][l])
+            if ev is not None:
+                ev["verify"][1].append(torch.cuda.Event(enable_timing=True))
+                ev["verify"][1][-1].record()
+        if ev is not None:
+            ev["accept"][0].append(torch.cuda.Event(enable_timing=True))
+            ev["accept"][0][-1].record()
+        vs.accept(loop.B, loop.cu_rows, self.logits[ring], self.tok_d)
+        if ev is not None:
+            ev["accept"][1].append(torch.cuda.Event(enable_timing=True))
+            ev["accept"][1][-1].record()
+            ev["commit"][0].append(torch.cuda.Event(enable_timing=True))
+            ev["commit"][0][-1].record()
+        vs.commit(loop.B, loop.cu_rows, loop.dst_slot)
+        if ev is not None:
+            ev["commit"][1].append(torch.cuda.Event(enable_timing=True))
+            ev["commit"][1][-1].record()
+        acc, bon, out = loop.readback()
+        n_ver = int(acc.sum().item()) + loop.B
+        loop.finish(acc)
+        self.step_no += 1
+        self.verified += n_ver
+        return n_ver, p
+
+    def step_bytes(self, p):
+        """Algorithmic bytes of verify (all layers) and commit for a plan."""
+        d = self.d
+        S = d.h_v * d.d_v * d.d_k * 4
+        rows = p.decode_rows
+        distinct_src = len(set(p.dec_src))
+        verify = self.spec.layers * (distinct_src * S + rows * S + rows * S_ROW_IO(d))
+        commit = self.spec.layers * p.n_decode * 2 * S
+        accept = rows * self.spec.vocab * 2
+        return verify, commit, accept
+
+
+def stage_e2e(b: Bench):
+    """Pinned host copies of the ring inputs and one device staging set."""
+    from speculative_decoding_hybrid_gb300.step import LayerRows
+    host, nbytes = [], 0
+    for i in range(b.spec.ring):
+        hl = []
+        for r in b.rows[i]:
+            t = [x.detach().to("cpu").pin_memory() for x in (r.q, r.k, r.v, r.g, r.beta)]
+            hl.append(t)
+        host.append((hl, b.logits[i].detach().to("cpu").pin_memory()))
+    stage_rows = [LayerRows(*(torch.empty_like(x) for x in (r.q, r.k, r.v, r.g, r.beta))) for r in b.rows[0]]
+    stage_logits = torch.empty_like(b.logits[0])
+    return host, stage_rows, stage_logits
+
+
+def run_e2e(b: Bench, host, stage_rows, stage_logits, steps, warmup):
+    """Same step through the public API, with every step's inputs copied from
+    pinned host memory and the results read back inside the timed region."""
+    spec = b.spec
+    saved_rows, saved_logits = b.rows, b.logits
+    b.rows = [stage_rows] * spec.ring
+    b.logits = [stage_logits] * spec.ring
+    h2d = 0
+
+    def one():
+        nonlocal h2d
+        ring = b.step_no % spec.ring
+        hl, hlog = host[ring]
+        moved = 0
+        for l in range(spec.layers):
+            dst = stage_rows[l]
+            for x, dt in zip(hl[l], (dst.q, dst.k, dst.v, dst.g, dst.beta)):
+                dt.copy_(x, non_blocking=True)
+                moved += x.numel() * x.element_size()
+        stage_logits.copy_(hlog, non_blocking=True)
+        moved += hlog.numel() * hlog.element_size()
+        n, p = b.step()
+        moved += (p.n_decode + 1) * 3 * 4 + b.cap * 4       # tables + tokens
+        return n, moved
+
+    try:
+        for _ in range(warmup):
+            one()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        tok = 0
+        for _ in range(steps):
+            n, moved = one()
+            tok += n
+            h2d += moved
+        torch.cuda.synchronize()
+        dt = time.perf_counter() - t0
+    finally:
+        b.rows, b.logits = saved_rows, saved_logits
+    d2h = (2 * spec.batch + b.cap) * 4
+    return tok / dt, h2d / steps, d2h
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle arm (baseline)
+# ---------------------------------------------------------------------------
+
+def oracle_sample_step(spec: sy.Spec, step: int, n_req: int, seed: int = 0):
+    """One step of the workload for n_req requests, run by the FP64 oracle:
+    planner model, recurrence over every layer and head with checkpoints,
+    greedy choice over the vocabulary, acceptance and commit.  Returns the
+    verified tokens."""
+    import oracle
+    d = spec.dims
+    K = spec.k_fixed if spec.k_fixed is not None else spec.k_max
+    pool = oracle.PoolModel(n_req)
+    reqs = []
+    for i in range(n_req):
+        _, s = pool.alloc()
+        reqs.append(oracle.Req(oracle.DECODE, K, cur_len=1, slot=s))
+    P = oracle.plan_transaction(reqs, n_req * (K + 1), n_req, spec.k_max, pool)
+    cu = P.dec_cu
+    R = cu[-1]
+    gen = sy.generator(sy.mix_seed(seed, 4242, step))
+    lg, tgt = sy.logits(gen, R, spec.vocab, spec.logit_std)
+    drafts = sy.step_drafts(spec, step, P.k, tgt.tolist())
+    toks = np.array([t for dr in drafts for t in dr], np.int32)
+    am = oracle.argmax_bf16(oracle.bf16_bits(lg))
+    res = oracle.greedy_accept(am, toks, np.array(cu), spec.vocab)
+    for l in range(spec.layers):
+        rows = sy.rows(gen, R, d)
+        S0 = sy.state(gen, (n_req, d.h_v, d.d_v, d.d_k))
+        units = []
+        for r in range(n_req):
+            a, b = cu[r], cu[r + 1]
+            units += oracle.head_units(rows.q[a:b], rows.k[a:b], rows.v[a:b], rows.g[a:b], rows.beta[a:b], S0[r])
+        S, o, ck = oracle.recurrent_units(units, want_ckpt=True)
+        for r in range(n_req):
+            j = int(res.accept_len[r])
+            _ = [ck[r * d.h_v + h][j] for h in range(d.h_v)]     # commit: the accepted checkpoint
+    return int(res.accept_len.sum()) + n_req
+
+
+def cpu_baseline(spec: sy.Spec, budget_s: float = 12.0, n_req: int = 16):
+    import oracle
+    t0 = time.perf_counter()
+    tok, steps = 0, 0
+    while steps == 0 or time.perf_counter() - t0 < budget_s:
+        tok += oracle_sample_step(spec, steps, n_req)
+        steps += 1
+    dt = time.perf_counter() - t0
+    return {"value": tok / dt, "unit": "verified tokens/s", "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": "%d steps x %d requests x %d layers of the %s workload (FP64 C oracle, OpenMP over "
+                      "(request, head); inputs drawn on the host with the same recipe)" %
+                      (steps, n_req, spec.layers, spec.name)}
+
+
+def run_reference(args, spec):
+    import oracle
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    n_req = min(4, spec.batch)
+    for w in range(args.warmup):
+        oracle_sample_step(spec, w, n_req)
+    t0 = time.perf_counter()
+    tok = 0
+    for s in range(args.steps):
+        tok += oracle_sample_step(spec, args.warmup + s, n_req)
+    dt = time.perf_counter() - t0
+    val = tok / dt
+    line = {"impl": "reference", "metric": "verified tokens/s", "value": val, "unit": "verified tokens/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000 * dt / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": args.workload, "desc": WORKLOAD_TEXT[args.workload],
+                       "per_step_sample": "%d of %d requests" % (n_req, spec.batch)},
+            "cpu_baseline": {"value": val, "unit": "verified tokens/s", "cores": oracle.num_threads(),
+                             "kind": "oracle", "sample": "each step: %d requests x %d layers of the %s workload"
+                                                         % (n_req, spec.layers, spec.name)},
+            "e2e": {"value": val, "unit": "verified tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=None)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="paged256", choices=sorted(WORKLOADS))
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args()
+    spec = WORKLOADS[args.workload]
+    if args.steps is None:
+        args.steps = min(spec.steps, 100)
+    if args.warmup < 3 and args.impl == "ours":
+        ap.error("at least 3 warm-up steps")
+    if args.impl == "reference":
+        run_reference(args, spec)
+        return
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local if world > 1 else 0)
+    torch.cuda.set_device(dev)
+
+    from speculative_decoding_hybrid_gb300 import build
+    build.build()
+    b = Bench(spec, dev, rank)
+    for _ in range(args.warmup):
+        b.step()
+    torch.cuda.synchronize()
+
+    ev = {"verify": ([], []), "accept": ([], []), "commit": ([], [])}
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(dev.index if world == 1 else local)
+    sampler.start()
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    start.record()
+    tok = 0
+    vbytes = cbytes = abytes = 0
+    for _ in range(args.steps):
+        n, p = b.step(ev)
+        tok += n
+        v, c, a = b.step_bytes(p)
+        vbytes += v
+        cbytes += c
+        abytes += a
+    end.record()
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    ms = start.elapsed_time(end)
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+        tt = torch.tensor([tok], device=dev, dtype=torch.float64)
+        dist.all_reduce(tt)
+        tok_all = float(tt.item())
+    else:
+        tok_all = tok
+
+    def avg_ms(name):
+        s, e = ev[name]
+        return sum(a.elapsed_time(bb) for a, bb in zip(s, e)) / max(len(s), 1)
+
+    v_ms, a_ms, c_ms = avg_ms("verify"), avg_ms("accept"), avg_ms("commit")
+    n_ver_launch = len(ev["verify"][0])
+    peak, peak_kind = load_peaks()
+    v_per_launch = vbytes / max(n_ver_launch, 1)
+    achieved = v_per_launch / (v_ms * 1e-3) / 1e9
+    vc_gbs = (vbytes + cbytes) / ((v_ms * n_ver_launch + c_ms * args.steps) * 1e-3) / 1e9
+    src = os.path.join(ROOT, "speculative_decoding_hybrid_gb300", "csrc", "gdn_recurrent.cu")
+    tr = TRAFFIC.get("gdn_verify")
+    traffic = tr["bytes_per_launch"] * (v_per_launch / tr["alg_bytes_per_launch"]) \
+        if tr and tr["src_sha"] == src_digest(src) and tr.get("workload") == args.workload else None
+
+    e2e = None
+    if not args.no_e2e:
+        host, srows, slog = stage_e2e(b)
+        val, h2d, d2h = run_e2e(b, host, srows, slog, args.e2e_steps, 3)
+        if world > 1:
+            t = torch.tensor([val], device=dev, dtype=torch.float64)
+            dist.all_reduce(t)
+            val = float(t.item())
+        e2e = {"value": val, "unit": "verified tokens/s", "h2d_bytes_per_step": int(h2d),
+               "d2h_bytes_per_step": int(d2h), "steps": args.e2e_steps}
+
+    if rank != 0:
+        if world > 1:
+            dist.barrier()
+            dist.destroy_process_group()
+        return
+    cpu = None
+    if not args.no_cpu_baseline and world == 1:
+        cpu = cpu_baseline(spec)
+    line = {
+        "metric": "verified tokens/s and GDN verify+commit HBM GB/s (% of GB300 peak)",
+        "value": tok_all / (ms * 1e-3),
+        "unit": "verified tokens/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms / args.steps,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": args.workload, "desc": WORKLOAD_TEXT[args.workload],
+                   "l2": "inputs larger than L2: state pool %.1f GiB, checkpoints %.1f GiB, ring of %d input sets" % (
+                       b.vs.pool.numel() * 4 / 2 ** 30, b.vs.ckpt.numel() * 4 / 2 ** 30, spec.ring),
+                   "parallelism": "replicas (requests sharded, no collective)" if world > 1 else "single GPU"},
+        "verify_commit_gbs": vc_gbs,
+        "verify_commit_frac": vc_gbs / peak,
+        "roofline": {"bound": "hbm", "kernel": "gdn_verify", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": traffic, "peak_source": peak_kind,
+                     "alg_bytes_per_launch": v_per_launch, "avg_launch_ms": v_ms},
+        "kernels_ms": {"gdn_verify": v_ms, "mtp_greedy_accept": a_ms, "gdn_commit": c_ms,
+                       "commit_gbs": cbytes / args.steps / (c_ms * 1e-3) / 1e9,
+                       "accept_gbs": abytes / args.steps / (a_ms * 1e-3) / 1e9},
+        "gpu_launches": args.steps * (spec.layers + 3),
+        "clocks": clocks,
+        "e2e": e2e,
+        "cpu_baseline": cpu,
+        "acceptance": {"verified_tokens": tok, "requests": spec.batch},
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,111 @@
+// Commit / rollback of every layer's state slot to its accepted checkpoint
+// (sm_103a).  "Run chained MTP drafting in the batch Engine", Correctness fix:
+// a rejected request must publish the checkpoint of its accepted row and
+// never one that the transaction did not write; RC4 evidence: rollback.
+//
+// One launch covers all (request, layer) pairs.  Each CTA copies one
+// contiguous 32 KB piece of a state (fp32 [h_v][d_v][d_k]) with 16-byte
+// streaming loads and stores, after checking the checkpoint tag written by
+// gdn_verify: the tag must carry this transaction id and a row count larger
+// than the accept length.  HBM roofline: read + write of S_bytes per pair.
+#include "common.cuh"
+
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kChunkFloats = 8192;  // 32 KB per CTA
+constexpr int kUnroll = kChunkFloats / 4 / kThreads;
+
+struct CommitArgs {
+    int32_t B, L, row_capacity, num_slots, chunks;
+    const int32_t *cu_rows, *accept_len, *dst_slot;
+    const float *ckpt;
+    int64_t ckpt_layer_stride, s_elems, slot_stride, layer_stride;
+    const uint64_t *tag;
+    uint32_t txn;
+    float *pool;
+    uint32_t *status;
+};
+
+__global__ void __launch_bounds__(kThreads) gdn_commit_kernel(const CommitArgs a) {
+    const long long idx = blockIdx.x;
+    const int c = int(idx % a.chunks);
+    const long long rl = idx / a.chunks;
+    const int r = int(rl % a.B);
+    const int l = int(rl / a.B);
+    if (a.status && (*reinterpret_cast<volatile uint32_t *>(a.status) & GDN_DEV_TIMEOUT)) return;
+    const uint64_t tag = a.tag[int64_t(l) * a.B + r];
+    const int j = a.accept_len[r];
+    const int dst = a.dst_slot[r];
+    const int t0 = a.cu_rows[r];
+    const uint32_t n = uint32_t(tag & 0xffffffffull);
+    uint32_t bad = 0;
+    if (uint32_t(tag >> 32) != a.txn || n == 0)
+        bad = GDN_DEV_CKPT_UNWRITTEN;
+    else if (j < 0 || uint32_t(j) >= n)
+        bad = GDN_DEV_ACCEPT_BAD;
+    else if (dst < 0 || dst >= a.num_slots)
+        bad = GDN_DEV_SLOT_OOR;
+    else if (t0 < 0 || int64_t(t0) + j >= a.row_capacity)
+        bad = GDN_DEV_ROWS_BAD;
+    if (bad) {
+        if (c == 0 && threadIdx.x == 0) gdn::set_status(a.status, bad);
+        return;
+    }
+    const int64_t off = int64_t(c) * kChunkFloats;
+    const int64_t nf = min(int64_t(kChunkFloats), a.s_elems - off);
+    const float4 *src = reinterpret_cast<const float4 *>(a.ckpt + int64_t(l) * a.ckpt_layer_stride +
+                                                         (int64_t(t0) + j) * a.s_elems + off);
+    float4 *dp = reinterpret_cast<float4 *>(a.pool + int64_t(dst) * a.slot_stride + int64_t(l) * a.layer_stride + off);
+    const int n4 = int(nf / 4);
+    if (n4 == kChunkFloats / 4) {
+        float4 buf[kUnroll];
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) buf[u] = __ldcs(src + threadIdx.x + u * kThreads);
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) __stcs(dp + threadIdx.x + u * kThreads, buf[u]);
+    } else {
+        for (int i = threadIdx.x; i < n4; i += kThreads) __stcs(dp + i, __ldcs(src + i));
+    }
+}
+
+}  // namespace
+
+extern "C" int gdn_commit(const gdn_dims *dims, int32_t B, int32_t num_layers, int32_t row_capacity,
+                          const int32_t *cu_rows, const int32_t *accept_len, const float *ckpt,
+                          int64_t ckpt_layer_stride, const uint64_t *ckpt_tag, uint32_t txn, float *pool,
+                          int64_t slot_stride, int64_t layer_stride, int32_t num_slots, const int32_t *dst_slot,
+                          uint32_t *dev_status, void *stream) {
+    if (!dims) return GDN_ERR_NULL;
+    if (!gdn_host::dims_ok(dims)) return GDN_ERR_SHAPE;
+    if (B < 0 || num_layers < 0 || row_capacity < 0 || num_slots <= 0) return GDN_ERR_ARG;
+    if (B == 0 || num_layers == 0) return GDN_OK;
+    if (!cu_rows || !accept_len || !ckpt || !ckpt_tag || !pool || !dst_slot) return GDN_ERR_NULL;
+    const int64_t se = int64_t(dims->h_v) * dims->d_v * dims->d_k;
+    if (layer_stride < se || slot_stride < layer_stride * num_layers) return GDN_ERR_ARG;
+    if (ckpt_layer_stride < se * row_capacity) return GDN_ERR_ARG;
+    if ((slot_stride | layer_stride | ckpt_layer_stride) % 4 != 0) return GDN_ERR_ARG;
+    if (!gdn_host::aligned16(ckpt) || !gdn_host::aligned16(pool)) return GDN_ERR_ARG;
+    CommitArgs a{};
+    a.B = B;
+    a.L = num_layers;
+    a.row_capacity = row_capacity;
+    a.num_slots = num_slots;
+    a.chunks = int((se + kChunkFloats - 1) / kChunkFloats);
+    a.cu_rows = cu_rows;
+    a.accept_len = accept_len;
+    a.dst_slot = dst_slot;
+    a.ckpt = ckpt;
+    a.ckpt_layer_stride = ckpt_layer_stride;
+    a.s_elems = se;
+    a.slot_stride = slot_stride;
+    a.layer_stride = layer_stride;
+    a.tag = ckpt_tag;
+    a.txn = txn;
+    a.pool = pool;
+    a.status = dev_status;
+    const long long grid = (long long)B * num_layers * a.chunks;
+    if (grid > 0x7fffffffLL) return GDN_ERR_ARG;
+    gdn_commit_kernel<<<unsigned(grid), kThreads, 0, static_cast<cudaStream_t>(stream)>>>(a);
+    return gdn_host::launch_status(cudaGetLastError());
+}

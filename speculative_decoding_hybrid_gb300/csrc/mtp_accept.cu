@@ -1,0 +1,259 @@
+// Greedy target choice over the vocabulary and draft acceptance (sm_103a).
+//
+// Operation ("Native three-step MTP", Apply...: greedy requests; "Run chained
+// MTP drafting in the batch Engine", Summary: device-resident draft ids and
+// cumulative telemetry; Quality follow-up: verification-row selection and
+// per-request bonus):
+//   argmax[t]     = first index of the largest bf16 logit of row t
+//   accept_len[r] = longest j with tokens[t0+i] == argmax[t0+i-1], i = 1..j
+//   bonus[r]      = argmax[t0+j]
+//
+// Two launches.  (1) argmax_partial: rows x splits CTAs stream the logits
+// with 16-byte loads and reduce a 64-bit key per split,
+//     key = order17(value) << 32 | (0xffffffff - index),
+// whose unsigned maximum is the largest value with the lowest index (order17
+// maps bf16 to an order-preserving integer, -0 to +0, and every NaN above
+// +inf so that the first NaN wins).  (2) accept_finalize: one warp per
+// request reduces its rows' partial keys, applies the acceptance rule, writes
+// the emitted tokens and adds to the telemetry counters.
+// HBM roofline: vocab x 2 bytes per row read once.
+#include "common.cuh"
+
+namespace {
+
+constexpr int kArgThreads = 256;
+constexpr int kMaxSplits = 64;
+constexpr int kMinSplitElems = 2048;
+
+__device__ __forceinline__ uint32_t order17(uint32_t bits) {
+    uint32_t m = bits & 0x7fffu;
+    if (m > 0x7f80u) return 0x10000u;            // NaN
+    if (m == 0) return 0x8000u;                  // +0 and -0
+    return (bits & 0x8000u) ? (0x7fffu - m) : (0x8000u + m);
+}
+
+__device__ __forceinline__ unsigned long long make_key(uint32_t bits, uint32_t idx) {
+    return (static_cast<unsigned long long>(order17(bits)) << 32) | (0xffffffffu - idx);
+}
+
+__device__ __forceinline__ unsigned long long umax64(unsigned long long a, unsigned long long b) {
+    return a > b ? a : b;
+}
+
+__device__ __forceinline__ unsigned long long warp_max64(unsigned long long x) {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) x = umax64(x, __shfl_xor_sync(0xffffffffu, x, off));
+    return x;
+}
+
+struct ArgArgs {
+    const int32_t *cu_rows;
+    int32_t B, row_capacity, splits;
+    const uint16_t *logits;
+    int64_t vocab, row_stride, chunk;
+    int vec;  // 16-byte loads allowed
+    unsigned long long *partial;
+};
+
+__global__ void __launch_bounds__(kArgThreads) argmax_partial_kernel(const ArgArgs a) {
+    const int split = blockIdx.x;
+    const int row = blockIdx.y;
+    int total = a.cu_rows[a.B];
+    if (total > a.row_capacity || total < 0) total = a.row_capacity;
+    if (row >= total) return;
+    const int64_t c0 = int64_t(split) * a.chunk;
+    const int64_t c1 = min(a.vocab, c0 + a.chunk);
+    const uint16_t *rp = a.logits + int64_t(row) * a.row_stride;
+    unsigned long long best = 0ull;
+    if (c1 <= c0) {
+        // empty range: nothing to scan
+    } else if (a.vec) {
+        // c0 and chunk are multiples of 8 elements: whole 16-byte vectors.
+        const uint4 *vp = reinterpret_cast<const uint4 *>(rp + c0);
+        const int64_t nvec = (c1 - c0) / 8;
+        int64_t i = threadIdx.x;
+        for (; i + 3 * kArgThreads < nvec; i += 4 * kArgThreads) {
+            uint4 w[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) w[u] = __ldcs(vp + i + u * kArgThreads);
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const uint32_t base = uint32_t(c0 + (i + u * kArgThreads) * 8);
+                const uint32_t ws[4] = {w[u].x, w[u].y, w[u].z, w[u].w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    best = umax64(best, make_key(ws[e] & 0xffffu, base + 2 * e));
+                    best = umax64(best, make_key(ws[e] >> 16, base + 2 * e + 1));
+                }
+            }
+        }
+        for (; i < nvec; i += kArgThreads) {
+            const uint4 w = __ldcs(vp + i);
+            const uint32_t base = uint32_t(c0 + i * 8);
+            const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                best = umax64(best, make_key(ws[e] & 0xffffu, base + 2 * e));
+                best = umax64(best, make_key(ws[e] >> 16, base + 2 * e + 1));
+            }
+        }
+        // tail (vocab not a multiple of 8)
+        for (int64_t j = c0 + nvec * 8 + threadIdx.x; j < c1; j += kArgThreads)
+            best = umax64(best, make_key(rp[j], uint32_t(j)));
+    } else {
+        for (int64_t j = c0 + threadIdx.x; j < c1; j += kArgThreads) best = umax64(best, make_key(rp[j], uint32_t(j)));
+    }
+    __shared__ unsigned long long red[kArgThreads / 32];
+    best = warp_max64(best);
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = best;
+    __syncthreads();
+    if (threadIdx.x < 32) {
+        unsigned long long x = threadIdx.x < kArgThreads / 32 ? red[threadIdx.x] : 0ull;
+        x = warp_max64(x);
+        if (threadIdx.x == 0) a.partial[int64_t(row) * a.splits + split] = x;
+    }
+}
+
+struct AccArgs {
+    const int32_t *cu_rows;
+    int32_t B, row_capacity, splits;
+    int64_t vocab;
+    const unsigned long long *partial;
+    const int32_t *tokens;
+    int32_t *argmax, *accept_len, *bonus, *out_tokens;
+    mtp_stats *stats;
+    uint32_t *status;
+};
+
+constexpr int kAccWarps = 4;
+
+__global__ void __launch_bounds__(kAccWarps * 32) accept_finalize_kernel(const AccArgs a) {
+    const int lane = threadIdx.x & 31;
+    const int r = blockIdx.x * kAccWarps + (threadIdx.x >> 5);
+    if (r >= a.B) return;
+    if (r == 0 && lane == 0 && a.stats) atomicAdd(reinterpret_cast<unsigned long long *>(&a.stats->steps), 1ull);
+    const int t0 = a.cu_rows[r];
+    const int t1 = a.cu_rows[r + 1];
+    const int n = t1 - t0;
+    // rows past cu_rows[B] got no partial maxima (non-monotone table)
+    const int total = a.cu_rows[a.B];
+    if (t0 < 0 || n < 1 || n > GDN_MAX_ROWS || t1 > a.row_capacity || t1 > total) {
+        if (lane == 0) {
+            gdn::set_status(a.status, GDN_DEV_ROWS_BAD);
+            a.accept_len[r] = -1;
+            a.bonus[r] = -1;
+        }
+        return;
+    }
+    int am[GDN_MAX_ROWS];
+#pragma unroll
+    for (int m = 0; m < GDN_MAX_ROWS; ++m) {
+        if (m < n) {
+            unsigned long long x = 0ull;
+            for (int s = lane; s < a.splits; s += 32) x = umax64(x, a.partial[int64_t(t0 + m) * a.splits + s]);
+            x = warp_max64(x);
+            am[m] = x == 0ull ? -1 : int(0xffffffffu - uint32_t(x & 0xffffffffull));
+        }
+    }
+    if (lane != 0) return;
+    const int K = n - 1;
+    bool oor = false;
+    for (int i = 1; i <= K; ++i) {
+        const int d = a.tokens[t0 + i];
+        if (d < 0 || int64_t(d) >= a.vocab) oor = true;
+    }
+    int j = 0;
+    while (j < K && a.tokens[t0 + j + 1] == am[j]) ++j;
+    for (int m = 0; m < n; ++m) {
+        a.argmax[t0 + m] = am[m];
+        a.out_tokens[t0 + m] = m <= j ? am[m] : -1;
+    }
+    a.accept_len[r] = j;
+    a.bonus[r] = am[j];
+    if (oor) gdn::set_status(a.status, GDN_DEV_TOKEN_OOR);
+    if (a.stats) {
+        atomicAdd(reinterpret_cast<unsigned long long *>(&a.stats->proposed), (unsigned long long)K);
+        atomicAdd(reinterpret_cast<unsigned long long *>(&a.stats->evaluated),
+                  (unsigned long long)(j + 1 < K ? j + 1 : K));
+        atomicAdd(reinterpret_cast<unsigned long long *>(&a.stats->accepted), (unsigned long long)j);
+        atomicAdd(reinterpret_cast<unsigned long long *>(&a.stats->emitted), (unsigned long long)(j + 1));
+    }
+}
+
+int accept_splits(int32_t rows, int64_t vocab) {
+    int64_t s = (1024 + int64_t(rows > 0 ? rows : 1) - 1) / int64_t(rows > 0 ? rows : 1);
+    if (s > kMaxSplits) s = kMaxSplits;
+    int64_t smax = vocab / kMinSplitElems;
+    if (smax < 1) smax = 1;
+    if (s > smax) s = smax;
+    if (s < 1) s = 1;
+    return int(s);
+}
+
+}  // namespace
+
+int gdn_accept_launch(int32_t B, int32_t row_capacity, const int32_t *cu_rows, const gdn_bf16 *logits,
+                      int64_t vocab, int64_t row_stride, const int32_t *tokens, int32_t *argmax,
+                      int32_t *accept_len, int32_t *bonus, int32_t *out_tokens, mtp_stats *stats,
+                      void *workspace, size_t workspace_bytes, uint32_t *dev_status, cudaStream_t st);
+
+extern "C" size_t mtp_accept_workspace_bytes(int32_t row_capacity, int64_t vocab) {
+    if (row_capacity <= 0 || vocab <= 0) return 0;
+    return size_t(row_capacity) * size_t(accept_splits(row_capacity, vocab)) * sizeof(unsigned long long);
+}
+
+int gdn_accept_launch(int32_t B, int32_t row_capacity, const int32_t *cu_rows, const gdn_bf16 *logits,
+                      int64_t vocab, int64_t row_stride, const int32_t *tokens, int32_t *argmax,
+                      int32_t *accept_len, int32_t *bonus, int32_t *out_tokens, mtp_stats *stats,
+                      void *workspace, size_t workspace_bytes, uint32_t *dev_status, cudaStream_t st) {
+    if (B < 0 || row_capacity < 0 || vocab <= 0 || row_stride < vocab || vocab > 0x7fffffffLL) return GDN_ERR_ARG;
+    if (!cu_rows || !logits || !tokens || !argmax || !accept_len || !bonus || !out_tokens) return GDN_ERR_NULL;
+    if (B == 0) return GDN_OK;
+    const size_t need = mtp_accept_workspace_bytes(row_capacity, vocab);
+    if (row_capacity > 0 && (!workspace || workspace_bytes < need)) return GDN_ERR_WORKSPACE;
+    if ((reinterpret_cast<uintptr_t>(workspace) & 7u) != 0) return GDN_ERR_ARG;
+    const int splits = accept_splits(row_capacity, vocab);
+    if (row_capacity > 0) {
+        ArgArgs aa{};
+        aa.cu_rows = cu_rows;
+        aa.B = B;
+        aa.row_capacity = row_capacity;
+        aa.splits = splits;
+        aa.logits = logits;
+        aa.vocab = vocab;
+        aa.row_stride = row_stride;
+        int64_t chunk = (vocab + splits - 1) / splits;
+        chunk = (chunk + 7) / 8 * 8;
+        aa.chunk = chunk;
+        aa.vec = (gdn_host::aligned16(logits) && (row_stride % 8) == 0) ? 1 : 0;
+        aa.partial = static_cast<unsigned long long *>(workspace);
+        if (row_capacity > 65535) return GDN_ERR_ARG;
+        argmax_partial_kernel<<<dim3(splits, row_capacity), kArgThreads, 0, st>>>(aa);
+        if (cudaGetLastError() != cudaSuccess) return GDN_ERR_CUDA;
+    }
+    AccArgs ac{};
+    ac.cu_rows = cu_rows;
+    ac.B = B;
+    ac.row_capacity = row_capacity;
+    ac.splits = splits;
+    ac.vocab = vocab;
+    ac.partial = static_cast<const unsigned long long *>(workspace);
+    ac.tokens = tokens;
+    ac.argmax = argmax;
+    ac.accept_len = accept_len;
+    ac.bonus = bonus;
+    ac.out_tokens = out_tokens;
+    ac.stats = stats;
+    ac.status = dev_status;
+    accept_finalize_kernel<<<(B + kAccWarps - 1) / kAccWarps, kAccWarps * 32, 0, st>>>(ac);
+    return gdn_host::launch_status(cudaGetLastError());
+}
+
+extern "C" int mtp_greedy_accept(int32_t B, int32_t row_capacity, const int32_t *cu_rows, const gdn_bf16 *logits,
+                                 int64_t vocab, int64_t row_stride, const int32_t *tokens, int32_t *argmax,
+                                 int32_t *accept_len, int32_t *bonus, int32_t *out_tokens, mtp_stats *stats,
+                                 void *workspace, size_t workspace_bytes, uint32_t *dev_status, void *stream) {
+    return gdn_accept_launch(B, row_capacity, cu_rows, logits, vocab, row_stride, tokens, argmax, accept_len,
+                             bonus, out_tokens, stats, workspace, workspace_bytes, dev_status,
+                             static_cast<cudaStream_t>(stream));
+}

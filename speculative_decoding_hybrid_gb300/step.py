@@ -1,0 +1,167 @@
+"""Per-transaction call sequence of K-draft verification, over the C ABI.
+
+``VerifyStep`` owns the device buffers of one verification loop (state pool,
+per-row checkpoints and their tags, outputs, accept workspace, telemetry,
+status word) and issues, on one stream:
+
+    gdn_verify            x num_layers   (rows -> checkpoints, o)
+    mtp_greedy_accept     x 1            (argmax, accept length, bonus, tokens)
+    gdn_commit            x 1            (every layer's slot <- accepted checkpoint)
+
+Layer inputs (q, k, v, g, beta of the packed rows) and the logits are the
+caller's device tensors.  All arithmetic happens in the library's kernels.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+from typing import List, Optional, Sequence
+
+import torch
+
+from . import binding as gs
+
+
+@dataclass
+class LayerRows:
+    q: torch.Tensor      # bf16 [R, h_qk, d_k]
+    k: torch.Tensor      # bf16 [R, h_qk, d_k]
+    v: torch.Tensor      # bf16 [R, h_v, d_v]
+    g: torch.Tensor      # fp32 [R, h_v]
+    beta: torch.Tensor   # fp32 [R, h_v]
+
+
+class VerifyStep:
+    def __init__(self, dims: gs.gdn_dims, num_layers: int, num_slots: int, row_capacity: int, max_batch: int,
+                 vocab: int, device="cuda", pool: Optional[torch.Tensor] = None):
+        self.d = dims
+        self.L = num_layers
+        self.num_slots = num_slots
+        self.cap = row_capacity
+        self.max_batch = max_batch
+        self.vocab = vocab
+        dev = torch.device(device)
+        self.dev = dev
+        h_v, dv, dk = dims.h_v, dims.d_v, dims.d_k
+        if pool is None:
+            pool = torch.zeros((num_slots, num_layers, h_v, dv, dk), dtype=torch.float32, device=dev)
+        assert pool.shape == (num_slots, num_layers, h_v, dv, dk) and pool.is_contiguous()
+        self.pool = pool
+        self.ckpt = torch.empty((num_layers, row_capacity, h_v, dv, dk), dtype=torch.float32, device=dev)
+        self.tags = torch.zeros((num_layers, max_batch), dtype=torch.int64, device=dev)
+        self.o = torch.empty((num_layers, row_capacity, h_v, dv), dtype=torch.bfloat16, device=dev)
+        self.argmax = torch.full((row_capacity,), -1, dtype=torch.int32, device=dev)
+        self.accept_len = torch.full((max_batch,), -1, dtype=torch.int32, device=dev)
+        self.bonus = torch.full((max_batch,), -1, dtype=torch.int32, device=dev)
+        self.out_tokens = torch.full((row_capacity,), -1, dtype=torch.int32, device=dev)
+        self.ws_bytes = gs.mtp_accept_workspace_bytes(row_capacity, vocab)
+        self.workspace = torch.empty((max(self.ws_bytes, 8),), dtype=torch.uint8, device=dev)
+        self.stats = torch.zeros((5,), dtype=torch.int64, device=dev)
+        self.status = torch.zeros((1,), dtype=torch.int32, device=dev)
+        self.slot_stride = pool.stride(0)
+        self.layer_stride = pool.stride(1)
+        self.ckpt_layer_stride = self.ckpt.stride(0)
+        self.txn = 0
+
+    def pool_layer(self, l: int) -> int:
+        return self.pool.data_ptr() + 4 * l * self.layer_stride
+
+    def verify_layer(self, l: int, B: int, cu_rows: torch.Tensor, src_slot: torch.Tensor, rows: LayerRows,
+                     stream=None):
+        gs.gdn_verify(self.d, B, self.cap, cu_rows, rows.q, rows.k, rows.v, rows.g, rows.beta, self.pool_layer(l),
+                      self.slot_stride, self.num_slots, src_slot, self.ckpt[l], self.tags[l], self.txn, self.o[l],
+                      self.status, stream)
+
+    def accept(self, B: int, cu_rows: torch.Tensor, logits: torch.Tensor, tokens: torch.Tensor, stream=None):
+        gs.mtp_greedy_accept(B, self.cap, cu_rows, logits, self.vocab, logits.stride(0), tokens, self.argmax,
+                             self.accept_len, self.bonus, self.out_tokens, self.stats, self.workspace,
+                             self.ws_bytes, self.status, stream)
+
+    def commit(self, B: int, cu_rows: torch.Tensor, dst_slot: torch.Tensor, stream=None):
+        gs.gdn_commit(self.d, B, self.L, self.cap, cu_rows, self.accept_len, self.ckpt, self.ckpt_layer_stride,
+                      self.tags, self.txn, self.pool, self.slot_stride, self.layer_stride, self.num_slots, dst_slot,
+                      self.status, stream)
+
+    def run(self, B: int, cu_rows: torch.Tensor, src_slot: torch.Tensor, dst_slot: torch.Tensor,
+            layer_rows: Sequence[LayerRows], logits: torch.Tensor, tokens: torch.Tensor, stream=None):
+        """One transaction: verify every layer, accept, commit.  Asynchronous."""
+        self.txn = (self.txn + 1) & 0xFFFFFFFF
+        for l in range(self.L):
+            self.verify_layer(l, B, cu_rows, src_slot, layer_rows[l], stream)
+        self.accept(B, cu_rows, logits, tokens, stream)
+        self.commit(B, cu_rows, dst_slot, stream)
+
+
+class DecodeLoop:
+    """Decode-only transactions for a fixed set of requests.
+
+    Per step: the host planner (``plan_transaction``) grants drafts, packs the
+    rows and picks destination slots (copy-on-write for shared slots); the
+    tables go to the device; ``VerifyStep.run`` verifies, accepts and commits;
+    one device-to-host read brings back accept lengths, bonus and emitted
+    tokens; the pool then releases the slots that requests moved away from.
+    """
+
+    def __init__(self, vs: VerifyStep, slots: Sequence[int], pool: "gs.Pool", k_max: int = 3,
+                 max_len: int = 1 << 30, cur_len: int = 1):
+        self.vs = vs
+        self.B = len(slots)
+        self.slot = list(slots)
+        self.cur_len = [cur_len] * self.B
+        self.max_len = max_len
+        self.pool = pool
+        self.plan = gs.Plan(self.B)
+        self.lim = gs.gdn_plan_limits(vs.cap, self.B, k_max)
+        dev = vs.dev
+        self.h_tab = torch.zeros((3, self.B + 1), dtype=torch.int32).pin_memory()
+        self.d_tab = torch.zeros((3, self.B + 1), dtype=torch.int32, device=dev)
+        self.h_out = torch.zeros((2 * self.B + vs.cap,), dtype=torch.int32).pin_memory()
+
+    def plan_step(self, k_draft: Sequence[int]):
+        reqs = gs.make_reqs([(gs.REQ_DECODE, int(k_draft[i]), 0, self.cur_len[i], self.max_len, self.slot[i])
+                             for i in range(self.B)])
+        st = gs.plan_transaction(reqs, self.B, self.lim, self.pool, self.plan)
+        if st != gs.GDN_OK:
+            raise gs.GdnError("plan_transaction", st)
+        p = self.plan
+        if p.n_decode != self.B:
+            raise RuntimeError("row budget too small for the batch: %d of %d requests selected" % (p.n_decode, self.B))
+        self.h_tab[0, :self.B + 1] = torch.tensor(p.dec_cu, dtype=torch.int32)
+        self.h_tab[1, :self.B] = torch.tensor(p.dec_src, dtype=torch.int32)
+        self.h_tab[2, :self.B] = torch.tensor(p.dec_dst, dtype=torch.int32)
+        return p
+
+    def upload_tables(self, stream=None):
+        self.d_tab.copy_(self.h_tab, non_blocking=True)
+
+    @property
+    def cu_rows(self):
+        return self.d_tab[0]
+
+    @property
+    def src_slot(self):
+        return self.d_tab[1, :self.B]
+
+    @property
+    def dst_slot(self):
+        return self.d_tab[2, :self.B]
+
+    def run(self, layer_rows, logits, tokens, stream=None):
+        self.vs.run(self.B, self.cu_rows, self.src_slot, self.dst_slot, layer_rows, logits, tokens, stream)
+
+    def readback(self):
+        """The step's one device-to-host read: accept_len, bonus, emitted tokens."""
+        B, cap = self.B, self.vs.cap
+        self.h_out[:B].copy_(self.vs.accept_len[:B], non_blocking=True)
+        self.h_out[B:2 * B].copy_(self.vs.bonus[:B], non_blocking=True)
+        self.h_out[2 * B:].copy_(self.vs.out_tokens, non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+        return self.h_out[:B], self.h_out[B:2 * B], self.h_out[2 * B:]
+
+    def finish(self, accept_len):
+        st = gs.gdn_pool_apply(self.pool, self.plan, self.B)
+        if st != gs.GDN_OK:
+            raise gs.GdnError("gdn_pool_apply", st)
+        dst = self.plan.dst
+        for i in range(self.B):
+            self.slot[i] = dst[i]
+            self.cur_len[i] += int(accept_len[i]) + 1
