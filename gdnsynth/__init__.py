@@ -22,7 +22,7 @@ Recipe (one line per tensor; all draws from a seeded ``torch.Generator``):
   is ``(target + 1 + r) mod V`` with r uniform in [0, V-2]; drafts after the
   first miss are uniform in [0, V).
 
-Sizes and seeds for the five workloads live in :func:`workload`.
+Sizes and seeds of the workloads live in ``SPECS`` and :func:`prefill_lengths`.
 """
 from __future__ import annotations
 
@@ -87,43 +87,50 @@ class Rows:
         return Rows(*(t.to(device) for t in (self.q, self.k, self.v, self.g, self.beta)))
 
 
-def _unit_bf16(gen, shape, device):
-    x = torch.randn(shape, generator=gen, device=device, dtype=torch.float32)
+# Every draw happens on the generator's own device (so a seed gives the same
+# numbers wherever the result is asked for) and is then moved to ``device``.
+
+def _unit_bf16(gen, shape):
+    x = torch.randn(shape, generator=gen, device=gen.device, dtype=torch.float32)
     if x.numel():
         x = x / x.norm(dim=-1, keepdim=True)
     return x.to(torch.bfloat16)
 
 
 def rows(gen, n: int, dims: Dims, device="cpu") -> Rows:
-    q = _unit_bf16(gen, (n, dims.h_qk, dims.d_k), device)
-    k = _unit_bf16(gen, (n, dims.h_qk, dims.d_k), device)
-    v = torch.randn((n, dims.h_v, dims.d_v), generator=gen, device=device,
-                    dtype=torch.float32).to(torch.bfloat16)
-    xg = torch.randn((n, dims.h_v), generator=gen, device=device, dtype=torch.float32) + 2.0
+    gd = gen.device
+    q = _unit_bf16(gen, (n, dims.h_qk, dims.d_k))
+    k = _unit_bf16(gen, (n, dims.h_qk, dims.d_k))
+    v = torch.randn((n, dims.h_v, dims.d_v), generator=gen, device=gd, dtype=torch.float32).to(torch.bfloat16)
+    xg = torch.randn((n, dims.h_v), generator=gen, device=gd, dtype=torch.float32) + 2.0
     g = torch.nn.functional.logsigmoid(xg)
-    xb = torch.randn((n, dims.h_v), generator=gen, device=device, dtype=torch.float32)
+    xb = torch.randn((n, dims.h_v), generator=gen, device=gd, dtype=torch.float32)
     beta = torch.sigmoid(xb)
-    return Rows(q.contiguous(), k.contiguous(), v.contiguous(), g.contiguous(), beta.contiguous())
+    return Rows(*(t.to(device).contiguous() for t in (q, k, v, g, beta)))
 
 
 def state(gen, shape, device="cpu", std: float = 0.1, out: Optional[torch.Tensor] = None):
-    """fp32 N(0, std^2) state; ``shape`` ends in (h_v, d_v, d_k)."""
+    """fp32 N(0, std^2) state; ``shape`` ends in (h_v, d_v, d_k).  With ``out``
+    the draw is written into it (it must live on the generator's device)."""
     if out is None:
-        out = torch.empty(shape, dtype=torch.float32, device=device)
+        x = torch.empty(shape, dtype=torch.float32, device=gen.device)
+        x.normal_(0.0, std, generator=gen)
+        return x.to(device)
     out.normal_(0.0, std, generator=gen)
     return out
 
 
 def logits(gen, n: int, vocab: int, std: float, device="cpu"):
     """bf16 logits [n, vocab] and the planted target id per row (int64)."""
-    lg = torch.empty((n, vocab), dtype=torch.float32, device=device)
+    gd = gen.device
+    lg = torch.empty((n, vocab), dtype=torch.float32, device=gd)
     if n:
         lg.normal_(0.0, std, generator=gen)
     lg = lg.to(torch.bfloat16)
-    tgt = torch.randint(0, vocab, (n,), generator=gen, device=device, dtype=torch.int64)
+    tgt = torch.randint(0, vocab, (n,), generator=gen, device=gd, dtype=torch.int64)
     if n:
-        lg[torch.arange(n, device=device), tgt] = TARGET_LOGIT
-    return lg, tgt
+        lg[torch.arange(n, device=gd), tgt] = TARGET_LOGIT
+    return lg.to(device), tgt.to(device)
 
 
 def drafts(gen_cpu, targets: List[int], ks: List[int], vocab: int, p_accept: float,
@@ -270,5 +277,5 @@ def prefill_inputs(lengths: List[int], dims: Dims, seed: int = 3, device="cpu"):
     s0 = torch.zeros((len(lengths), dims.h_v, dims.d_v, dims.d_k), dtype=torch.float32, device=device)
     half = len(lengths) // 2
     if len(lengths) - half:
-        state(generator(mix_seed(seed, 809), device), s0[half:].shape, device, 0.1, s0[half:])
+        s0[half:] = state(generator(mix_seed(seed, 809), device), s0[half:].shape, device, 0.1)
     return r, torch.tensor(cu, dtype=torch.int32), s0

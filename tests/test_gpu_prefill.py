@@ -1,0 +1,205 @@
+"""GPU parity of gdn_chunked_prefill against the FP64 token-by-token oracle,
+and the mixed prefill + draft transaction (deferral, publication order)."""
+import numpy as np
+import pytest
+import torch
+
+import gdnsynth as sy
+import oracle
+from gpu_util import build_lib, out_err, state_err
+
+pytestmark = pytest.mark.gpu
+
+CHUNK_STATE_RTOL = 5e-3   # ||S_chunk - S_rec||_F / ||S_rec||_F per (sequence, head)
+
+
+@pytest.fixture(scope="module")
+def gs(cuda_dev):
+    build_lib()
+    from speculative_decoding_hybrid_gb300 import binding
+    return binding
+
+
+def run_prefill(gs, dev, dims, lengths, src, dst, pool, seed=3, cap=None):
+    rows, cu, s0 = sy.prefill_inputs(lengths, dims, seed=seed)
+    R = int(cu[-1])
+    cap = R if cap is None else cap
+    d = gs.dims(dims.h_qk, dims.h_v, dims.d_k, dims.d_v)
+    ws_bytes = gs.gdn_prefill_workspace_bytes(d, len(lengths), cap)
+    ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
+    r = rows.to(dev)
+    o = torch.full((max(cap, 1), dims.h_v, dims.d_v), float("nan"), dtype=torch.bfloat16, device=dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    cu_d = cu.to(dev)
+    gs.gdn_chunked_prefill(d, len(lengths), cap, cu_d, max(lengths) if lengths else 0, r.q, r.k, r.v, r.g, r.beta,
+                           pool, pool.stride(0), pool.shape[0], torch.tensor(src, dtype=torch.int32, device=dev),
+                           torch.tensor(dst, dtype=torch.int32, device=dev), o, 64, ws, ws_bytes, st)
+    torch.cuda.synchronize()
+    return rows, cu, o, int(st.item())
+
+
+def check_sequences(rows, cu, o, S0s, finals, lengths):
+    worst_s, worst_o = 0.0, 0.0
+    units = []
+    for i, L in enumerate(lengths):
+        a, b = int(cu[i]), int(cu[i + 1])
+        units += oracle.head_units(rows.q[a:b], rows.k[a:b], rows.v[a:b], rows.g[a:b], rows.beta[a:b], S0s[i])
+    H = rows.v.shape[1]
+    S, o_list, _ = oracle.recurrent_units(units)
+    o_cpu = o.cpu()
+    for i, L in enumerate(lengths):
+        a, b = int(cu[i]), int(cu[i + 1])
+        ref = S[i * H:(i + 1) * H]
+        got = finals[i].astype(np.float64)
+        for h in range(H):
+            rel = np.linalg.norm(got[h] - ref[h]) / max(np.linalg.norm(ref[h]), 1e-30)
+            worst_s = max(worst_s, rel)
+        if L:
+            o_ref = np.stack(o_list[i * H:(i + 1) * H], axis=1)
+            worst_o = max(worst_o, out_err(o_cpu[a:b], o_ref))
+    return worst_s, worst_o
+
+
+@pytest.mark.parametrize("lengths", [[1, 63, 64, 200], [129], [0, 5, 64, 65]])
+def test_prefill_small_ragged(gs, cuda_dev, lengths):
+    dims = sy.Dims(2, 4, 128, 128)
+    n = len(lengths)
+    pool = sy.state(sy.generator(1), (2 * n + 1, dims.h_v, dims.d_v, dims.d_k)).to(cuda_dev)
+    init = pool.clone()
+    src = [(-1 if i % 2 == 0 else i) for i in range(n)]
+    dst = [n + i for i in range(n)]
+    dst[-1] = src[-1] if src[-1] >= 0 else dst[-1]            # one in-place publish
+    rows, cu, o, st = run_prefill(gs, cuda_dev, dims, lengths, src, dst, pool)
+    assert st == 0
+    S0s = [np.zeros((dims.h_v, 128, 128)) if s < 0 else init[s].cpu().numpy() for s in src]
+    finals = [pool[d].cpu().numpy() for d in dst]
+    ws, wo = check_sequences(rows, cu, o, S0s, finals, lengths)
+    assert ws <= CHUNK_STATE_RTOL, ws
+    assert wo <= 1.0, wo
+    for s in range(2 * n + 1):
+        if s not in dst:
+            assert torch.equal(pool[s], init[s]), "only destination slots are written"
+
+
+def test_prefill_workload_full_size(gs, cuda_dev):
+    """Eight sequences, log-uniform lengths in [512, 32768], 32 v-heads, d=128,
+    chunk 64; the first four start from zero, the last four from a state."""
+    dims = sy.DIMS_FULL
+    lengths = sy.prefill_lengths()
+    n = len(lengths)
+    rows, cu, s0 = sy.prefill_inputs(lengths, dims, seed=3)
+    pool = torch.zeros((2 * n, dims.h_v, dims.d_v, dims.d_k), dtype=torch.float32, device=cuda_dev)
+    pool[:n] = s0.to(cuda_dev)
+    src = [-1] * (n // 2) + list(range(n // 2, n))
+    dst = list(range(n, 2 * n))
+    rows2, cu2, o, st = run_prefill(gs, cuda_dev, dims, lengths, src, dst, pool)
+    assert st == 0
+    finals = [pool[d].cpu().numpy() for d in dst]
+    ws, wo = check_sequences(rows, cu, o, [s0[i].numpy() for i in range(n)], finals, lengths)
+    print("prefill full size: worst state rel %.3e, worst output ratio %.3f" % (ws, wo))
+    assert ws <= CHUNK_STATE_RTOL, ws
+    assert wo <= 1.0, wo
+
+
+def test_mixed_transaction_defers_then_resumes(gs, cuda_dev):
+    """Four prefills and four decode requests asking for K=3 share a
+    transaction: the planner defers every draft (12 rows), decode requests
+    advance by one token, prefills publish their final state; the next,
+    decode-only transaction resumes K=3 and reads the published state."""
+    from speculative_decoding_hybrid_gb300.step import LayerRows, VerifyStep
+    dims = sy.DIMS_FULL
+    d = gs.dims(dims.h_qk, dims.h_v, dims.d_k, dims.d_v)
+    num_slots = 12
+    pool_c = gs.Pool(num_slots)
+    dec_slots = [pool_c.alloc() for _ in range(4)]
+    init = sy.state(sy.generator(77), (num_slots, 1, dims.h_v, dims.d_v, dims.d_k)).to(cuda_dev)
+    vs = VerifyStep(d, 1, num_slots, 64, 8, 1024, cuda_dev, pool=init.clone())
+    plens = [300, 64, 129, 17]
+    reqs = [(gs.REQ_PREFILL, 0, L, 0, 1 << 30, -1) for L in plens] + \
+           [(gs.REQ_DECODE, 3, 0, 10, 1 << 30, s) for s in dec_slots]
+    plan = gs.Plan(8)
+    st = gs.plan_transaction(gs.make_reqs(reqs), 8, gs.gdn_plan_limits(4096, 8, 3), pool_c, plan)
+    assert st == gs.GDN_OK and plan.deferred == 12 and plan.plan == gs.PLAN_CHUNKED
+    assert plan.k == [0] * 8 and plan.dec_cu == [0, 1, 2, 3, 4] and plan.pre_cu == [0, 300, 364, 493, 510]
+    # oracle planner agrees
+    mp = oracle.PoolModel(num_slots)
+    for _ in range(4):
+        mp.alloc()
+    pm = oracle.plan_transaction([oracle.Req(oracle.PREFILL, n_tokens=L) for L in plens] +
+                                 [oracle.Req(oracle.DECODE, 3, cur_len=10, slot=s) for s in dec_slots],
+                                 4096, 8, 3, mp)
+    assert pm.deferred == 12 and pm.dst == plan.dst and pm.dec_cu == plan.dec_cu
+    # prefills: chunked, publishing only the final state into their fresh slots
+    pr, pcu, ps0 = sy.prefill_inputs(plens, dims, seed=12)
+    R = int(pcu[-1])
+    pool_l = vs.pool[:, 0]
+    ws_bytes = gs.gdn_prefill_workspace_bytes(d, 4, R)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=cuda_dev)
+    o = torch.empty((R, dims.h_v, dims.d_v), dtype=torch.bfloat16, device=cuda_dev)
+    prd = pr.to(cuda_dev)
+    stat = torch.zeros(1, dtype=torch.int32, device=cuda_dev)
+    gs.gdn_chunked_prefill(d, 4, R, pcu.to(cuda_dev), max(plens), prd.q, prd.k, prd.v, prd.g, prd.beta, pool_l,
+                           vs.slot_stride, num_slots, torch.tensor(plan.pre_src, dtype=torch.int32, device=cuda_dev),
+                           torch.tensor(plan.pre_dst, dtype=torch.int32, device=cuda_dev), o, 64, ws, ws_bytes, stat)
+    # decode requests: one token each (K = 0), verify + accept + commit
+    dr = sy.rows(sy.generator(13), 4, dims, cuda_dev)
+    cu = torch.tensor(plan.dec_cu, dtype=torch.int32, device=cuda_dev)
+    srcs = torch.tensor(plan.dec_src, dtype=torch.int32, device=cuda_dev)
+    dsts = torch.tensor(plan.dec_dst, dtype=torch.int32, device=cuda_dev)
+    lg, tgt = sy.logits(sy.generator(14), 4, 1024, 2.0, cuda_dev)
+    vs.run(4, cu, srcs, dsts, [LayerRows(dr.q, dr.k, dr.v, dr.g, dr.beta)], lg,
+           torch.zeros(4, dtype=torch.int32, device=cuda_dev))
+    torch.cuda.synchronize()
+    assert int(stat.item()) == 0 and int(vs.status.item()) == 0
+    assert vs.accept_len[:4].tolist() == [0, 0, 0, 0]                 # one token each, no drafts
+    # oracle: prefill final states and decode steps
+    for i in range(4):
+        a, b = int(pcu[i]), int(pcu[i + 1])
+        S, _, _ = oracle.gdn_recurrent(pr.q[a:b], pr.k[a:b], pr.v[a:b], pr.g[a:b], pr.beta[a:b],
+                                       np.zeros((dims.h_v, 128, 128)))
+        got = vs.pool[plan.pre_dst[i], 0].cpu().numpy()
+        rel = max(np.linalg.norm(got[h] - S[h]) / np.linalg.norm(S[h]) for h in range(dims.h_v))
+        assert rel <= CHUNK_STATE_RTOL
+    drh = dr.to("cpu")
+    for i, s in enumerate(dec_slots):
+        S, _, _ = oracle.gdn_recurrent(drh.q[i:i + 1], drh.k[i:i + 1], drh.v[i:i + 1], drh.g[i:i + 1],
+                                       drh.beta[i:i + 1], init[s, 0].cpu().numpy())
+        assert state_err(vs.pool[plan.dec_dst[i], 0].cpu().numpy(), S) <= 1.0
+    assert gs.gdn_pool_apply(pool_c, plan, 8) == gs.GDN_OK
+    # next transaction: decode-only (the four prefilled sequences now decode too) -> K = 3 again
+    slots2 = plan.dst
+    reqs2 = [(gs.REQ_DECODE, 3, 0, 400, 1 << 30, s) for s in slots2]
+    plan2 = gs.Plan(8)
+    assert gs.plan_transaction(gs.make_reqs(reqs2), 8, gs.gdn_plan_limits(4096, 8, 3), pool_c, plan2) == gs.GDN_OK
+    assert plan2.k == [3] * 8 and plan2.deferred == 0 and plan2.plan == gs.PLAN_RECURRENT
+    published = vs.pool[plan.pre_dst[0], 0].clone()
+    r2 = sy.rows(sy.generator(15), 32, dims, cuda_dev)
+    cu2 = torch.tensor(plan2.dec_cu, dtype=torch.int32, device=cuda_dev)
+    src2 = torch.tensor(plan2.dec_src, dtype=torch.int32, device=cuda_dev)
+    vs2 = VerifyStep(d, 1, num_slots, 32, 8, 1024, cuda_dev, pool=vs.pool)
+    vs2.txn = 5
+    vs2.verify_layer(0, 8, cu2, src2, LayerRows(r2.q, r2.k, r2.v, r2.g, r2.beta))
+    torch.cuda.synchronize()
+    r2h = r2.to("cpu")
+    S, o_ref, ck = oracle.gdn_recurrent(r2h.q[0:4], r2h.k[0:4], r2h.v[0:4], r2h.g[0:4], r2h.beta[0:4],
+                                        published.cpu().numpy(), want_ckpt=True)
+    assert state_err(vs2.ckpt[0, 0:4].cpu().numpy(), ck) <= 1.0       # verify read the published state
+
+
+def test_prefill_fail_closed(gs, cuda_dev):
+    dims = sy.Dims(2, 4, 128, 128)
+    pool = torch.zeros((4, 4, 128, 128), device=cuda_dev)
+    d = gs.dims(2, 4, 128, 128)
+    z = torch.zeros(64, dtype=torch.int32, device=cuda_dev)
+    with pytest.raises(gs.GdnError) as e:          # chunk length other than 64
+        gs.gdn_chunked_prefill(d, 1, 8, z, 8, pool, pool, pool, pool, pool, pool, pool.stride(0), 4, z, z, pool,
+                               32, pool, 1 << 20, z)
+    assert e.value.status == gs.GDN_ERR_ARG
+    with pytest.raises(gs.GdnError) as e:          # workspace too small
+        gs.gdn_chunked_prefill(d, 1, 8, z, 8, pool, pool, pool, pool, pool, pool, pool.stride(0), 4, z, z, pool,
+                               64, pool, 16, z)
+    assert e.value.status == gs.GDN_ERR_WORKSPACE
+    # a destination slot outside the pool is refused on the device, nothing written
+    rows, cu, o, st = run_prefill(gs, cuda_dev, dims, [70], [-1], [9], pool)
+    assert st & gs.DEV_SLOT_OOR
+    assert torch.count_nonzero(pool) == 0
