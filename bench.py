@@ -66,6 +66,86 @@ def src_digest(path):
         return hashlib.sha256(f.read()).hexdigest()[:16]
 
 
+def prefill_flops(lengths, h_v, d=128, C=64):
+    """Algorithmic flops of the chunk form: per chunk of n tokens and head,
+    n^2 (6 d_k + 4 d_v) + 6 n d_k d_v + n^3 / 3."""
+    tot = 0.0
+    for L in lengths:
+        for c0 in range(0, L, C):
+            n = min(C, L - c0)
+            tot += n * n * (6 * d + 4 * d) + 6 * n * d * d + n ** 3 / 3.0
+    return tot * h_v
+
+
+PREFILL_SETS = {
+    "prefill": None,                  # 8 sequences, log-uniform lengths in [512, 32768]
+    "prefill_small": [2048, 2048, 2048, 2048],
+}
+
+
+def bench_prefill(dev, lengths, reps=5, warmup=3):
+    """Times gdn_chunked_prefill of one layer over the ragged batch (inputs
+    resident in HBM; the 8 sequences' rows are ~1.6 GB, larger than L2)."""
+    from speculative_decoding_hybrid_gb300 import binding as gs
+    dims = sy.DIMS_FULL
+    n = len(lengths)
+    rows, cu, s0 = sy.prefill_inputs(lengths, dims, seed=3, device=dev)
+    R = int(cu[-1])
+    d = gs.dims(dims.h_qk, dims.h_v, dims.d_k, dims.d_v)
+    pool = torch.zeros((2 * n, dims.h_v, dims.d_v, dims.d_k), dtype=torch.float32, device=dev)
+    pool[:n] = s0
+    src = torch.tensor([-1] * (n // 2) + list(range(n // 2, n)), dtype=torch.int32, device=dev)
+    dst = torch.tensor(list(range(n, 2 * n)), dtype=torch.int32, device=dev)
+    ws_bytes = gs.gdn_prefill_workspace_bytes(d, n, R)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    o = torch.empty((R, dims.h_v, dims.d_v), dtype=torch.bfloat16, device=dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    cu_d = cu.to(dev)
+
+    def call():
+        gs.gdn_chunked_prefill(d, n, R, cu_d, max(lengths), rows.q, rows.k, rows.v, rows.g, rows.beta, pool,
+                               pool.stride(0), pool.shape[0], src, dst, o, 64, ws, ws_bytes, st)
+
+    for _ in range(warmup):
+        call()
+    torch.cuda.synchronize()
+    evs = []
+    for _ in range(reps):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        call()
+        b.record()
+        evs.append((a, b))
+    torch.cuda.synchronize()
+    ms = sum(a.elapsed_time(b) for a, b in evs) / reps
+    flops = prefill_flops(lengths, dims.h_v)
+    if int(st.item()) != 0:
+        raise RuntimeError("prefill status %d" % int(st.item()))
+    return {"tokens": R, "sequences": n, "ms_per_call": ms, "tokens_per_s": R / (ms * 1e-3),
+            "alg_tflops": flops / (ms * 1e-3) / 1e12, "launches_per_call": 2,
+            "workspace_gb": ws_bytes / 1e9}
+
+
+def rank_spec(spec: sy.Spec, rank: int) -> sy.Spec:
+    """Requests are independent problems: rank r runs its own batch, drawn
+    with its own seed (weak scaling, no data-path exchange)."""
+    import dataclasses
+    return spec if rank == 0 else dataclasses.replace(spec, seed=spec.seed + 1000 * rank)
+
+
+def reduce_across_ranks(ms: float, tokens: float, device=None):
+    """Whole-job figures: the slowest rank's timed region and the tokens of
+    all ranks.  The barrier and these two reductions are the only collectives."""
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return ms, tokens
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    n = torch.tensor([tokens], dtype=torch.float64, device=device)
+    dist.all_reduce(n, op=dist.ReduceOp.SUM)
+    return float(t.item()), float(n.item())
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -178,14 +258,32 @@ class Bench:
         self.verified = 0
         self.last_plan = None
 
+    def precompute_drafts(self, n_steps):
+        """Draft tokens are synthetic inputs: draw them for every step before
+        timing, assuming the planner grants the requested draft counts (it
+        does when no request is near its length limit; checked per step)."""
+        self.pre = {}
+        for s in range(n_steps):
+            ks = self.ks[s % self.ks.shape[0]].tolist()
+            drafts = sy.step_drafts(self.spec, s, ks, self.targets[s % self.spec.ring])
+            toks = [t for dr in drafts for t in dr]
+            h = torch.zeros(self.cap, dtype=torch.int32)
+            h[:len(toks)] = torch.tensor(toks, dtype=torch.int32)
+            self.pre[s] = (ks, h.pin_memory())
+
     def prepare(self, s):
         """Host part of a step: plan, drafts, table upload."""
-        p = self.loop.plan_step(self.ks[s % self.ks.shape[0]].tolist())
+        ks = self.ks[s % self.ks.shape[0]].tolist()
+        p = self.loop.plan_step(ks)
         ring = s % self.spec.ring
-        drafts = sy.step_drafts(self.spec, s, p.k, self.targets[ring])
-        toks = [t for dr in drafts for t in dr]
-        self.tok_h[:len(toks)] = torch.tensor(toks, dtype=torch.int32)
-        self.tok_d.copy_(self.tok_h, non_blocking=True)
+        pre = getattr(self, "pre", {}).get(s)
+        if pre is not None and pre[0] == p.k:
+            self.tok_d.copy_(pre[1], non_blocking=True)
+        else:
+            drafts = sy.step_drafts(self.spec, s, p.k, self.targets[ring])
+            toks = [t for dr in drafts for t in dr]
+            self.tok_h[:len(toks)] = torch.tensor(toks, dtype=torch.int32)
+            self.tok_d.copy_(self.tok_h, non_blocking=True)
         self.loop.upload_tables()
         self.last_plan = p
         return ring, p
@@ -381,11 +479,24 @@ def main():
     ap.add_argument("--steps", type=int, default=None)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="paged256", choices=sorted(WORKLOADS))
+    ap.add_argument("--workload", default="paged256", choices=sorted(WORKLOADS) + sorted(PREFILL_SETS))
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-prefill", action="store_true")
     args = ap.parse_args()
+    if args.workload in PREFILL_SETS:
+        if args.impl == "reference":
+            print(json.dumps({"impl": "reference", "unavailable": "prefill-only workloads have no CPU timing arm"}))
+            return
+        from speculative_decoding_hybrid_gb300 import build
+        build.build()
+        dev = torch.device("cuda", 0)
+        lengths = PREFILL_SETS[args.workload] or sy.prefill_lengths()
+        r = bench_prefill(dev, lengths, reps=args.steps or 5, warmup=args.warmup)
+        print(json.dumps({"metric": "chunked prefill tokens/s", "value": r["tokens_per_s"], "unit": "tokens/s",
+                          "workload": args.workload, "prefill": r}), flush=True)
+        return
     spec = WORKLOADS[args.workload]
     if args.steps is None:
         args.steps = min(spec.steps, 100)
@@ -407,7 +518,8 @@ def main():
 
     from speculative_decoding_hybrid_gb300 import build
     build.build()
-    b = Bench(spec, dev, rank)
+    b = Bench(rank_spec(spec, rank), dev, rank)
+    b.precompute_drafts(args.warmup + args.steps + (0 if args.no_e2e else 3 + args.e2e_steps))
     for _ in range(args.warmup):
         b.step()
     torch.cuda.synchronize()
@@ -434,15 +546,7 @@ def main():
     torch.cuda.synchronize()
     clocks = sampler.stop()
     ms = start.elapsed_time(end)
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
-        tt = torch.tensor([tok], device=dev, dtype=torch.float64)
-        dist.all_reduce(tt)
-        tok_all = float(tt.item())
-    else:
-        tok_all = tok
+    ms, tok_all = reduce_across_ranks(ms, tok, dev)
 
     def avg_ms(name):
         s, e = ev[name]
@@ -475,6 +579,9 @@ def main():
             dist.barrier()
             dist.destroy_process_group()
         return
+    prefill = None
+    if not args.no_prefill and args.workload == "paged256":
+        prefill = bench_prefill(dev, sy.prefill_lengths())
     cpu = None
     if not args.no_cpu_baseline and world == 1:
         cpu = cpu_baseline(spec)
@@ -508,6 +615,7 @@ def main():
         "e2e": e2e,
         "cpu_baseline": cpu,
         "acceptance": {"verified_tokens": tok, "requests": spec.batch},
+        "prefill": prefill,
     }
     print(json.dumps(line), flush=True)
     if world > 1:

@@ -6,11 +6,13 @@ import oracle
 
 # Tolerances (written from the arithmetic; see the parity section of the design notes):
 #   FP32 state: |x - y| <= 1e-4 * max(|y|, 1e-2 * max|y over the head|)
-#   bf16 output vs the unrounded FP64 value: |o - y| <= max(2e-3, 2^-8 |y|)
+#   bf16 output vs the unrounded FP64 value: |o - y| <= max(2e-3, (2^-8 + 1e-4) |y|)
+#   (bf16 rounding of an FP32 value is within half an ulp, at most 2^-8 of
+#   it; the FP32 value itself may sit 1e-4 relative from y, the FP32 budget)
 STATE_RTOL = 1e-4
 STATE_FLOOR = 1e-2
 OUT_ATOL = 2e-3
-OUT_RREL = 2.0 ** -8
+OUT_RREL = 2.0 ** -8 + 1e-4
 
 
 def state_err(gpu, ref):
