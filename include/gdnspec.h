@@ -26,8 +26,9 @@
  *
  * Conventions shared by every entry point
  *   - Tensor pointers are DEVICE pointers unless a parameter says "host".
- *     The caller owns every buffer; the library allocates no device memory
- *     and keeps no global state.
+ *     The caller owns every buffer; the library allocates no device memory.
+ *     Its only global state is the fixed scratch array of
+ *     mtp_greedy_accept_noalloc (see there).
  *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy
  *     default stream).  Errors that the host can see (null pointers, shapes,
  *     sizes) are returned at once and nothing is launched.  Errors only the
@@ -162,6 +163,27 @@ int mtp_greedy_accept(int32_t B, int32_t row_capacity, const int32_t *cu_rows,
                       int32_t *bonus, int32_t *out_tokens, mtp_stats *stats,
                       void *workspace, size_t workspace_bytes,
                       uint32_t *dev_status, void *stream);
+
+/*
+ * mtp_greedy_accept_noalloc -- mtp_greedy_accept without a workspace, for
+ * callers that cannot allocate device memory (a plugin whose host engine owns
+ * all device memory, or a latency-critical loop that cannot afford a
+ * cudaMalloc).  The pages describe no such call; it computes exactly what
+ * mtp_greedy_accept computes, with the same arguments minus the workspace.
+ *   Scratch: a fixed 512 KiB device array inside the library (held by every
+ *   device that loads it until exit), shared by all calls and keeping the
+ *   last call's contents.  A request whose mtp_accept_workspace_bytes()
+ *   exceeds 512 KiB returns GDN_ERR_WORKSPACE and launches nothing.  Calls
+ *   that overlap on the GPU race on the scratch: order them on one stream.
+ *   The first call on a device resolves the array's address with that device
+ *   current (make it before any stream capture); the stream must belong to
+ *   the current device.  No call allocates or frees memory.
+ */
+int mtp_greedy_accept_noalloc(int32_t B, int32_t row_capacity, const int32_t *cu_rows,
+                              const gdn_bf16 *logits, int64_t vocab, int64_t row_stride,
+                              const int32_t *tokens, int32_t *argmax, int32_t *accept_len,
+                              int32_t *bonus, int32_t *out_tokens, mtp_stats *stats,
+                              uint32_t *dev_status, void *stream);
 
 /*
  * gdn_commit -- rollback/commit of all layers in one launch ([ENGINE]

@@ -28,7 +28,8 @@ MAX_ROWS = K_MAX + 1
 REQ_DECODE, REQ_PREFILL = 0, 1
 PLAN_RECURRENT, PLAN_CHUNKED = 0, 1
 
-EXPORTS = ["gdn_decode_step", "gdn_verify", "mtp_accept_workspace_bytes", "mtp_greedy_accept", "gdn_commit",
+EXPORTS = ["gdn_decode_step", "gdn_verify", "mtp_accept_workspace_bytes", "mtp_greedy_accept",
+           "mtp_greedy_accept_noalloc", "gdn_commit",
            "gdn_prefill_workspace_bytes", "gdn_chunked_prefill", "gdn_pool_init", "gdn_pool_alloc",
            "gdn_pool_share", "gdn_pool_release", "plan_transaction", "gdn_pool_apply", "gdn_pool_abort",
            "gdn_status_string"]
@@ -84,6 +85,7 @@ def _load():
         "gdn_verify": [DP, I32, I32, P, P, P, P, P, P, P, I64, I32, P, P, P, U32, P, P, P],
         "mtp_accept_workspace_bytes": [I32, I64],
         "mtp_greedy_accept": [I32, I32, P, P, I64, I64, P, P, P, P, P, P, P, SZ, P, P],
+        "mtp_greedy_accept_noalloc": [I32, I32, P, P, I64, I64, P, P, P, P, P, P, P, P],
         "gdn_commit": [DP, I32, I32, I32, P, P, P, I64, P, U32, P, I64, I64, I32, P, P, P],
         "gdn_prefill_workspace_bytes": [DP, I32, I32],
         "gdn_chunked_prefill": [DP, I32, I32, P, I32, P, P, P, P, P, P, I64, I32, P, P, P, I32, P, SZ, P, P],
@@ -174,6 +176,15 @@ def mtp_greedy_accept(B, row_capacity, cu_rows, logits, vocab, row_stride, token
         B, row_capacity, _ptr(cu_rows), _ptr(logits), vocab, row_stride, _ptr(tokens), _ptr(argmax),
         _ptr(accept_len), _ptr(bonus), _ptr(out_tokens), _ptr(stats), _ptr(workspace), workspace_bytes,
         _ptr(dev_status), _stream(stream)))
+
+
+def mtp_greedy_accept_noalloc(B, row_capacity, cu_rows, logits, vocab, row_stride, tokens, argmax, accept_len,
+                              bonus, out_tokens, stats, dev_status, stream=None):
+    """mtp_greedy_accept with the library's fixed device scratch instead of a
+    caller workspace (for callers that cannot allocate device memory)."""
+    return _check("mtp_greedy_accept_noalloc", lib.mtp_greedy_accept_noalloc(
+        B, row_capacity, _ptr(cu_rows), _ptr(logits), vocab, row_stride, _ptr(tokens), _ptr(argmax),
+        _ptr(accept_len), _ptr(bonus), _ptr(out_tokens), _ptr(stats), _ptr(dev_status), _stream(stream)))
 
 
 def gdn_commit(d: gdn_dims, B, num_layers, row_capacity, cu_rows, accept_len, ckpt, ckpt_layer_stride, ckpt_tag,
