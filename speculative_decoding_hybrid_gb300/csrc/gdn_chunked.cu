@@ -9,15 +9,15 @@
 //   O  = diag(e^G) Q S0^T + (M o Q K^T) U,   M[t][i] = e^{G_t-G_i} (i <= t)
 //   S' = e^{G_C} S0 + U^T diag(e^{G_C-G}) K
 //
-// Two kernels.
+// Two kernels, both on the 5th-generation tensor cores (tcgen05).
 //  (1) gdn_chunk_wy_kernel -- one CTA per (chunk, v-head), all chunks of all
-//      sequences at once: K K^T, the unit lower-triangular inverse T by
-//      column-wise forward substitution, W and Ut; W and Ut go to the
-//      workspace (fp32, 64 KB per chunk and head).
-//  (2) gdn_chunk_scan_kernel -- one CTA per (sequence, v-head, slice of
-//      d_v rows of S): the state slice stays in shared memory across the
-//      sequence's chunks; per chunk it forms U, the outputs and the next
-//      state.  Rows of S are independent, so slices run in parallel.
+//      sequences at once (state-independent): [K;Q] K^T, the unit
+//      lower-triangular inverse T in 16x16 blocks, W and Ut, and the masked,
+//      decayed P = M o Q K^T; W, Ut and P go to the workspace (fp32, 80 KB
+//      per chunk and head).
+//  (2) gdn_chunk_scan_kernel -- one CTA per (sequence, v-head): the only
+//      sequential part.  The state stays on chip across the sequence's
+//      chunks; per chunk it forms U, the outputs and the next state.
 // Sequence i's chunks start at cu_seqlens[i]; chunk c of sequence i uses
 // workspace slot (cu_seqlens[i] + 64c)/64 + i, unique and below
 // ceil(row_capacity/64) + nseq.
@@ -29,7 +29,6 @@ namespace {
 constexpr int kC = 64;         // chunk length
 constexpr int kD = 128;        // d_k = d_v supported by this kernel pair
 constexpr int kThreads = 256;
-constexpr int kSlice = 32;     // state rows per scan CTA
 
 __device__ __forceinline__ int chunk_slot(int seq_start, int c, int seq) { return (seq_start + kC * c) / kC + seq; }
 
@@ -47,8 +46,12 @@ struct PrefArgs {
     uint32_t *status;
 };
 
+// Workspace per (chunk slot, v-head): W [C][D], Ut [C][D] and P [C][C], fp32,
+// with P[t][i] = e^{G_t-G_i} q_t.k_i for i <= t (0 elsewhere and past the chunk).
+constexpr size_t kWsFloats = size_t(2) * kC * kD + size_t(kC) * kC;
+
 __device__ __forceinline__ float *ws_w(const PrefArgs &a, int slot, int h) {
-    return a.ws + ((size_t(slot) * a.h_v + h) * 2) * size_t(kC) * kD;
+    return a.ws + (size_t(slot) * a.h_v + h) * kWsFloats;
 }
 
 // ---------------------------------------------------------------------------
@@ -65,7 +68,8 @@ __device__ __forceinline__ float *ws_w(const PrefArgs &a, int slot, int h) {
 //    inversion live in the TB/TV area before those tiles are written)
 //   misc G, beta, e^G, mbarrier, tensor-memory base, flags
 // Tensor memory (256 columns): D1 = [K;Q] K^T at columns 0..63 (rows 0..63:
-// K K^T), D2 = W^T at 64..127, D3 = Ut^T at 128..191 (lane = d index).
+// K K^T, rows 64..127: Q K^T, which becomes P for the scan), D2 = W^T at
+// 64..127, D3 = Ut^T at 128..191 (lane = d index).
 namespace wy {
 constexpr uint32_t kA1 = 0, kKT = 32768, kVT = 49152, kT = 65536, kMisc = 98304;
 constexpr uint32_t kTbHi = kT, kTbLo = kT + 8192, kTvHi = kT + 16384, kTvLo = kT + 24576;
@@ -110,8 +114,10 @@ __global__ void __launch_bounds__(kThreads) gdn_chunk_wy_kernel(const PrefArgs a
     if (tid == 0) gdn::mbar_init(bar, 1);
 
     // Stage K, Q (rows of A1), K^T and V^T as bf16 operand tiles; rows past n are zero.
+    // A warp covers 32 consecutive tokens of one 8-column group, so the
+    // transposed stores of a warp land in one row of K^T / V^T (no bank conflicts).
     for (int e = tid; e < kC * (kD / 8); e += kThreads) {
-        const int t = e / (kD / 8), c8 = (e % (kD / 8)) * 8;
+        const int t = e % kC, c8 = (e / kC) * 8;
         uint4 kv = make_uint4(0, 0, 0, 0), qv = kv, vv = kv;
         if (t < n) {
             kv = __ldg(reinterpret_cast<const uint4 *>(a.k + (size_t(t0 + t) * a.h_qk + hq) * kD + c8));
@@ -164,19 +170,33 @@ __global__ void __launch_bounds__(kThreads) gdn_chunk_wy_kernel(const PrefArgs a
         (void)gdn::mbar_try_wait(bar, 0);
         tc::fence_after();
         if (tid < kC) eG[tid] = expf(Gs[tid]);
-        // A[t][i] = beta_t e^{G_t-G_i} (k_t.k_i), i < t, from the accumulator rows 0..63
+        // Rows 0..63: A[t][i] = beta_t e^{G_t-G_i} (k_t.k_i), i < t.
+        // Rows 64..127: P[t][i] = e^{G_t-G_i} (q_t.k_i), i <= t, to the workspace.
         const int q4 = warp & 3, hc = warp >> 2;
-        if (q4 < 2) {
-            const int t = 32 * q4 + lane;
+        float *Pw = ws_w(a, chunk_slot(s0, c, seq), h) + 2 * kC * kD;
+        const int t = 32 * (q4 & 1) + lane;
 #pragma unroll
-            for (int part = 0; part < 2; ++part) {
-                float v16[16];
-                const int col0 = 32 * hc + 16 * part;
-                tc::ld16(tm + (uint32_t(32 * q4) << 16) + uint32_t(col0), v16);
+        for (int part = 0; part < 2; ++part) {
+            float v16[16];
+            const int col0 = 32 * hc + 16 * part;
+            tc::ld16(tm + (uint32_t(32 * q4) << 16) + uint32_t(col0), v16);
+            if (q4 < 2) {
 #pragma unroll
                 for (int x = 0; x < 16; ++x) {
                     const int i = col0 + x;
                     Af[t * (kC + 1) + i] = (i < t && t < n) ? Bs[t] * expf(Gs[t] - Gs[i]) * v16[x] : 0.f;
+                }
+            } else {
+#pragma unroll
+                for (int x = 0; x < 16; x += 4) {
+                    float4 pv;
+                    float *pe = &pv.x;
+#pragma unroll
+                    for (int y = 0; y < 4; ++y) {
+                        const int i = col0 + x + y;
+                        pe[y] = (i <= t && t < n) ? expf(Gs[t] - Gs[i]) * v16[x + y] : 0.f;
+                    }
+                    *reinterpret_cast<float4 *>(Pw + t * kC + col0 + x) = pv;
                 }
             }
         }
@@ -308,14 +328,53 @@ __global__ void __launch_bounds__(kThreads) gdn_chunk_wy_kernel(const PrefArgs a
 }
 
 // ---------------------------------------------------------------------------
-// (2) sequential scan over chunks, one state slice per CTA
+// (2) sequential scan over chunks on the tensor cores (tcgen05, kind::f16)
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(kThreads) gdn_chunk_scan_kernel(const PrefArgs a) {
-    const int nsl = kD / kSlice;
-    const int sl = blockIdx.x % nsl;
-    const int h = (blockIdx.x / nsl) % a.h_v;
-    const int seq = blockIdx.x / (nsl * a.h_v);
-    const int tid = threadIdx.x;
+// One CTA per (sequence, v-head); the 128 value rows of S are the M = 128
+// side of every product, so each thread owns one row of S (lane quadrant of
+// its warp) and half of its columns.  The FP32 master copy of S stays in
+// registers for the whole sequence.  Every operand that is not exactly bf16
+// is split into two bf16 parts, x = x1 + x2 with x1 = bf16(x) and
+// x2 = bf16(x - x1) (about 2^-16 relative), and a product keeps the three
+// leading terms a1 b1 + a1 b2 + a2 b1; q and k are exact bf16.  Per chunk:
+//   phase A:  Uacc = S W^T         (M128 N64  K128)  -> U^T = Ut^T - Uacc
+//             Oi   = S Q^T         (M128 N64  K128)
+//   phase B:  Oa   = U^T P^T       (M128 N64  K64)
+//             dS   = U^T (dec o K) (M128 N128 K64),   S <- e^{G_last} S + dS
+//   o_t = q_scale (e^{G_t} Oi[:,t] + Oa[:,t]),  dec_i = e^{G_last - G_i},
+// with P, W and Ut from the per-chunk kernel's workspace.
+// Shared-memory map (bytes from a 1024-aligned base), bf16 K-major tiles:
+namespace sc {
+constexpr uint32_t kS1 = 0, kS2 = 32768;        // S parts      128 rows (d_v) x 128 (d_k)
+constexpr uint32_t kW1 = 65536, kW2 = 81920;    // W parts       64 rows (t)   x 128 (d_k)
+constexpr uint32_t kQ = 98304;                  // Q             64 rows (t)   x 128 (d_k)
+constexpr uint32_t kP1 = 114688, kP2 = 122880;  // P parts       64 rows (t)   x  64 (i)
+constexpr uint32_t kK1 = 131072, kK2 = 147456;  // dec K parts  128 rows (d_k) x  64 (i)
+constexpr uint32_t kU1 = 163840, kU2 = 180224;  // U^T parts    128 rows (d_v) x  64 (i)
+constexpr uint32_t kMisc = 196608;              // G, e^G, dec, mbarrier, tensor-memory base, flag
+constexpr size_t kSmem = kMisc + 1024 + 1024;
+constexpr uint32_t kTmemCols = 512;  // Uacc 0..63, Oi 64..127, Oa 128..191, dS 256..383
+}  // namespace sc
+
+// Two-term bf16 split of 8 consecutive values, packed as two 16-byte chunks.
+__device__ __forceinline__ void split8(const float (&x)[8], uint4 &hi, uint4 &lo) {
+    uint32_t h[4], l[4];
+#pragma unroll
+    for (int p = 0; p < 4; ++p) {
+        const uint16_t h0 = gdn::f32_to_bf16(x[2 * p]), h1 = gdn::f32_to_bf16(x[2 * p + 1]);
+        const uint16_t l0 = gdn::f32_to_bf16(x[2 * p] - gdn::bf16_to_f32(h0));
+        const uint16_t l1 = gdn::f32_to_bf16(x[2 * p + 1] - gdn::bf16_to_f32(h1));
+        h[p] = uint32_t(h0) | (uint32_t(h1) << 16);
+        l[p] = uint32_t(l0) | (uint32_t(l1) << 16);
+    }
+    hi = make_uint4(h[0], h[1], h[2], h[3]);
+    lo = make_uint4(l[0], l[1], l[2], l[3]);
+}
+
+__global__ void __launch_bounds__(kThreads, 1) gdn_chunk_scan_kernel(const PrefArgs a) {
+    const int h = blockIdx.x % a.h_v;
+    const int seq = blockIdx.x / a.h_v;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int s0 = a.cu[seq];
     const int s1 = a.cu[seq + 1];
     const int len = s1 - s0;
@@ -325,45 +384,74 @@ __global__ void __launch_bounds__(kThreads) gdn_chunk_scan_kernel(const PrefArgs
     if (s0 < 0 || len < 0 || s1 > a.row_capacity) bad |= GDN_DEV_ROWS_BAD;
     if (src < -1 || src >= a.num_slots || dst < 0 || dst >= a.num_slots) bad |= GDN_DEV_SLOT_OOR;
     if (bad) {
-        if (h == 0 && sl == 0 && tid == 0) gdn::set_status(a.status, bad);
+        if (h == 0 && tid == 0) gdn::set_status(a.status, bad);
         return;
     }
     const int hq = h / a.grp;
-    const int a0 = sl * kSlice;
 
-    extern __shared__ __align__(16) float sm[];
-    float *Ss = sm;                        // [kSlice][D+1]   state rows a0..a0+kSlice
-    float *Qs = Ss + kSlice * (kD + 1);    // [C][D+1]
-    float *Ks = Qs + kC * (kD + 1);        // [C][D+1]
-    float *Ws = Ks + kC * (kD + 1);        // [C][D+1]
-    float *Us = Ws + kC * (kD + 1);        // [C][kSlice+1]
-    float *Ps = Us + kC * (kSlice + 1);    // [C][C+1]
-    float *Gs = Ps + kC * (kC + 1);        // [C]
+    extern __shared__ unsigned char smraw[];
+    const uint32_t raw_u = gdn::smem_u32(smraw);
+    unsigned char *sm = smraw + (((raw_u + 1023u) & ~1023u) - raw_u);
+    const uint32_t sb = gdn::smem_u32(sm);
+    float *Gs = reinterpret_cast<float *>(sm + sc::kMisc);
+    float *eG = Gs + kC;
+    float *dec = eG + kC;
+    uint64_t *bar = reinterpret_cast<uint64_t *>(sm + sc::kMisc + 768);
+    uint32_t *tbase = reinterpret_cast<uint32_t *>(sm + sc::kMisc + 776);
+    int *flag = reinterpret_cast<int *>(sm + sc::kMisc + 780);
 
-    const size_t head_off = size_t(h) * kD * kD + size_t(a0) * kD;
-    for (int e = tid; e < kSlice * kD; e += kThreads) {
-        const int r = e / kD, j = e % kD;
-        Ss[r * (kD + 1) + j] = src >= 0 ? a.pool[size_t(src) * a.slot_stride + head_off + e] : 0.f;
+    if (warp == 0) tc::tmem_alloc(tbase, sc::kTmemCols);
+    if (tid == 0) gdn::mbar_init(bar, 1);
+
+    const int q4 = warp & 3, hc = warp >> 2;
+    const int arow = 32 * q4 + lane;  // row of S held by this thread
+    const uint32_t lane_base = uint32_t(32 * q4) << 16;
+    const size_t row_off = size_t(h) * kD * kD + size_t(arow) * kD + 64 * hc;
+    float sv[64];  // S[arow][64hc .. 64hc+63], FP32 master
+    if (src >= 0) {
+        const float4 *sp = reinterpret_cast<const float4 *>(a.pool + size_t(src) * a.slot_stride + row_off);
+#pragma unroll
+        for (int x = 0; x < 16; ++x) {
+            const float4 v = sp[x];
+            sv[4 * x] = v.x;
+            sv[4 * x + 1] = v.y;
+            sv[4 * x + 2] = v.z;
+            sv[4 * x + 3] = v.w;
+        }
+    } else {
+#pragma unroll
+        for (int x = 0; x < 64; ++x) sv[x] = 0.f;
     }
+    auto write_S = [&]() {
+#pragma unroll
+        for (int x = 0; x < 8; ++x) {
+            float e[8];
+#pragma unroll
+            for (int y = 0; y < 8; ++y) e[y] = sv[8 * x + y];
+            uint4 hi, lo;
+            split8(e, hi, lo);
+            const uint32_t off = tc::swz_off(128, arow, 64 * hc + 8 * x);
+            *reinterpret_cast<uint4 *>(sm + sc::kS1 + off) = hi;
+            *reinterpret_cast<uint4 *>(sm + sc::kS2 + off) = lo;
+        }
+    };
+    write_S();
+    tc::fence_before();
+    __syncthreads();
+    tc::fence_after();
+    const uint32_t tm = *tbase;
+    constexpr uint32_t id64 = tc::idesc_bf16(128, 64);
+    constexpr uint32_t id128 = tc::idesc_bf16(128, 128);
+
+    uint32_t phase = 0;
+    bool ok = true;
     const int nchunks = (len + kC - 1) / kC;
     for (int c = 0; c < nchunks; ++c) {
         const int t0 = s0 + c * kC;
         const int n = min(kC, len - c * kC);
         const float *W = ws_w(a, chunk_slot(s0, c, seq), h);
         const float *Ut = W + kC * kD;
-        __syncthreads();  // previous chunk's readers are done with the buffers
-        for (int e = tid; e < kC * kD; e += kThreads) {
-            const int t = e / kD, j = e % kD;
-            float qv = 0.f, kv = 0.f, wv = 0.f;
-            if (t < n) {
-                qv = gdn::bf16_to_f32(a.q[(size_t(t0 + t) * a.h_qk + hq) * kD + j]);
-                kv = gdn::bf16_to_f32(a.k[(size_t(t0 + t) * a.h_qk + hq) * kD + j]);
-                wv = W[e];
-            }
-            Qs[t * (kD + 1) + j] = qv;
-            Ks[t * (kD + 1) + j] = kv;
-            Ws[t * (kD + 1) + j] = wv;
-        }
+        const float *P = W + 2 * kC * kD;
         if (tid < kC) Gs[tid] = tid < n ? a.g[size_t(t0 + tid) * a.h_v + h] : 0.f;
         __syncthreads();
         if (tid == 0) {
@@ -373,64 +461,188 @@ __global__ void __launch_bounds__(kThreads) gdn_chunk_scan_kernel(const PrefArgs
                 Gs[t] = run;
             }
         }
+        float ut[32];  // Ut[t][arow] for t in [32hc, 32hc+32), consumed after phase A
+#pragma unroll
+        for (int x = 0; x < 32; ++x) ut[x] = Ut[(32 * hc + x) * kD + arow];
         __syncthreads();
-        // U[t][a] = Ut[t][a] - sum_j W[t][j] S[a][j]
-        for (int e = tid; e < kC * kSlice; e += kThreads) {
-            const int t = e / kSlice, r = e % kSlice;
-            float acc = 0.f;
-            for (int j = 0; j < kD; ++j) acc = fmaf(Ws[t * (kD + 1) + j], Ss[r * (kD + 1) + j], acc);
-            Us[t * (kSlice + 1) + r] = t < n ? Ut[t * kD + a0 + r] - acc : 0.f;
+        if (tid < kC) {
+            eG[tid] = expf(Gs[tid]);
+            dec[tid] = tid < n ? expf(Gs[n - 1] - Gs[tid]) : 0.f;
         }
-        // P[t][i] = e^{G_t-G_i} q_t.k_i for i <= t
-        for (int e = tid; e < kC * kC; e += kThreads) {
-            const int t = e / kC, i = e % kC;
-            float val = 0.f;
-            if (i <= t && t < n) {
-                float acc = 0.f;
-                for (int j = 0; j < kD; ++j) acc = fmaf(Qs[t * (kD + 1) + j], Ks[i * (kD + 1) + j], acc);
-                val = expf(Gs[t] - Gs[i]) * acc;
+        __syncthreads();
+        // Stage the chunk's operand tiles.
+        for (int e = tid; e < kC * (kD / 8); e += kThreads) {  // W parts and Q: row t, 8 d_k values
+            const int t = e >> 4, j8 = (e & 15) * 8;
+            float w[8];
+            uint4 qv = make_uint4(0, 0, 0, 0);
+            if (t < n) {
+                const float4 w0 = *reinterpret_cast<const float4 *>(W + t * kD + j8);
+                const float4 w1 = *reinterpret_cast<const float4 *>(W + t * kD + j8 + 4);
+                w[0] = w0.x; w[1] = w0.y; w[2] = w0.z; w[3] = w0.w;
+                w[4] = w1.x; w[5] = w1.y; w[6] = w1.z; w[7] = w1.w;
+                qv = __ldg(reinterpret_cast<const uint4 *>(a.q + (size_t(t0 + t) * a.h_qk + hq) * kD + j8));
+            } else {
+#pragma unroll
+                for (int y = 0; y < 8; ++y) w[y] = 0.f;
             }
-            Ps[t * (kC + 1) + i] = val;
+            uint4 hi, lo;
+            split8(w, hi, lo);
+            const uint32_t off = tc::swz_off(64, t, j8);
+            *reinterpret_cast<uint4 *>(sm + sc::kW1 + off) = hi;
+            *reinterpret_cast<uint4 *>(sm + sc::kW2 + off) = lo;
+            *reinterpret_cast<uint4 *>(sm + sc::kQ + off) = qv;
+        }
+        for (int e = tid; e < kC * (kC / 8); e += kThreads) {  // P parts: row t, 8 values of i
+            const int t = e >> 3, i8 = (e & 7) * 8;
+            const float4 p0 = *reinterpret_cast<const float4 *>(P + t * kC + i8);
+            const float4 p1 = *reinterpret_cast<const float4 *>(P + t * kC + i8 + 4);
+            const float pe[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
+            uint4 hi, lo;
+            split8(pe, hi, lo);
+            const uint32_t off = tc::swz_off(64, t, i8);
+            *reinterpret_cast<uint4 *>(sm + sc::kP1 + off) = hi;
+            *reinterpret_cast<uint4 *>(sm + sc::kP2 + off) = lo;
+        }
+        for (int e = tid; e < kD * (kC / 8); e += kThreads) {  // dec o K, transposed: row d_k index j, 8 tokens
+            const int j = e >> 3, i8 = (e & 7) * 8;
+            float kv[8];
+#pragma unroll
+            for (int y = 0; y < 8; ++y) {
+                const int i = i8 + y;
+                kv[y] = i < n ? gdn::bf16_to_f32(a.k[(size_t(t0 + i) * a.h_qk + hq) * kD + j]) * dec[i] : 0.f;
+            }
+            uint4 hi, lo;
+            split8(kv, hi, lo);
+            const uint32_t off = tc::swz_off(128, j, i8);
+            *reinterpret_cast<uint4 *>(sm + sc::kK1 + off) = hi;
+            *reinterpret_cast<uint4 *>(sm + sc::kK2 + off) = lo;
+        }
+        gdn::fence_proxy_async_smem();
+        tc::fence_before();
+        __syncthreads();
+        // Phase A: Uacc = S W^T, Oi = S Q^T.
+        if (tid == 0) {
+            tc::fence_after();
+#pragma unroll
+            for (int at = 0; at < 2; ++at)
+#pragma unroll
+                for (int s = 0; s < 4; ++s) {
+                    const uint32_t ka = at * 16384 + s * 32, kb = at * 8192 + s * 32;
+                    const uint64_t a1 = tc::smem_desc(sb + sc::kS1 + ka), a2 = tc::smem_desc(sb + sc::kS2 + ka);
+                    const uint64_t w1 = tc::smem_desc(sb + sc::kW1 + kb), w2 = tc::smem_desc(sb + sc::kW2 + kb);
+                    const uint64_t qd = tc::smem_desc(sb + sc::kQ + kb);
+                    tc::mma_bf16(tm, a1, w1, id64, (at | s) ? 1u : 0u);
+                    tc::mma_bf16(tm, a1, w2, id64, 1u);
+                    tc::mma_bf16(tm, a2, w1, id64, 1u);
+                    tc::mma_bf16(tm + 64, a1, qd, id64, (at | s) ? 1u : 0u);
+                    tc::mma_bf16(tm + 64, a2, qd, id64, 1u);
+                }
+            tc::commit(bar);
+            *flag = gdn::mbar_wait_bounded(bar, phase) ? 1 : 0;
         }
         __syncthreads();
-        // O[t][a] = e^{G_t} q_t.S[a] + sum_{i<=t} P[t][i] U[i][a]
-        for (int e = tid; e < kC * kSlice; e += kThreads) {
-            const int t = e / kSlice, r = e % kSlice;
-            if (t >= n) continue;
-            float inter = 0.f;
-            for (int j = 0; j < kD; ++j) inter = fmaf(Qs[t * (kD + 1) + j], Ss[r * (kD + 1) + j], inter);
-            float intra = 0.f;
-            for (int i = 0; i <= t; ++i) intra = fmaf(Ps[t * (kC + 1) + i], Us[i * (kSlice + 1) + r], intra);
-            const float ov = a.q_scale * fmaf(expf(Gs[t]), inter, intra);
-            a.o[(size_t(t0 + t) * a.h_v + h) * kD + a0 + r] = gdn::f32_to_bf16(ov);
+        if (*flag == 0) {
+            ok = false;
+            break;
+        }
+        (void)gdn::mbar_try_wait(bar, phase);
+        phase ^= 1u;
+        tc::fence_after();
+        // U^T[arow][t] = Ut[t][arow] - Uacc[arow][t], split into two bf16 parts.
+#pragma unroll
+        for (int part = 0; part < 2; ++part) {
+            float v16[16];
+            const int col0 = 32 * hc + 16 * part;
+            tc::ld16(tm + lane_base + uint32_t(col0), v16);
+#pragma unroll
+            for (int x = 0; x < 16; x += 8) {
+                float u[8];
+#pragma unroll
+                for (int y = 0; y < 8; ++y) u[y] = ut[16 * part + x + y] - v16[x + y];
+                uint4 hi, lo;
+                split8(u, hi, lo);
+                const uint32_t off = tc::swz_off(128, arow, col0 + x);
+                *reinterpret_cast<uint4 *>(sm + sc::kU1 + off) = hi;
+                *reinterpret_cast<uint4 *>(sm + sc::kU2 + off) = lo;
+            }
+        }
+        gdn::fence_proxy_async_smem();
+        tc::fence_before();
+        __syncthreads();
+        // Phase B: Oa = U^T P^T, dS = U^T (dec o K).
+        if (tid == 0) {
+            tc::fence_after();
+#pragma unroll
+            for (int s = 0; s < 4; ++s) {
+                const uint64_t u1 = tc::smem_desc(sb + sc::kU1 + s * 32), u2 = tc::smem_desc(sb + sc::kU2 + s * 32);
+                const uint64_t p1 = tc::smem_desc(sb + sc::kP1 + s * 32), p2 = tc::smem_desc(sb + sc::kP2 + s * 32);
+                const uint64_t k1 = tc::smem_desc(sb + sc::kK1 + s * 32), k2 = tc::smem_desc(sb + sc::kK2 + s * 32);
+                tc::mma_bf16(tm + 128, u1, p1, id64, s ? 1u : 0u);
+                tc::mma_bf16(tm + 128, u1, p2, id64, 1u);
+                tc::mma_bf16(tm + 128, u2, p1, id64, 1u);
+                tc::mma_bf16(tm + 256, u1, k1, id128, s ? 1u : 0u);
+                tc::mma_bf16(tm + 256, u1, k2, id128, 1u);
+                tc::mma_bf16(tm + 256, u2, k1, id128, 1u);
+            }
+            tc::commit(bar);
+            *flag = gdn::mbar_wait_bounded(bar, phase) ? 1 : 0;
         }
         __syncthreads();
-        // S[a][j] = e^{G_last} S[a][j] + sum_i U[i][a] e^{G_last-G_i} K[i][j]
-        const float gl = Gs[n - 1];
-        for (int e = tid; e < kSlice * kD; e += kThreads) {
-            const int r = e / kD, j = e % kD;
-            float acc = 0.f;
-            for (int i = 0; i < n; ++i) acc = fmaf(Us[i * (kSlice + 1) + r] * expf(gl - Gs[i]), Ks[i * (kD + 1) + j], acc);
-            Ss[r * (kD + 1) + j] = fmaf(expf(gl), Ss[r * (kD + 1) + j], acc);
+        if (*flag == 0) {
+            ok = false;
+            break;
         }
+        (void)gdn::mbar_try_wait(bar, phase);
+        phase ^= 1u;
+        tc::fence_after();
+        // Outputs of the chunk's tokens.
+#pragma unroll
+        for (int part = 0; part < 2; ++part) {
+            float oi[16], oa[16];
+            const int col0 = 32 * hc + 16 * part;
+            tc::ld16(tm + lane_base + 64u + uint32_t(col0), oi);
+            tc::ld16(tm + lane_base + 128u + uint32_t(col0), oa);
+#pragma unroll
+            for (int x = 0; x < 16; ++x) {
+                const int t = col0 + x;
+                if (t < n)
+                    a.o[(size_t(t0 + t) * a.h_v + h) * kD + arow] =
+                        gdn::f32_to_bf16(a.q_scale * fmaf(eG[t], oi[x], oa[x]));
+            }
+        }
+        // S <- e^{G_last} S + dS (FP32 master), then its bf16 parts.
+        const float egl = eG[n - 1];
+#pragma unroll
+        for (int part = 0; part < 4; ++part) {
+            float v16[16];
+            tc::ld16(tm + lane_base + 256u + uint32_t(64 * hc + 16 * part), v16);
+#pragma unroll
+            for (int x = 0; x < 16; ++x) sv[16 * part + x] = fmaf(egl, sv[16 * part + x], v16[x]);
+        }
+        write_S();
+        // (the next chunk's staging ends with the proxy fence and barrier the MMAs need)
     }
+    if (ok) {
+        float4 *dp = reinterpret_cast<float4 *>(a.pool + size_t(dst) * a.slot_stride + row_off);
+#pragma unroll
+        for (int x = 0; x < 16; ++x) dp[x] = make_float4(sv[4 * x], sv[4 * x + 1], sv[4 * x + 2], sv[4 * x + 3]);
+    } else if (tid == 0) {
+        gdn::set_status(a.status, GDN_DEV_TIMEOUT);
+    }
+    tc::fence_before();
     __syncthreads();
-    for (int e = tid; e < kSlice * kD; e += kThreads) {
-        const int r = e / kD, j = e % kD;
-        a.pool[size_t(dst) * a.slot_stride + head_off + e] = Ss[r * (kD + 1) + j];
-    }
+    if (warp == 0) tc::tmem_dealloc(tm, sc::kTmemCols);
 }
 
 constexpr size_t kWySmem = wy::kSmem;
-constexpr size_t kScanSmem =
-    sizeof(float) * (kSlice * (kD + 1) + 3 * kC * (kD + 1) + kC * (kSlice + 1) + kC * (kC + 1) + kC);
+constexpr size_t kScanSmem = sc::kSmem;
 
 }  // namespace
 
 extern "C" size_t gdn_prefill_workspace_bytes(const gdn_dims *dims, int32_t nseq, int32_t row_capacity) {
     if (!dims || nseq < 0 || row_capacity < 0) return 0;
     const size_t slots = size_t((row_capacity + kC - 1) / kC) + size_t(nseq);
-    return slots * size_t(dims->h_v) * 2 * kC * kD * sizeof(float);
+    return slots * size_t(dims->h_v) * kWsFloats * sizeof(float);
 }
 
 extern "C" int gdn_chunked_prefill(const gdn_dims *dims, int32_t nseq, int32_t row_capacity,
@@ -448,7 +660,10 @@ extern "C" int gdn_chunked_prefill(const gdn_dims *dims, int32_t nseq, int32_t r
     if (!cu_seqlens || !q || !k || !v || !g || !beta || !pool_layer || !src_slot || !dst_slot || !o)
         return GDN_ERR_NULL;
     const int64_t se = int64_t(dims->h_v) * dims->d_v * dims->d_k;
-    if (slot_stride < se) return GDN_ERR_ARG;
+    if (slot_stride < se || (slot_stride % 4) != 0) return GDN_ERR_ARG;
+    if (!gdn_host::aligned16(pool_layer) || !gdn_host::aligned16(q) || !gdn_host::aligned16(k) ||
+        !gdn_host::aligned16(v))
+        return GDN_ERR_ARG;
     const size_t need = gdn_prefill_workspace_bytes(dims, nseq, row_capacity);
     if (!workspace || workspace_bytes < need) return GDN_ERR_WORKSPACE;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -485,7 +700,7 @@ extern "C" int gdn_chunked_prefill(const gdn_dims *dims, int32_t nseq, int32_t r
         gdn_chunk_wy_kernel<<<dim3(unsigned(gx), dims->h_v), kThreads, kWySmem, st>>>(a);
         if (cudaGetLastError() != cudaSuccess) return GDN_ERR_CUDA;
     }
-    const long long gs = (long long)nseq * dims->h_v * (kD / kSlice);
+    const long long gs = (long long)nseq * dims->h_v;
     gdn_chunk_scan_kernel<<<unsigned(gs), kThreads, kScanSmem, st>>>(a);
     return gdn_host::launch_status(cudaGetLastError());
 }

@@ -1,13 +1,14 @@
 // tcgen05 (5th-generation tensor core) helpers for sm_103a: tensor-memory
 // allocation, shared-memory matrix descriptors for 128-byte-swizzled K-major
-// tiles, single-CTA MMA issue with bf16 operands and fp32 accumulation,
-// completion through an mbarrier, and tensor-memory loads.
+// tiles, single-CTA MMA issue (kind::f16 with bf16 operands, kind::tf32) with
+// fp32 accumulation, completion through an mbarrier, and tensor-memory loads.
 //
 // Tile convention used throughout: a K-major operand tile of R rows stores,
-// for every 64-element slice of K ("atom", 128 bytes of bf16), R rows of 128
-// bytes; the 16-byte chunks of row r are permuted by (chunk ^ (r & 7)) -- the
-// 128-byte swizzle -- and 8-row groups are 1024 bytes apart.  Tiles start on
-// 1024-byte boundaries.
+// for every 128-byte slice of K ("atom": 64 bf16 or 32 tf32 elements), R rows
+// of 128 bytes; the 16-byte chunks of row r are permuted by (chunk ^ (r & 7))
+// -- the 128-byte swizzle -- and 8-row groups are 1024 bytes apart.  Tiles
+// start on 1024-byte boundaries.  One MMA consumes 32 bytes of K (16 bf16 or
+// 8 tf32 elements), so K steps inside an atom advance the start by 32 bytes.
 #pragma once
 
 #include "common.cuh"
@@ -21,6 +22,24 @@ __device__ __forceinline__ uint32_t swz_off(int R, int r, int k) {
     const int chunk = kin >> 3;
     return uint32_t(atom) * uint32_t(R) * 128u + uint32_t(r) * 128u + (uint32_t(chunk ^ (r & 7)) << 4) +
            (uint32_t(kin & 7) << 1);
+}
+
+// Byte offset of fp32/tf32 element (r, k) inside a swizzled K-major tile of R
+// rows: an atom is 32 elements (128 bytes) of K.
+__device__ __forceinline__ uint32_t swz_off_f32(int R, int r, int k) {
+    const int atom = k >> 5;
+    const int kin = k & 31;
+    const int chunk = kin >> 2;
+    return uint32_t(atom) * uint32_t(R) * 128u + uint32_t(r) * 128u + (uint32_t(chunk ^ (r & 7)) << 4) +
+           (uint32_t(kin & 3) << 2);
+}
+
+// Round an fp32 value to tf32 (10 explicit mantissa bits, nearest, ties away),
+// so that the tensor core consumes it without a further truncation.
+__device__ __forceinline__ float round_tf32(float x) {
+    uint32_t r;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+    return __uint_as_float(r);
 }
 
 // Shared-memory matrix descriptor: start address, leading byte offset 16 B
@@ -43,6 +62,24 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
            | (1u << 10)                    // B format: bf16
            | (uint32_t(N >> 3) << 17)      // N / 8
            | (uint32_t(M >> 4) << 24);     // M / 16
+}
+
+// Instruction descriptor for kind::tf32 with tf32 A/B, fp32 D, both K-major.
+__host__ __device__ constexpr uint32_t idesc_tf32(int M, int N) {
+    return (1u << 4)                       // D format: f32
+           | (2u << 7)                     // A format: tf32
+           | (2u << 10)                    // B format: tf32
+           | (uint32_t(N >> 3) << 17)      // N / 8
+           | (uint32_t(M >> 4) << 24);     // M / 16
+}
+
+__device__ __forceinline__ void mma_tf32(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                         uint32_t accumulate) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
 }
 
 __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
