@@ -56,9 +56,11 @@ WORKLOAD_TEXT = {
     "small": "ncu case: 32 requests, 64 slots, 2 layers, K=3",
 }
 
-# DRAM traffic of one gdn_verify launch from an ncu capture (dram__bytes_read.sum + dram__bytes_write.sum),
-# valid only while the kernel source is unchanged.  Filled from profiles/ summaries.
-TRAFFIC = {}
+# DRAM traffic of one gdn_verify launch from an ncu capture (dram__bytes_read.sum + dram__bytes_write.sum)
+# on the full paged256 workload (profiles/dram_verify_paged256.md); reported only while the kernel source
+# is the one that was captured (its digest), otherwise null.
+TRAFFIC = {"gdn_verify": {"src_sha": "ab37bc2427cc02e5", "workload": "paged256",
+                          "bytes_per_launch": 554067968 + 2093959424, "alg_bytes_per_launch": 2709782528}}
 
 
 def src_digest(path):
@@ -214,9 +216,11 @@ class ClockSampler:
 # ---------------------------------------------------------------------------
 
 class Bench:
-    def __init__(self, spec: sy.Spec, dev, rank=0):
+    def __init__(self, spec: sy.Spec, dev, rank=0, arena=False, replay=False):
         from speculative_decoding_hybrid_gb300 import binding as gs
-        from speculative_decoding_hybrid_gb300.step import DecodeLoop, LayerRows, VerifyStep
+        from speculative_decoding_hybrid_gb300.step import ArenaStep, DecodeLoop, LayerRows, ReplayStep, VerifyStep
+        self.arena = arena
+        self.replay = replay
         self.gs, self.spec, self.dev = gs, spec, dev
         d = spec.dims
         self.d = d
@@ -235,10 +239,17 @@ class Bench:
             else:
                 self.pool_c.alloc()
                 seen.add(s)
-        pool = torch.empty((spec.num_slots, spec.layers, d.h_v, d.d_v, d.d_k), dtype=torch.float32, device=dev)
-        sy.pool_state(spec, dev, out=pool)
-        self.vs = VerifyStep(gs.dims(d.h_qk, d.h_v, d.d_k, d.d_v), spec.layers, spec.num_slots, self.cap,
-                             spec.batch, spec.vocab, dev, pool=pool)
+        if arena:
+            self.vs = ArenaStep(gs.dims(d.h_qk, d.h_v, d.d_k, d.d_v), spec.layers, spec.num_slots, self.cap,
+                                spec.batch, spec.vocab, dev)
+            sy.pool_state(spec, dev, out=self.vs.pool)
+            self.vs.point_at_slots(slot_of)
+        else:
+            pool = torch.empty((spec.num_slots, spec.layers, d.h_v, d.d_v, d.d_k), dtype=torch.float32, device=dev)
+            sy.pool_state(spec, dev, out=pool)
+            cls = ReplayStep if replay else VerifyStep
+            self.vs = cls(gs.dims(d.h_qk, d.h_v, d.d_k, d.d_v), spec.layers, spec.num_slots, self.cap,
+                          spec.batch, spec.vocab, dev, pool=pool)
         self.loop = DecodeLoop(self.vs, slot_of, self.pool_c, k_max=spec.k_max)
         self.rows = []
         self.logits, self.targets = [], []
@@ -292,6 +303,10 @@ class Bench:
         s = self.step_no
         ring, p = self.prepare(s)
         vs, loop = self.vs, self.loop
+        if self.arena:
+            return self._arena_step(ring, p, ev)
+        if self.replay:
+            return self._replay_step(ring, p, ev)
         vs.txn = (vs.txn + 1) & 0xFFFFFFFF
         for l in range(self.spec.layers):
             if ev is not None:
@@ -321,6 +336,81 @@ class Bench:
         self.verified += n_ver
         return n_ver, p
 
+    def _arena_step(self, ring, p, ev=None):
+        """Zero-copy commit: verify from each request's location, point the
+        locations at the accepted checkpoints (no state copy)."""
+        from speculative_decoding_hybrid_gb300 import binding as gs
+        vs, loop = self.vs, self.loop
+        B = loop.B
+        vs.txn = (vs.txn + 1) & 0xFFFFFFFF
+        area = vs.txn & 1
+        for l in range(self.spec.layers):
+            x = self.rows[ring][l]
+            if ev is not None:
+                ev["verify"][0].append(torch.cuda.Event(enable_timing=True))
+                ev["verify"][0][-1].record()
+            gs.gdn_verify_at(vs.d, B, vs.cap, loop.cu_rows, x.q, x.k, x.v, x.g, x.beta, vs.arena, vs.total,
+                             vs.loc[l], vs.areas[area][l], vs.tags(B)[l], vs.txn, vs.o[l], vs.status)
+            if ev is not None:
+                ev["verify"][1].append(torch.cuda.Event(enable_timing=True))
+                ev["verify"][1][-1].record()
+        if ev is not None:
+            ev["accept"][0].append(torch.cuda.Event(enable_timing=True))
+            ev["accept"][0][-1].record()
+        vs.accept(B, loop.cu_rows, self.logits[ring], self.tok_d)
+        if ev is not None:
+            ev["accept"][1].append(torch.cuda.Event(enable_timing=True))
+            ev["accept"][1][-1].record()
+            ev["commit"][0].append(torch.cuda.Event(enable_timing=True))
+            ev["commit"][0][-1].record()
+        gs.gdn_commit_at(vs.d, B, vs.L, vs.cap, loop.cu_rows, vs.accept_len, vs.area_off[area],
+                         vs.ckpt_layer_stride, vs.tags(B), vs.txn, vs.loc, vs.status)
+        if ev is not None:
+            ev["commit"][1].append(torch.cuda.Event(enable_timing=True))
+            ev["commit"][1][-1].record()
+        acc, bon, out = loop.readback()
+        n_ver = int(acc.sum().item()) + B
+        loop.finish(acc)
+        self.step_no += 1
+        self.verified += n_ver
+        return n_ver, p
+
+    def _replay_step(self, ring, p, ev=None):
+        """Compact fixed-state replay: each verify commits the previous
+        transaction's accepted rows into the slot, then verifies the new rows."""
+        from speculative_decoding_hybrid_gb300 import binding as gs
+        vs, loop = self.vs, self.loop
+        B = loop.B
+        vs._advance()
+        prev = vs.prev_rows if vs.prev_rows is not None else self.rows[ring]
+        for l in range(self.spec.layers):
+            x, pr = self.rows[ring][l], prev[l]
+            if ev is not None:
+                ev["verify"][0].append(torch.cuda.Event(enable_timing=True))
+                ev["verify"][0][-1].record()
+            gs.gdn_verify_replay(vs.d, B, vs.cap, loop.cu_rows, x.q, x.k, x.v, x.g, x.beta, vs.cap, vs.prev_cu,
+                                 vs.prev_acc, pr.k, pr.v, pr.g, pr.beta, vs.pool_layer(l), vs.slot_stride,
+                                 vs.num_slots, loop.src_slot, loop.dst_slot, vs.o[l], vs.status)
+            if ev is not None:
+                ev["verify"][1].append(torch.cuda.Event(enable_timing=True))
+                ev["verify"][1][-1].record()
+        if ev is not None:
+            ev["accept"][0].append(torch.cuda.Event(enable_timing=True))
+            ev["accept"][0][-1].record()
+        vs.accept(B, loop.cu_rows, self.logits[ring], self.tok_d)
+        if ev is not None:
+            ev["accept"][1].append(torch.cuda.Event(enable_timing=True))
+            ev["accept"][1][-1].record()
+        vs.prev_cu.copy_(loop.cu_rows[:B + 1], non_blocking=True)
+        vs.prev_rows = self.rows[ring]
+        vs.pending = True
+        acc, bon, out = loop.readback()
+        n_ver = int(acc.sum().item()) + B
+        loop.finish(acc)
+        self.step_no += 1
+        self.verified += n_ver
+        return n_ver, p
+
     def step_bytes(self, p):
         """Algorithmic bytes of verify (all layers) and commit for a plan."""
         d = self.d
@@ -328,9 +418,48 @@ class Bench:
         rows = p.decode_rows
         distinct_src = len(set(p.dec_src))
         verify = self.spec.layers * (distinct_src * S + rows * S + rows * S_ROW_IO(d))
-        commit = self.spec.layers * p.n_decode * 2 * S
+        if self.replay:
+            # read the slot, write it back (the replay), row inputs of this and the previous transaction
+            verify = self.spec.layers * (p.n_decode * 2 * S + rows * S_ROW_IO(d) + rows * (S_ROW_IO(d) // 2))
+        commit = 0 if (self.arena or self.replay) else self.spec.layers * p.n_decode * 2 * S
         accept = rows * self.spec.vocab * 2
         return verify, commit, accept
+
+
+def run_zero_copy(spec, dev, args, replay=False):
+    """The same steps with the commit that rewrites locations instead of
+    copying states (verify reads from a state arena), or with compact
+    fixed-state replay (no checkpoints)."""
+    b = Bench(spec, dev, 0, arena=not replay, replay=replay)
+    b.precompute_drafts(args.warmup + args.steps)
+    for _ in range(args.warmup):
+        b.step()
+    torch.cuda.synchronize()
+    ev = {"verify": ([], []), "accept": ([], []), "commit": ([], [])}
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    start.record()
+    tok, vbytes = 0, 0
+    for _ in range(args.steps):
+        n, p = b.step(ev)
+        tok += n
+        vbytes += b.step_bytes(p)[0]
+    end.record()
+    torch.cuda.synchronize()
+    ms = start.elapsed_time(end)
+    avg = lambda k: sum(x.elapsed_time(y) for x, y in zip(*ev[k])) / max(len(ev[k][0]), 1)
+    v_ms, c_ms = avg("verify"), avg("commit")
+    n_ver = len(ev["verify"][0])
+    peak, _ = load_peaks()
+    gbs = vbytes / ((v_ms * n_ver + c_ms * args.steps) * 1e-3) / 1e9
+    if int(b.vs.status.item()) != 0:
+        raise RuntimeError("zero-copy loop status %d" % int(b.vs.status.item()))
+    res = {"value": tok / (ms * 1e-3), "unit": "verified tokens/s", "ms_per_step": ms / args.steps,
+           "verify_ms": v_ms, "commit_at_ms": c_ms, "verify_commit_gbs": gbs, "verify_commit_frac": gbs / peak,
+           "state_gib": (b.vs.arena.numel() if not replay else b.vs.pool.numel()) * 4 / 2 ** 30}
+    del b
+    torch.cuda.empty_cache()
+    return res
 
 
 def stage_e2e(b: Bench):
@@ -484,6 +613,12 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-prefill", action="store_true")
+    ap.add_argument("--zero-copy", dest="zero_copy", action="store_true", default=True,
+                    help="also time the zero-copy commit (state arena) on the same workload")
+    ap.add_argument("--no-zero-copy", dest="zero_copy", action="store_false")
+    ap.add_argument("--replay", dest="replay", action="store_true", default=True,
+                    help="also time compact fixed-state replay (no checkpoints) on the same workload")
+    ap.add_argument("--no-replay", dest="replay", action="store_false")
     args = ap.parse_args()
     if args.workload in PREFILL_SETS:
         if args.impl == "reference":
@@ -563,10 +698,13 @@ def main():
     traffic = tr["bytes_per_launch"] * (v_per_launch / tr["alg_bytes_per_launch"]) \
         if tr and tr["src_sha"] == src_digest(src) and tr.get("workload") == args.workload else None
 
+    l2desc = "inputs larger than L2: state pool %.1f GiB, checkpoints %.1f GiB, ring of %d input sets" % (
+        b.vs.pool.numel() * 4 / 2 ** 30, b.vs.ckpt.numel() * 4 / 2 ** 30, spec.ring)
     e2e = None
     if not args.no_e2e:
         host, srows, slog = stage_e2e(b)
         val, h2d, d2h = run_e2e(b, host, srows, slog, args.e2e_steps, 3)
+        del host, srows, slog
         if world > 1:
             t = torch.tensor([val], device=dev, dtype=torch.float64)
             dist.all_reduce(t)
@@ -579,12 +717,30 @@ def main():
             dist.barrier()
             dist.destroy_process_group()
         return
+    def guarded(fn, *a, **k):
+        """A secondary measurement that fails records its error instead of
+        losing the main line."""
+        try:
+            return fn(*a, **k)
+        except Exception as e:  # noqa: BLE001
+            torch.cuda.synchronize()
+            return {"error": "%s: %s" % (type(e).__name__, e)}
+
     prefill = None
     if not args.no_prefill and args.workload == "paged256":
-        prefill = bench_prefill(dev, sy.prefill_lengths())
+        prefill = guarded(bench_prefill, dev, sy.prefill_lengths())
+    zero_copy = replay = None
+    if (args.zero_copy or args.replay) and world == 1:
+        del b
+        torch.cuda.empty_cache()
+        if args.replay:
+            replay = guarded(run_zero_copy, spec, dev, args, replay=True)
+            torch.cuda.empty_cache()
+        if args.zero_copy:
+            zero_copy = guarded(run_zero_copy, spec, dev, args)
     cpu = None
     if not args.no_cpu_baseline and world == 1:
-        cpu = cpu_baseline(spec)
+        cpu = guarded(cpu_baseline, spec)
     line = {
         "metric": "verified tokens/s and GDN verify+commit HBM GB/s (% of GB300 peak)",
         "value": tok_all / (ms * 1e-3),
@@ -599,8 +755,7 @@ def main():
         "dtype": "f32",
         "data": "synthetic",
         "config": {"workload": args.workload, "desc": WORKLOAD_TEXT[args.workload],
-                   "l2": "inputs larger than L2: state pool %.1f GiB, checkpoints %.1f GiB, ring of %d input sets" % (
-                       b.vs.pool.numel() * 4 / 2 ** 30, b.vs.ckpt.numel() * 4 / 2 ** 30, spec.ring),
+                   "l2": l2desc,
                    "parallelism": "replicas (requests sharded, no collective)" if world > 1 else "single GPU"},
         "verify_commit_gbs": vc_gbs,
         "verify_commit_frac": vc_gbs / peak,
@@ -616,6 +771,8 @@ def main():
         "cpu_baseline": cpu,
         "acceptance": {"verified_tokens": tok, "requests": spec.batch},
         "prefill": prefill,
+        "zero_copy_commit": zero_copy,
+        "fixed_state_replay": replay,
     }
     print(json.dumps(line), flush=True)
     if world > 1:

@@ -205,6 +205,95 @@ int gdn_commit(const gdn_dims *dims, int32_t B, int32_t num_layers,
                int32_t num_slots, const int32_t *dst_slot,
                uint32_t *dev_status, void *stream);
 
+/* ------------------------------------------------------------------------
+ * Zero-copy commit (the slot table points at the accepted checkpoint).
+ * A "state arena" is one fp32 buffer holding the pool slots and two
+ * checkpoint areas used on alternate transactions; the state of (request r,
+ * layer l) lives at state_base + loc[l*B + r] (element offset).  Instead of
+ * copying 2*S_bytes per (request, layer) the commit rewrites loc; the next
+ * transaction verifies from there while writing its checkpoints into the
+ * other area ([ENGINE] Correctness fix: rollback to the accepted checkpoint;
+ * H200 RC4 evidence: the paged Engine addresses state through a table).
+ * ------------------------------------------------------------------------ */
+
+/*
+ * gdn_verify_at -- gdn_verify whose start states are read at
+ *   state_base + src_off[r] (device int64, element offsets, multiples of 4,
+ *   each state fully inside [0, state_elems_total)); everything else as in
+ *   gdn_verify.  An offset out of range sets GDN_DEV_SLOT_OOR and skips r.
+ */
+int gdn_verify_at(const gdn_dims *dims, int32_t B, int32_t row_capacity,
+                  const int32_t *cu_rows,
+                  const gdn_bf16 *q, const gdn_bf16 *k, const gdn_bf16 *v,
+                  const float *g, const float *beta,
+                  const float *state_base, int64_t state_elems_total,
+                  const int64_t *src_off,
+                  float *ckpt_layer, uint64_t *ckpt_tag, uint32_t txn,
+                  gdn_bf16 *o, uint32_t *dev_status, void *stream);
+
+/*
+ * gdn_commit_at -- for every (request r, layer l) whose checkpoint tag passes
+ *   the checks of gdn_commit, set loc[l*B + r] = ckpt_off +
+ *   l*ckpt_layer_stride + (cu_rows[r] + accept_len[r]) * S_elems, the element
+ *   offset (from the same state_base) of the accepted checkpoint.  Refused
+ *   pairs keep their location.  No state bytes move.
+ */
+int gdn_commit_at(const gdn_dims *dims, int32_t B, int32_t num_layers,
+                  int32_t row_capacity, const int32_t *cu_rows,
+                  const int32_t *accept_len,
+                  int64_t ckpt_off, int64_t ckpt_layer_stride,
+                  const uint64_t *ckpt_tag, uint32_t txn,
+                  int64_t *loc, uint32_t *dev_status, void *stream);
+
+/*
+ * gdn_materialize -- copy the state at state_base + loc[l*B + r] into
+ *   pool + dst_slot[r]*slot_stride + l*layer_stride for every (r, l) (a
+ *   request leaving the batch, or whose checkpoint area is about to be
+ *   reused).  Pairs already in place are skipped; a location out of range or
+ *   a bad slot sets GDN_DEV_SLOT_OOR.  Sources and destinations must not
+ *   overlap other than being equal.
+ */
+int gdn_materialize(const gdn_dims *dims, int32_t B, int32_t num_layers,
+                    const float *state_base, int64_t state_elems_total,
+                    const int64_t *loc, float *pool, int64_t slot_stride,
+                    int64_t layer_stride, int32_t num_slots,
+                    const int32_t *dst_slot, uint32_t *dev_status, void *stream);
+
+/* ------------------------------------------------------------------------
+ * Compact fixed-state replay ([ENGINE] closing comment: the runtime rebuilt
+ * on compact fixed-state replay without dense recurrent checkpoints).
+ * ------------------------------------------------------------------------ */
+
+/*
+ * gdn_verify_replay -- verification without checkpoints.  For request r:
+ *  1. the previous transaction's accepted rows, prev_cu_rows[r] ..
+ *     prev_cu_rows[r] + prev_accept_len[r] (none when prev_accept_len[r] < 0),
+ *     are run from slot src_slot[r] through the state update of
+ *     gdn_decode_step, and the result is written to slot dst_slot[r] (also
+ *     when nothing is pending but dst_slot[r] != src_slot[r]).  This is the
+ *     commit of the previous transaction, bit-identical to gdn_commit of its
+ *     accepted checkpoint;
+ *  2. this transaction's rows cu_rows[r] .. cu_rows[r+1]-1 (0..GDN_MAX_ROWS;
+ *     0 rows only commits) run from that state and write o; no state is kept.
+ *   prev_k, prev_v (bf16) and prev_g, prev_beta (fp32) are the previous
+ *   transaction's rows in the packed layout of gdn_verify (prev_capacity
+ *   rows; q is not needed).  Per (request, layer) this moves S_bytes in and
+ *   at most S_bytes out instead of (K+2) S_bytes in and (K+2) out.
+ *   Rows past either capacity or more accepted rows than existed set
+ *   GDN_DEV_ROWS_BAD and skip the request.
+ */
+int gdn_verify_replay(const gdn_dims *dims, int32_t B, int32_t row_capacity,
+                      const int32_t *cu_rows,
+                      const gdn_bf16 *q, const gdn_bf16 *k, const gdn_bf16 *v,
+                      const float *g, const float *beta,
+                      int32_t prev_capacity, const int32_t *prev_cu_rows,
+                      const int32_t *prev_accept_len,
+                      const gdn_bf16 *prev_k, const gdn_bf16 *prev_v,
+                      const float *prev_g, const float *prev_beta,
+                      float *pool_layer, int64_t slot_stride, int32_t num_slots,
+                      const int32_t *src_slot, const int32_t *dst_slot,
+                      gdn_bf16 *o, uint32_t *dev_status, void *stream);
+
 /*
  * gdn_chunked_prefill -- chunked (WY/UT) GatedDeltaNet prefill of one layer
  * ([ENGINE] Correctness fix: the chunked plan publishes the final state but

@@ -29,7 +29,8 @@ REQ_DECODE, REQ_PREFILL = 0, 1
 PLAN_RECURRENT, PLAN_CHUNKED = 0, 1
 
 EXPORTS = ["gdn_decode_step", "gdn_verify", "mtp_accept_workspace_bytes", "mtp_greedy_accept",
-           "mtp_greedy_accept_noalloc", "gdn_commit",
+           "mtp_greedy_accept_noalloc", "gdn_commit", "gdn_verify_at", "gdn_commit_at", "gdn_materialize",
+           "gdn_verify_replay",
            "gdn_prefill_workspace_bytes", "gdn_chunked_prefill", "gdn_pool_init", "gdn_pool_alloc",
            "gdn_pool_share", "gdn_pool_release", "plan_transaction", "gdn_pool_apply", "gdn_pool_abort",
            "gdn_status_string"]
@@ -87,6 +88,10 @@ def _load():
         "mtp_greedy_accept": [I32, I32, P, P, I64, I64, P, P, P, P, P, P, P, SZ, P, P],
         "mtp_greedy_accept_noalloc": [I32, I32, P, P, I64, I64, P, P, P, P, P, P, P, P],
         "gdn_commit": [DP, I32, I32, I32, P, P, P, I64, P, U32, P, I64, I64, I32, P, P, P],
+        "gdn_verify_at": [DP, I32, I32, P, P, P, P, P, P, P, I64, P, P, P, U32, P, P, P],
+        "gdn_commit_at": [DP, I32, I32, I32, P, P, I64, I64, P, U32, P, P, P],
+        "gdn_materialize": [DP, I32, I32, P, I64, P, P, I64, I64, I32, P, P, P],
+        "gdn_verify_replay": [DP, I32, I32, P, P, P, P, P, P, I32, P, P, P, P, P, P, P, I64, I32, P, P, P, P, P],
         "gdn_prefill_workspace_bytes": [DP, I32, I32],
         "gdn_chunked_prefill": [DP, I32, I32, P, I32, P, P, P, P, P, P, I64, I32, P, P, P, I32, P, SZ, P, P],
         "gdn_pool_init": [ctypes.POINTER(gdn_pool), I32, P, P, P],
@@ -192,6 +197,38 @@ def gdn_commit(d: gdn_dims, B, num_layers, row_capacity, cu_rows, accept_len, ck
     return _check("gdn_commit", lib.gdn_commit(
         ctypes.byref(d), B, num_layers, row_capacity, _ptr(cu_rows), _ptr(accept_len), _ptr(ckpt),
         ckpt_layer_stride, _ptr(ckpt_tag), txn, _ptr(pool), slot_stride, layer_stride, num_slots, _ptr(dst_slot),
+        _ptr(dev_status), _stream(stream)))
+
+
+def gdn_verify_at(d: gdn_dims, B, row_capacity, cu_rows, q, k, v, g, beta, state_base, state_elems_total, src_off,
+                  ckpt_layer, ckpt_tag, txn, o, dev_status, stream=None):
+    return _check("gdn_verify_at", lib.gdn_verify_at(
+        ctypes.byref(d), B, row_capacity, _ptr(cu_rows), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
+        _ptr(state_base), state_elems_total, _ptr(src_off), _ptr(ckpt_layer), _ptr(ckpt_tag), txn, _ptr(o),
+        _ptr(dev_status), _stream(stream)))
+
+
+def gdn_commit_at(d: gdn_dims, B, num_layers, row_capacity, cu_rows, accept_len, ckpt_off, ckpt_layer_stride,
+                  ckpt_tag, txn, loc, dev_status, stream=None):
+    return _check("gdn_commit_at", lib.gdn_commit_at(
+        ctypes.byref(d), B, num_layers, row_capacity, _ptr(cu_rows), _ptr(accept_len), ckpt_off, ckpt_layer_stride,
+        _ptr(ckpt_tag), txn, _ptr(loc), _ptr(dev_status), _stream(stream)))
+
+
+def gdn_materialize(d: gdn_dims, B, num_layers, state_base, state_elems_total, loc, pool, slot_stride, layer_stride,
+                    num_slots, dst_slot, dev_status, stream=None):
+    return _check("gdn_materialize", lib.gdn_materialize(
+        ctypes.byref(d), B, num_layers, _ptr(state_base), state_elems_total, _ptr(loc), _ptr(pool), slot_stride,
+        layer_stride, num_slots, _ptr(dst_slot), _ptr(dev_status), _stream(stream)))
+
+
+def gdn_verify_replay(d: gdn_dims, B, row_capacity, cu_rows, q, k, v, g, beta, prev_capacity, prev_cu_rows,
+                      prev_accept_len, prev_k, prev_v, prev_g, prev_beta, pool_layer, slot_stride, num_slots, src_slot,
+                      dst_slot, o, dev_status, stream=None):
+    return _check("gdn_verify_replay", lib.gdn_verify_replay(
+        ctypes.byref(d), B, row_capacity, _ptr(cu_rows), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
+        prev_capacity, _ptr(prev_cu_rows), _ptr(prev_accept_len), _ptr(prev_k), _ptr(prev_v), _ptr(prev_g),
+        _ptr(prev_beta), _ptr(pool_layer), slot_stride, num_slots, _ptr(src_slot), _ptr(dst_slot), _ptr(o),
         _ptr(dev_status), _stream(stream)))
 
 

@@ -69,7 +69,140 @@ __global__ void __launch_bounds__(kThreads) gdn_commit_kernel(const CommitArgs a
     }
 }
 
+// Zero-copy commit: each (request, layer) location is pointed at its accepted
+// checkpoint, under the same tag checks as the copying commit.
+struct LocArgs {
+    int32_t B, L, row_capacity;
+    const int32_t *cu_rows, *accept_len;
+    int64_t ckpt_off, ckpt_layer_stride, s_elems;
+    const uint64_t *tag;
+    uint32_t txn;
+    int64_t *loc;
+    uint32_t *status;
+};
+
+__global__ void __launch_bounds__(kThreads) gdn_commit_at_kernel(const LocArgs a) {
+    const long long idx = (long long)blockIdx.x * kThreads + threadIdx.x;
+    if (idx >= (long long)a.B * a.L) return;
+    if (a.status && (*reinterpret_cast<volatile uint32_t *>(a.status) & GDN_DEV_TIMEOUT)) return;
+    const int r = int(idx % a.B);
+    const int l = int(idx / a.B);
+    const uint64_t tag = a.tag[int64_t(l) * a.B + r];
+    const int j = a.accept_len[r];
+    const int t0 = a.cu_rows[r];
+    const uint32_t n = uint32_t(tag & 0xffffffffull);
+    uint32_t bad = 0;
+    if (uint32_t(tag >> 32) != a.txn || n == 0)
+        bad = GDN_DEV_CKPT_UNWRITTEN;
+    else if (j < 0 || uint32_t(j) >= n)
+        bad = GDN_DEV_ACCEPT_BAD;
+    else if (t0 < 0 || int64_t(t0) + j >= a.row_capacity)
+        bad = GDN_DEV_ROWS_BAD;
+    if (bad) {
+        gdn::set_status(a.status, bad);
+        return;
+    }
+    a.loc[int64_t(l) * a.B + r] = a.ckpt_off + int64_t(l) * a.ckpt_layer_stride + (int64_t(t0) + j) * a.s_elems;
+}
+
+// Copies every (request, layer) state from its location into the request's slot.
+struct MatArgs {
+    int32_t B, L, num_slots, chunks;
+    const float *base;
+    int64_t max_off, s_elems, slot_stride, layer_stride;
+    const int64_t *loc;
+    float *pool;
+    const int32_t *dst_slot;
+    uint32_t *status;
+};
+
+__global__ void __launch_bounds__(kThreads) gdn_materialize_kernel(const MatArgs a) {
+    const long long idx = blockIdx.x;
+    const int c = int(idx % a.chunks);
+    const long long rl = idx / a.chunks;
+    const int r = int(rl % a.B);
+    const int l = int(rl / a.B);
+    const int64_t off = a.loc[int64_t(l) * a.B + r];
+    const int dst = a.dst_slot[r];
+    if (off < 0 || off > a.max_off || (off & 3) != 0 || dst < 0 || dst >= a.num_slots) {
+        if (c == 0 && threadIdx.x == 0) gdn::set_status(a.status, GDN_DEV_SLOT_OOR);
+        return;
+    }
+    const float *src = a.base + off;
+    float *dp = a.pool + int64_t(dst) * a.slot_stride + int64_t(l) * a.layer_stride;
+    if (src == dp) return;  // already in place
+    const int64_t o0 = int64_t(c) * kChunkFloats;
+    const int n4 = int(min(int64_t(kChunkFloats), a.s_elems - o0) / 4);
+    const float4 *s4 = reinterpret_cast<const float4 *>(src + o0);
+    float4 *d4 = reinterpret_cast<float4 *>(dp + o0);
+    for (int i = threadIdx.x; i < n4; i += kThreads) __stcs(d4 + i, __ldcs(s4 + i));
+}
+
 }  // namespace
+
+extern "C" int gdn_commit_at(const gdn_dims *dims, int32_t B, int32_t num_layers, int32_t row_capacity,
+                             const int32_t *cu_rows, const int32_t *accept_len, int64_t ckpt_off,
+                             int64_t ckpt_layer_stride, const uint64_t *ckpt_tag, uint32_t txn, int64_t *loc,
+                             uint32_t *dev_status, void *stream) {
+    if (!dims) return GDN_ERR_NULL;
+    if (!gdn_host::dims_ok(dims)) return GDN_ERR_SHAPE;
+    if (B < 0 || num_layers < 0 || row_capacity < 0 || ckpt_off < 0) return GDN_ERR_ARG;
+    if (B == 0 || num_layers == 0) return GDN_OK;
+    if (!cu_rows || !accept_len || !ckpt_tag || !loc) return GDN_ERR_NULL;
+    const int64_t se = int64_t(dims->h_v) * dims->d_v * dims->d_k;
+    if (ckpt_layer_stride < se * row_capacity || (ckpt_off % 4) != 0 || (ckpt_layer_stride % 4) != 0)
+        return GDN_ERR_ARG;
+    LocArgs a{};
+    a.B = B;
+    a.L = num_layers;
+    a.row_capacity = row_capacity;
+    a.cu_rows = cu_rows;
+    a.accept_len = accept_len;
+    a.ckpt_off = ckpt_off;
+    a.ckpt_layer_stride = ckpt_layer_stride;
+    a.s_elems = se;
+    a.tag = ckpt_tag;
+    a.txn = txn;
+    a.loc = loc;
+    a.status = dev_status;
+    const long long n = (long long)B * num_layers;
+    gdn_commit_at_kernel<<<unsigned((n + kThreads - 1) / kThreads), kThreads, 0, static_cast<cudaStream_t>(stream)>>>(
+        a);
+    return gdn_host::launch_status(cudaGetLastError());
+}
+
+extern "C" int gdn_materialize(const gdn_dims *dims, int32_t B, int32_t num_layers, const float *state_base,
+                               int64_t state_elems_total, const int64_t *loc, float *pool, int64_t slot_stride,
+                               int64_t layer_stride, int32_t num_slots, const int32_t *dst_slot,
+                               uint32_t *dev_status, void *stream) {
+    if (!dims) return GDN_ERR_NULL;
+    if (!gdn_host::dims_ok(dims)) return GDN_ERR_SHAPE;
+    if (B < 0 || num_layers < 0 || num_slots <= 0) return GDN_ERR_ARG;
+    if (B == 0 || num_layers == 0) return GDN_OK;
+    if (!state_base || !loc || !pool || !dst_slot) return GDN_ERR_NULL;
+    const int64_t se = int64_t(dims->h_v) * dims->d_v * dims->d_k;
+    if (state_elems_total < se || layer_stride < se || slot_stride < layer_stride * num_layers) return GDN_ERR_ARG;
+    if ((slot_stride | layer_stride) % 4 != 0 || !gdn_host::aligned16(state_base) || !gdn_host::aligned16(pool))
+        return GDN_ERR_ARG;
+    MatArgs a{};
+    a.B = B;
+    a.L = num_layers;
+    a.num_slots = num_slots;
+    a.chunks = int((se + kChunkFloats - 1) / kChunkFloats);
+    a.base = state_base;
+    a.max_off = state_elems_total - se;
+    a.s_elems = se;
+    a.slot_stride = slot_stride;
+    a.layer_stride = layer_stride;
+    a.loc = loc;
+    a.pool = pool;
+    a.dst_slot = dst_slot;
+    a.status = dev_status;
+    const long long grid = (long long)B * num_layers * a.chunks;
+    if (grid > 0x7fffffffLL) return GDN_ERR_ARG;
+    gdn_materialize_kernel<<<unsigned(grid), kThreads, 0, static_cast<cudaStream_t>(stream)>>>(a);
+    return gdn_host::launch_status(cudaGetLastError());
+}
 
 extern "C" int gdn_commit(const gdn_dims *dims, int32_t B, int32_t num_layers, int32_t row_capacity,
                           const int32_t *cu_rows, const int32_t *accept_len, const float *ckpt,

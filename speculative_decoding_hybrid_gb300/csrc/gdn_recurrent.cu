@@ -37,15 +37,24 @@ struct Lay {
     static constexpr int LPR = (DK / 4) < 8 ? (DK / 4) : 8;  // lanes per state row
     static constexpr int NV = DK / (4 * LPR);                // float4 slices per lane
     static constexpr int RPW = 32 / LPR;                     // rows per warp per pass
-    static constexpr int RPP = kWarps * RPW;                 // rows per CTA pass
-    static constexpr int PASSES = 2;
-    static constexpr int RB = RPP * PASSES;                  // state rows per CTA
+    static constexpr int RB = kWarps * RPW;                  // state rows per CTA
     static constexpr size_t kTileOff = 128;
     static constexpr size_t kKqOff = kTileOff + size_t(RB) * DK * 4;
     static constexpr size_t kVOff = kKqOff + size_t(GDN_MAX_ROWS) * 2 * DK * 2;
     static constexpr size_t kGOff = kVOff + size_t(GDN_MAX_ROWS) * RB * 4;
     static constexpr size_t kSmem = kGOff + 2 * GDN_MAX_ROWS * 4;
+    // replay mode: the previous transaction's accepted rows (k, v, g, beta)
+    static constexpr size_t kRkOff = kSmem;
+    static constexpr size_t kRvOff = kRkOff + size_t(GDN_MAX_ROWS) * DK * 2;
+    static constexpr size_t kRgOff = kRvOff + size_t(GDN_MAX_ROWS) * RB * 4;
+    static constexpr size_t kSmemReplay = kRgOff + 2 * GDN_MAX_ROWS * 4;
 };
+
+// Kernel modes: one token into a destination slot; K+1 rows with a
+// checkpoint per row; the same reading the start state at an arena offset;
+// replay of the previous transaction's accepted rows into the destination
+// slot followed by outputs for the new rows.
+enum { kDecode = 0, kVerify = 1, kVerifyAt = 2, kReplay = 3 };
 
 struct RecArgs {
     const int32_t *cu_rows;
@@ -56,6 +65,13 @@ struct RecArgs {
     int64_t slot_stride;
     int32_t num_slots;
     const int32_t *src_slot, *dst_slot;
+    const int64_t *src_off;  // start state at pool_src + src_off[r] (located variant)
+    int64_t max_off;         // largest valid src_off
+    // replay mode: rows prev_cu[r] .. prev_cu[r] + prev_acc[r] of the previous transaction
+    const int32_t *prev_cu, *prev_acc;
+    const uint16_t *pk, *pv;
+    const float *pg, *pbeta;
+    int32_t prev_capacity;
     float *ckpt;
     uint64_t *ckpt_tag;
     uint32_t txn;
@@ -88,11 +104,12 @@ __device__ __forceinline__ float lane_dot(const float4 (&s)[NV], const float4 (&
     return acc;
 }
 
-// One token for one state row held by a lane group.  Returns the row's
-// output value (before q_scale).  Shared by decode and verify.
+// The state half of a token: prediction S k, then S <- alpha S + u k^T.
+// row_update below performs exactly these operations and then the output dot
+// product, so a replayed state is bit-identical to a verified checkpoint.
 template <int NV, int LPR>
-__device__ __forceinline__ float row_update(float4 (&s)[NV], const float4 (&kf)[NV], const float4 (&qf)[NV],
-                                            float alpha, float b, float vv) {
+__device__ __forceinline__ void row_advance(float4 (&s)[NV], const float4 (&kf)[NV], float alpha, float b,
+                                            float vv) {
     const float pred = group_sum<LPR>(lane_dot<NV>(s, kf));
     const float u = __fmul_rn(b, __fsub_rn(vv, __fmul_rn(alpha, pred)));
 #pragma unroll
@@ -102,6 +119,14 @@ __device__ __forceinline__ float row_update(float4 (&s)[NV], const float4 (&kf)[
         s[c].z = __fmaf_rn(u, kf[c].z, __fmul_rn(alpha, s[c].z));
         s[c].w = __fmaf_rn(u, kf[c].w, __fmul_rn(alpha, s[c].w));
     }
+}
+
+// One token for one state row held by a lane group.  Returns the row's
+// output value (before q_scale).  Shared by decode and verify.
+template <int NV, int LPR>
+__device__ __forceinline__ float row_update(float4 (&s)[NV], const float4 (&kf)[NV], const float4 (&qf)[NV],
+                                            float alpha, float b, float vv) {
+    row_advance<NV, LPR>(s, kf, alpha, b, vv);
     return group_sum<LPR>(lane_dot<NV>(s, qf));
 }
 
@@ -110,9 +135,13 @@ __device__ __forceinline__ float4 bf16x4_to_f32(uint2 w) {
                        __uint_as_float(w.y & 0xffff0000u));
 }
 
-template <int DK, bool VERIFY>
-__global__ void __launch_bounds__(kThreads, 2) gdn_recurrent_kernel(const RecArgs a) {
+template <int DK, int MODE>
+__global__ void __launch_bounds__(kThreads, 4) gdn_recurrent_kernel(const RecArgs a) {
     using L = Lay<DK>;
+    constexpr bool VERIFY = (MODE == kVerify || MODE == kVerifyAt);
+    constexpr bool AT = (MODE == kVerifyAt);
+    constexpr bool REPLAY = (MODE == kReplay);
+    constexpr bool WRITES_SLOT = (MODE == kDecode || MODE == kReplay);
     extern __shared__ __align__(128) unsigned char smem[];
     uint64_t *bar = reinterpret_cast<uint64_t *>(smem);
     int *flag = reinterpret_cast<int *>(smem + 64);
@@ -131,19 +160,42 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_recurrent_kernel(const RecArg
 
     int t0, nrows;
     uint32_t bad = 0;
-    if (VERIFY) {
+    if (VERIFY || REPLAY) {
         t0 = a.cu_rows[r];
         const int t1 = a.cu_rows[r + 1];
         nrows = t1 - t0;
-        if (t0 < 0 || nrows < 1 || nrows > GDN_MAX_ROWS || t1 > a.row_capacity) bad |= GDN_DEV_ROWS_BAD;
+        const int min_rows = REPLAY ? 0 : 1;
+        if (t0 < 0 || nrows < min_rows || nrows > GDN_MAX_ROWS || t1 > a.row_capacity) bad |= GDN_DEV_ROWS_BAD;
     } else {
         t0 = r;
         nrows = 1;
     }
-    const int src = a.src_slot[r];
-    if (src < 0 || src >= a.num_slots) bad |= GDN_DEV_SLOT_OOR;
+    int p0 = 0, nrep = 0;  // replay rows p0 .. p0 + nrep - 1 of the previous transaction
+    if (REPLAY) {
+        const int acc = a.prev_acc[r];
+        if (acc >= 0) {
+            p0 = a.prev_cu[r];
+            nrep = acc + 1;
+            const int p1 = a.prev_cu[r + 1];
+            if (p0 < 0 || p0 + nrep > p1 || nrep > GDN_MAX_ROWS || p1 > a.prev_capacity) bad |= GDN_DEV_ROWS_BAD;
+        }
+    }
+    const float *src_base = a.pool_src;
+    if (AT) {
+        const int64_t off = a.src_off[r];
+        if (off < 0 || off > a.max_off || (off & 3) != 0)
+            bad |= GDN_DEV_SLOT_OOR;
+        else
+            src_base = a.pool_src + off;
+    } else {
+        const int src = a.src_slot[r];
+        if (src < 0 || src >= a.num_slots)
+            bad |= GDN_DEV_SLOT_OOR;
+        else
+            src_base = a.pool_src + size_t(src) * a.slot_stride;
+    }
     int dst = 0;
-    if (!VERIFY) {
+    if (WRITES_SLOT) {
         dst = a.dst_slot[r];
         if (dst < 0 || dst >= a.num_slots) bad |= GDN_DEV_SLOT_OOR;
     }
@@ -163,7 +215,7 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_recurrent_kernel(const RecArg
     if (tid == 0) {
         gdn::mbar_init(bar, 1);
         gdn::mbar_arrive_expect_tx(bar, uint32_t(nr) * DK * 4u);
-        gdn::bulk_g2s(tile, a.pool_src + size_t(src) * a.slot_stride + tile_off, uint32_t(nr) * DK * 4u, bar);
+        gdn::bulk_g2s(tile, src_base + tile_off, uint32_t(nr) * DK * 4u, bar);
     }
 
     // Stage k and q rows (bf16) of this request's qk-head, 16 B per load.
@@ -186,6 +238,25 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_recurrent_kernel(const RecArg
         gsm[tid] = a.g[size_t(t0 + tid) * a.h_v + h];
         bsm[tid] = a.beta[size_t(t0 + tid) * a.h_v + h];
     }
+    uint16_t *rk = reinterpret_cast<uint16_t *>(smem + L::kRkOff);
+    float *rv = reinterpret_cast<float *>(smem + L::kRvOff);
+    float *rg = reinterpret_cast<float *>(smem + L::kRgOff);
+    float *rbeta = rg + GDN_MAX_ROWS;
+    if (REPLAY) {
+        for (int i = tid; i < nrep * VPR; i += kThreads) {
+            const int t = i / VPR, c = i - t * VPR;
+            *reinterpret_cast<uint4 *>(rk + t * DK + c * 8) =
+                __ldg(reinterpret_cast<const uint4 *>(a.pk + (size_t(p0 + t) * a.h_qk + hq) * DK + c * 8));
+        }
+        for (int i = tid; i < nrep * nr; i += kThreads) {
+            const int t = i / nr, row = i - t * nr;
+            rv[t * L::RB + row] = gdn::bf16_to_f32(a.pv[(size_t(p0 + t) * a.h_v + h) * a.dv + row0 + row]);
+        }
+        if (tid < nrep) {
+            rg[tid] = a.pg[size_t(p0 + tid) * a.h_v + h];
+            rbeta[tid] = a.pbeta[size_t(p0 + tid) * a.h_v + h];
+        }
+    }
     if (tid == 0) *flag = gdn::mbar_wait_bounded(bar, 0) ? 1 : 0;
     __syncthreads();
     if (*flag == 0) {
@@ -198,20 +269,36 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_recurrent_kernel(const RecArg
     const int lane = tid & 31;
     const int gi = lane / L::LPR;
     const int li = lane - gi * L::LPR;
+    const int lr = warp * L::RPW + gi;  // state row of this lane group within the tile
+    const bool act = lr < nr;
 
-    float4 s[L::PASSES][L::NV];
-    int lr[L::PASSES];
-    bool act[L::PASSES];
+    float4 s[L::NV];
 #pragma unroll
-    for (int p = 0; p < L::PASSES; ++p) {
-        lr[p] = p * L::RPP + warp * L::RPW + gi;
-        act[p] = lr[p] < nr;
+    for (int c = 0; c < L::NV; ++c)
+        s[c] = act ? *reinterpret_cast<const float4 *>(tile + lr * DK + (c * L::LPR + li) * 4)
+                   : make_float4(0.f, 0.f, 0.f, 0.f);
+
+    if (REPLAY) {
+        // The previous transaction's accepted rows: the state half of each token.
+        for (int t = 0; t < nrep; ++t) {
+            const float alpha = expf(rg[t]);
+            const float b = rbeta[t];
+            float4 kf[L::NV];
 #pragma unroll
-        for (int c = 0; c < L::NV; ++c)
-            s[p][c] = act[p] ? *reinterpret_cast<const float4 *>(tile + lr[p] * DK + (c * L::LPR + li) * 4)
-                             : make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int c = 0; c < L::NV; ++c)
+                kf[c] = bf16x4_to_f32(*reinterpret_cast<const uint2 *>(rk + t * DK + (c * L::LPR + li) * 4));
+            const float vv = act ? rv[t * L::RB + lr] : 0.f;
+            row_advance<L::NV, L::LPR>(s, kf, alpha, b, vv);
+        }
+        // The replayed state is the request's committed state (also copied
+        // when nothing is pending but the request moves to a fresh slot).
+        const bool moved = a.src_slot[r] != dst;
+        if (act && (nrep > 0 || moved)) {
+            float *dp = a.pool_dst + size_t(dst) * a.slot_stride + tile_off;
+#pragma unroll
+            for (int c = 0; c < L::NV; ++c) *reinterpret_cast<float4 *>(dp + lr * DK + (c * L::LPR + li) * 4) = s[c];
+        }
     }
-
     for (int t = 0; t < nrows; ++t) {
         const float alpha = expf(gsm[t]);
         const float b = bsm[t];
@@ -221,41 +308,34 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_recurrent_kernel(const RecArg
             kf[c] = bf16x4_to_f32(*reinterpret_cast<const uint2 *>(kq + (t * 2 + 0) * DK + (c * L::LPR + li) * 4));
             qf[c] = bf16x4_to_f32(*reinterpret_cast<const uint2 *>(kq + (t * 2 + 1) * DK + (c * L::LPR + li) * 4));
         }
-        const size_t orow = size_t(t0 + t) * a.h_v * a.dv + size_t(h) * a.dv + row0;
-        float *ck = VERIFY ? a.ckpt + size_t(t0 + t) * state_elems + tile_off : nullptr;
+        const float vv = act ? vsm[t * L::RB + lr] : 0.f;
+        const float e = row_update<L::NV, L::LPR>(s, kf, qf, alpha, b, vv);
+        if (act) {
+            const size_t orow = size_t(t0 + t) * a.h_v * a.dv + size_t(h) * a.dv + row0;
+            if (li == 0) a.o[orow + lr] = gdn::f32_to_bf16(__fmul_rn(a.q_scale, e));
+            if (VERIFY) {
+                float *ck = a.ckpt + size_t(t0 + t) * state_elems + tile_off;
 #pragma unroll
-        for (int p = 0; p < L::PASSES; ++p) {
-            const float vv = act[p] ? vsm[t * L::RB + lr[p]] : 0.f;
-            const float e = row_update<L::NV, L::LPR>(s[p], kf, qf, alpha, b, vv);
-            if (act[p]) {
-                if (li == 0) a.o[orow + lr[p]] = gdn::f32_to_bf16(__fmul_rn(a.q_scale, e));
-                if (VERIFY) {
-#pragma unroll
-                    for (int c = 0; c < L::NV; ++c)
-                        __stcs(reinterpret_cast<float4 *>(ck + lr[p] * DK + (c * L::LPR + li) * 4), s[p][c]);
-                }
+                for (int c = 0; c < L::NV; ++c)
+                    __stcs(reinterpret_cast<float4 *>(ck + lr * DK + (c * L::LPR + li) * 4), s[c]);
             }
         }
     }
-    if (!VERIFY) {
+    if (MODE == kDecode && act) {
         float *dp = a.pool_dst + size_t(dst) * a.slot_stride + tile_off;
 #pragma unroll
-        for (int p = 0; p < L::PASSES; ++p)
-            if (act[p]) {
-#pragma unroll
-                for (int c = 0; c < L::NV; ++c)
-                    *reinterpret_cast<float4 *>(dp + lr[p] * DK + (c * L::LPR + li) * 4) = s[p][c];
-            }
+        for (int c = 0; c < L::NV; ++c) *reinterpret_cast<float4 *>(dp + lr * DK + (c * L::LPR + li) * 4) = s[c];
     }
     if (VERIFY && lead) a.ckpt_tag[r] = (uint64_t(a.txn) << 32) | uint32_t(nrows);
 }
 
-template <int DK, bool VERIFY>
+template <int DK, int MODE>
 int launch(const RecArgs &a, cudaStream_t st) {
     using L = Lay<DK>;
-    auto kern = gdn_recurrent_kernel<DK, VERIFY>;
-    if (L::kSmem > 48 * 1024) {
-        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(L::kSmem)) != cudaSuccess)
+    auto kern = gdn_recurrent_kernel<DK, MODE>;
+    constexpr size_t smem = MODE == kReplay ? L::kSmemReplay : L::kSmem;
+    if (smem > 48 * 1024) {
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)) != cudaSuccess)
             return GDN_ERR_CUDA;
     }
     RecArgs b = a;
@@ -263,17 +343,17 @@ int launch(const RecArgs &a, cudaStream_t st) {
     const long long grid = (long long)a.B * a.h_v * b.bph;
     if (grid <= 0) return GDN_OK;
     if (grid > 0x7fffffffLL) return GDN_ERR_ARG;
-    kern<<<unsigned(grid), kThreads, L::kSmem, st>>>(b);
+    kern<<<unsigned(grid), kThreads, smem, st>>>(b);
     return gdn_host::launch_status(cudaGetLastError());
 }
 
-template <bool VERIFY>
+template <int MODE>
 int dispatch(int dk, const RecArgs &a, cudaStream_t st) {
     switch (dk) {
-        case 16: return launch<16, VERIFY>(a, st);
-        case 32: return launch<32, VERIFY>(a, st);
-        case 64: return launch<64, VERIFY>(a, st);
-        case 128: return launch<128, VERIFY>(a, st);
+        case 16: return launch<16, MODE>(a, st);
+        case 32: return launch<32, MODE>(a, st);
+        case 64: return launch<64, MODE>(a, st);
+        case 128: return launch<128, MODE>(a, st);
         default: return GDN_ERR_SHAPE;
     }
 }
@@ -323,7 +403,7 @@ extern "C" int gdn_decode_step(const gdn_dims *dims, int32_t B, const gdn_bf16 *
     a.row_capacity = B;
     a.grp = dims->h_v / dims->h_qk;
     a.q_scale = dims->q_scale;
-    return dispatch<false>(dims->d_k, a, static_cast<cudaStream_t>(stream));
+    return dispatch<kDecode>(dims->d_k, a, static_cast<cudaStream_t>(stream));
 }
 
 extern "C" int gdn_verify(const gdn_dims *dims, int32_t B, int32_t row_capacity, const int32_t *cu_rows,
@@ -361,5 +441,93 @@ extern "C" int gdn_verify(const gdn_dims *dims, int32_t B, int32_t row_capacity,
     a.row_capacity = row_capacity;
     a.grp = dims->h_v / dims->h_qk;
     a.q_scale = dims->q_scale;
-    return dispatch<true>(dims->d_k, a, static_cast<cudaStream_t>(stream));
+    return dispatch<kVerify>(dims->d_k, a, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" int gdn_verify_at(const gdn_dims *dims, int32_t B, int32_t row_capacity, const int32_t *cu_rows,
+                             const gdn_bf16 *q, const gdn_bf16 *k, const gdn_bf16 *v, const float *g,
+                             const float *beta, const float *state_base, int64_t state_elems_total,
+                             const int64_t *src_off, float *ckpt_layer, uint64_t *ckpt_tag, uint32_t txn, gdn_bf16 *o,
+                             uint32_t *dev_status, void *stream) {
+    if (!dims) return GDN_ERR_NULL;
+    if (!gdn_host::dims_ok(dims)) return GDN_ERR_SHAPE;
+    if (B < 0 || row_capacity < 0) return GDN_ERR_ARG;
+    if (!q || !k || !v || !g || !beta || !state_base || !src_off || !cu_rows || !ckpt_layer || !ckpt_tag || !o)
+        return GDN_ERR_NULL;
+    const int64_t se = int64_t(dims->h_v) * dims->d_v * dims->d_k;
+    if (state_elems_total < se) return GDN_ERR_ARG;
+    if (!gdn_host::aligned16(q) || !gdn_host::aligned16(k) || !gdn_host::aligned16(state_base) ||
+        !gdn_host::aligned16(ckpt_layer))
+        return GDN_ERR_ARG;
+    if (B == 0) return GDN_OK;
+    RecArgs a{};
+    a.cu_rows = cu_rows;
+    a.q = q;
+    a.k = k;
+    a.v = v;
+    a.g = g;
+    a.beta = beta;
+    a.pool_src = state_base;
+    a.src_off = src_off;
+    a.max_off = state_elems_total - se;
+    a.num_slots = 1;
+    a.ckpt = ckpt_layer;
+    a.ckpt_tag = ckpt_tag;
+    a.txn = txn;
+    a.o = o;
+    a.status = dev_status;
+    a.B = B;
+    a.h_qk = dims->h_qk;
+    a.h_v = dims->h_v;
+    a.dv = dims->d_v;
+    a.row_capacity = row_capacity;
+    a.grp = dims->h_v / dims->h_qk;
+    a.q_scale = dims->q_scale;
+    return dispatch<kVerifyAt>(dims->d_k, a, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" int gdn_verify_replay(const gdn_dims *dims, int32_t B, int32_t row_capacity, const int32_t *cu_rows,
+                                 const gdn_bf16 *q, const gdn_bf16 *k, const gdn_bf16 *v, const float *g,
+                                 const float *beta, int32_t prev_capacity, const int32_t *prev_cu_rows,
+                                 const int32_t *prev_accept_len, const gdn_bf16 *prev_k, const gdn_bf16 *prev_v,
+                                 const float *prev_g, const float *prev_beta, float *pool_layer, int64_t slot_stride,
+                                 int32_t num_slots, const int32_t *src_slot, const int32_t *dst_slot, gdn_bf16 *o,
+                                 uint32_t *dev_status, void *stream) {
+    int st = common_checks(dims, B, q, k, v, g, beta, pool_layer, slot_stride, num_slots, src_slot, o);
+    if (st != GDN_OK) return st;
+    if (!cu_rows || !dst_slot || !prev_cu_rows || !prev_accept_len || !prev_k || !prev_v || !prev_g || !prev_beta)
+        return GDN_ERR_NULL;
+    if (row_capacity < 0 || prev_capacity < 0) return GDN_ERR_ARG;
+    if (!gdn_host::aligned16(prev_k)) return GDN_ERR_ARG;
+    if (B == 0) return GDN_OK;
+    RecArgs a{};
+    a.cu_rows = cu_rows;
+    a.q = q;
+    a.k = k;
+    a.v = v;
+    a.g = g;
+    a.beta = beta;
+    a.pool_src = pool_layer;
+    a.pool_dst = pool_layer;
+    a.slot_stride = slot_stride;
+    a.num_slots = num_slots;
+    a.src_slot = src_slot;
+    a.dst_slot = dst_slot;
+    a.prev_cu = prev_cu_rows;
+    a.prev_acc = prev_accept_len;
+    a.pk = prev_k;
+    a.pv = prev_v;
+    a.pg = prev_g;
+    a.pbeta = prev_beta;
+    a.prev_capacity = prev_capacity;
+    a.o = o;
+    a.status = dev_status;
+    a.B = B;
+    a.h_qk = dims->h_qk;
+    a.h_v = dims->h_v;
+    a.dv = dims->d_v;
+    a.row_capacity = row_capacity;
+    a.grp = dims->h_v / dims->h_qk;
+    a.q_scale = dims->q_scale;
+    return dispatch<kReplay>(dims->d_k, a, static_cast<cudaStream_t>(stream));
 }

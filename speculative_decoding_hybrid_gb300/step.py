@@ -32,7 +32,7 @@ class LayerRows:
 
 class VerifyStep:
     def __init__(self, dims: gs.gdn_dims, num_layers: int, num_slots: int, row_capacity: int, max_batch: int,
-                 vocab: int, device="cuda", pool: Optional[torch.Tensor] = None):
+                 vocab: int, device="cuda", pool: Optional[torch.Tensor] = None, checkpoints: bool = True):
         self.d = dims
         self.L = num_layers
         self.num_slots = num_slots
@@ -46,8 +46,9 @@ class VerifyStep:
             pool = torch.zeros((num_slots, num_layers, h_v, dv, dk), dtype=torch.float32, device=dev)
         assert pool.shape == (num_slots, num_layers, h_v, dv, dk) and pool.is_contiguous()
         self.pool = pool
-        self.ckpt = torch.empty((num_layers, row_capacity, h_v, dv, dk), dtype=torch.float32, device=dev)
-        self.tags = torch.zeros((num_layers, max_batch), dtype=torch.int64, device=dev)
+        self.ckpt = (torch.empty((num_layers, row_capacity, h_v, dv, dk), dtype=torch.float32, device=dev)
+                     if checkpoints else None)
+        self._tags = torch.zeros((num_layers * max_batch,), dtype=torch.int64, device=dev)
         self.o = torch.empty((num_layers, row_capacity, h_v, dv), dtype=torch.bfloat16, device=dev)
         self.argmax = torch.full((row_capacity,), -1, dtype=torch.int32, device=dev)
         self.accept_len = torch.full((max_batch,), -1, dtype=torch.int32, device=dev)
@@ -59,8 +60,12 @@ class VerifyStep:
         self.status = torch.zeros((1,), dtype=torch.int32, device=dev)
         self.slot_stride = pool.stride(0)
         self.layer_stride = pool.stride(1)
-        self.ckpt_layer_stride = self.ckpt.stride(0)
+        self.ckpt_layer_stride = self.ckpt.stride(0) if checkpoints else 0
         self.txn = 0
+
+    def tags(self, B: int) -> torch.Tensor:
+        """Checkpoint tags laid out [layer][request] for a batch of B requests."""
+        return self._tags[:self.L * B].view(self.L, B)
 
     def pool_layer(self, l: int) -> int:
         return self.pool.data_ptr() + 4 * l * self.layer_stride
@@ -68,7 +73,7 @@ class VerifyStep:
     def verify_layer(self, l: int, B: int, cu_rows: torch.Tensor, src_slot: torch.Tensor, rows: LayerRows,
                      stream=None):
         gs.gdn_verify(self.d, B, self.cap, cu_rows, rows.q, rows.k, rows.v, rows.g, rows.beta, self.pool_layer(l),
-                      self.slot_stride, self.num_slots, src_slot, self.ckpt[l], self.tags[l], self.txn, self.o[l],
+                      self.slot_stride, self.num_slots, src_slot, self.ckpt[l], self.tags(B)[l], self.txn, self.o[l],
                       self.status, stream)
 
     def accept(self, B: int, cu_rows: torch.Tensor, logits: torch.Tensor, tokens: torch.Tensor, stream=None):
@@ -78,8 +83,8 @@ class VerifyStep:
 
     def commit(self, B: int, cu_rows: torch.Tensor, dst_slot: torch.Tensor, stream=None):
         gs.gdn_commit(self.d, B, self.L, self.cap, cu_rows, self.accept_len, self.ckpt, self.ckpt_layer_stride,
-                      self.tags, self.txn, self.pool, self.slot_stride, self.layer_stride, self.num_slots, dst_slot,
-                      self.status, stream)
+                      self.tags(B), self.txn, self.pool, self.slot_stride, self.layer_stride, self.num_slots,
+                      dst_slot, self.status, stream)
 
     def run(self, B: int, cu_rows: torch.Tensor, src_slot: torch.Tensor, dst_slot: torch.Tensor,
             layer_rows: Sequence[LayerRows], logits: torch.Tensor, tokens: torch.Tensor, stream=None):
@@ -165,3 +170,110 @@ class DecodeLoop:
         for i in range(self.B):
             self.slot[i] = dst[i]
             self.cur_len[i] += int(accept_len[i]) + 1
+
+
+class ArenaStep(VerifyStep):
+    """Zero-copy commit over a state arena.
+
+    One fp32 buffer holds the pool slots followed by two checkpoint areas;
+    transaction n writes its checkpoints into area n % 2 and the commit only
+    points each (request, layer) location at its accepted checkpoint, so the
+    next transaction verifies from there.  ``materialize`` copies states
+    back into slots when a request leaves.  The batch size is fixed (the
+    location table is laid out [layer][request])."""
+
+    def __init__(self, dims: gs.gdn_dims, num_layers: int, num_slots: int, row_capacity: int, batch: int,
+                 vocab: int, device="cuda"):
+        h_v, dv, dk = dims.h_v, dims.d_v, dims.d_k
+        S = h_v * dv * dk
+        self.S = S
+        pool_elems = num_slots * num_layers * S
+        ck_elems = num_layers * row_capacity * S
+        self.arena = torch.empty((pool_elems + 2 * ck_elems,), dtype=torch.float32, device=device)
+        pool = self.arena[:pool_elems].view(num_slots, num_layers, h_v, dv, dk)
+        super().__init__(dims, num_layers, num_slots, row_capacity, batch, vocab, device, pool=pool,
+                         checkpoints=False)  # the checkpoint areas live in the arena
+        self.areas = [self.arena[pool_elems + i * ck_elems:pool_elems + (i + 1) * ck_elems]
+                      .view(num_layers, row_capacity, h_v, dv, dk) for i in range(2)]
+        self.area_off = [pool_elems, pool_elems + ck_elems]
+        self.ckpt_layer_stride = row_capacity * S
+        self.total = self.arena.numel()
+        self.B = batch
+        self.loc = torch.zeros((num_layers, batch), dtype=torch.int64, device=self.dev)
+
+    def point_at_slots(self, slots: Sequence[int]):
+        """Every request's state starts in its pool slot."""
+        L = self.L
+        off = [[s * self.slot_stride + l * self.layer_stride for s in slots] for l in range(L)]
+        self.loc.copy_(torch.tensor(off, dtype=torch.int64))
+
+    def run(self, B: int, cu_rows: torch.Tensor, layer_rows: Sequence[LayerRows], logits: torch.Tensor,
+            tokens: torch.Tensor, stream=None):
+        assert B == self.B
+        self.txn = (self.txn + 1) & 0xFFFFFFFF
+        area = self.txn & 1
+        base = self.areas[area]
+        for l in range(self.L):
+            x = layer_rows[l]
+            gs.gdn_verify_at(self.d, B, self.cap, cu_rows, x.q, x.k, x.v, x.g, x.beta, self.arena, self.total,
+                             self.loc[l], base[l], self.tags(B)[l], self.txn, self.o[l], self.status, stream)
+        self.accept(B, cu_rows, logits, tokens, stream)
+        gs.gdn_commit_at(self.d, B, self.L, self.cap, cu_rows, self.accept_len, self.area_off[area],
+                         self.ckpt_layer_stride, self.tags(B), self.txn, self.loc, self.status, stream)
+
+    def materialize(self, dst_slot: torch.Tensor, stream=None):
+        gs.gdn_materialize(self.d, self.B, self.L, self.arena, self.total, self.loc, self.pool, self.slot_stride,
+                           self.layer_stride, self.num_slots, dst_slot, self.status, stream)
+
+
+class ReplayStep(VerifyStep):
+    """Compact fixed-state replay: no checkpoints.  Each transaction's
+    ``gdn_verify_replay`` first runs the previous transaction's accepted rows
+    from the slot and writes the slot (the previous commit), then runs the new
+    rows for outputs only.  The caller keeps the previous transaction's layer
+    rows alive until the next run (or ``flush``)."""
+
+    def __init__(self, dims: gs.gdn_dims, num_layers: int, num_slots: int, row_capacity: int, batch: int,
+                 vocab: int, device="cuda", pool: Optional[torch.Tensor] = None):
+        super().__init__(dims, num_layers, num_slots, row_capacity, batch, vocab, device, pool=pool,
+                         checkpoints=False)
+        self.B = batch
+        self.acc_bufs = [torch.full((batch,), -1, dtype=torch.int32, device=self.dev) for _ in range(2)]
+        self.prev_cu = torch.zeros((batch + 1,), dtype=torch.int32, device=self.dev)
+        self.no_rows = torch.zeros((batch + 1,), dtype=torch.int32, device=self.dev)
+        self.prev_rows: Optional[Sequence[LayerRows]] = None
+        self.prev_acc = self.acc_bufs[1]      # read by the replay: the previous accept lengths
+        self.accept_len = self.acc_bufs[0]    # written by this transaction's accept
+        self.pending = False
+
+    def _advance(self):
+        if self.pending:  # the accept lengths just read back become the ones to replay
+            self.prev_acc, self.accept_len = self.accept_len, self.prev_acc
+
+    def _verify_all(self, B, cu_rows, src_slot, dst_slot, layer_rows, stream=None):
+        prev = self.prev_rows if self.prev_rows is not None else layer_rows
+        for l in range(self.L):
+            x, p = layer_rows[l], prev[l]
+            gs.gdn_verify_replay(self.d, B, self.cap, cu_rows, x.q, x.k, x.v, x.g, x.beta, self.cap, self.prev_cu,
+                                 self.prev_acc, p.k, p.v, p.g, p.beta, self.pool_layer(l), self.slot_stride,
+                                 self.num_slots, src_slot, dst_slot, self.o[l], self.status, stream)
+
+    def run(self, B: int, cu_rows: torch.Tensor, src_slot: torch.Tensor, dst_slot: torch.Tensor,
+            layer_rows: Sequence[LayerRows], logits: torch.Tensor, tokens: torch.Tensor, stream=None):
+        assert B == self.B
+        self._advance()
+        self._verify_all(B, cu_rows, src_slot, dst_slot, layer_rows, stream)
+        self.accept(B, cu_rows, logits, tokens, stream)
+        # this transaction's accepted rows are replayed by the next one
+        self.prev_cu.copy_(cu_rows[:B + 1], non_blocking=True)
+        self.prev_rows = layer_rows
+        self.pending = True
+
+    def flush(self, src_slot: torch.Tensor, dst_slot: torch.Tensor, stream=None):
+        """Commit the pending accepted rows without verifying new ones."""
+        if not self.pending:
+            return
+        self._advance()
+        self._verify_all(self.B, self.no_rows, src_slot, dst_slot, self.prev_rows, stream)
+        self.prev_acc.fill_(-1)
+        self.pending = False

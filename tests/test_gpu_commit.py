@@ -59,7 +59,7 @@ def test_commit_copies_accepted_checkpoint_and_refuses_the_rest(gs, cuda_dev):
             assert torch.equal(vs.pool[s], before[s])
 
     # the oracle's commit rule gives the same moves
-    tags = vs.tags[:, :B].cpu().numpy().astype(np.uint64)
+    tags = vs.tags(B).cpu().numpy().astype(np.uint64)
     moves, st = oracle.commit_plan(acc, cu, tags & 0xffffffff, tags >> 32, 41, dst.tolist(), 9)
     assert st == 0 and moves == [[cu[r] + acc[r] for r in range(B)] for _ in range(3)]
 

@@ -1,0 +1,95 @@
+"""Compact fixed-state replay (gdn_verify_replay) against the checkpoint path:
+same planner decisions, same accepted lengths, emitted tokens and outputs,
+and bit-for-bit the same committed states, including a copy-on-write slot."""
+import pytest
+import torch
+
+import gdnsynth as sy
+from gpu_util import build_lib
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def gs(cuda_dev):
+    build_lib()
+    from speculative_decoding_hybrid_gb300 import binding
+    return binding
+
+
+def _pool(gs, num_slots):
+    p = gs.Pool(num_slots, [5, 0, 3, 7, 1, 2, 4, 6, 8, 9, 10, 11])
+    for _ in range(5):
+        p.alloc()
+    p.share(5)
+    return p
+
+
+def test_replay_loop_matches_checkpoint_loop(gs, cuda_dev):
+    from speculative_decoding_hybrid_gb300.step import DecodeLoop, LayerRows, ReplayStep, VerifyStep
+    dims = sy.Dims(4, 8, 128, 128)
+    d = gs.dims(dims.h_qk, dims.h_v, dims.d_k, dims.d_v)
+    L, B, num_slots, vocab, steps = 3, 6, 12, 4096, 7
+    cap = B * 4
+    init = sy.state(sy.generator(3), (num_slots, L, dims.h_v, dims.d_v, dims.d_k)).to(cuda_dev)
+    slots = [5, 5, 0, 3, 7, 1]              # requests 0 and 1 share slot 5
+    vs = VerifyStep(d, L, num_slots, cap, B, vocab, cuda_dev, pool=init.clone())
+    rs = ReplayStep(d, L, num_slots, cap, B, vocab, cuda_dev, pool=init.clone())
+    lc = DecodeLoop(vs, slots, _pool(gs, num_slots))
+    lr = DecodeLoop(rs, slots, _pool(gs, num_slots))
+    kg = sy.generator(4)
+    keep = []
+    for s in range(steps):
+        ks = torch.randint(0, 4, (B,), generator=kg).tolist()
+        pc = lc.plan_step(ks)
+        pr = lr.plan_step(ks)
+        assert pc.dec_cu == pr.dec_cu and pc.dec_src == pr.dec_src and pc.dec_dst == pr.dec_dst
+        cu = pc.dec_cu
+        R = cu[-1]
+        rows = [sy.rows(sy.generator(50 * s + l), R, dims, cuda_dev) for l in range(L)]
+        lrows = [LayerRows(r.q, r.k, r.v, r.g, r.beta) for r in rows]
+        keep.append(lrows)
+        lg, tgt = sy.logits(sy.generator(70 + s), R, vocab, 2.0, cuda_dev)
+        toks = torch.tensor(sum(sy.drafts(sy.generator(90 + s), tgt.tolist(), pc.k, vocab, 0.85), []),
+                            dtype=torch.int32, device=cuda_dev)
+        lc.upload_tables()
+        lc.run(lrows, lg, toks)
+        ac, bc, oc = (x.clone() for x in lc.readback())
+        lr.upload_tables()
+        lr.run(lrows, lg, toks)
+        ar, br, orr = (x.clone() for x in lr.readback())
+        assert int(vs.status.item()) == 0 and int(rs.status.item()) == 0
+        assert torch.equal(ac, ar) and torch.equal(bc, br) and torch.equal(oc[:R], orr[:R])
+        assert torch.equal(vs.o[:, :R], rs.o[:, :R]), "outputs are computed from bit-identical states"
+        lc.finish(ac)
+        lr.finish(ar)
+    assert lc.slot == lr.slot
+    cur = torch.tensor(lr.slot, dtype=torch.int32, device=cuda_dev)
+    rs.flush(cur, cur)
+    torch.cuda.synchronize()
+    assert int(rs.status.item()) == 0
+    for r in range(B):
+        assert torch.equal(rs.pool[lr.slot[r]], vs.pool[lc.slot[r]]), r
+    # the shared slot was never written by either path
+    assert torch.equal(rs.pool[5], init[5]) and torch.equal(vs.pool[5], init[5])
+
+
+def test_replay_refuses_more_accepted_rows_than_existed(gs, cuda_dev):
+    from speculative_decoding_hybrid_gb300.step import LayerRows
+    dims = sy.Dims(2, 4, 64, 64)
+    d = gs.dims(2, 4, 64, 64)
+    pool = sy.state(sy.generator(1), (3, 4, 64, 64)).to(cuda_dev)
+    before = pool.clone()
+    r = sy.rows(sy.generator(2), 4, dims, cuda_dev)
+    cu = torch.tensor([0, 2, 4], dtype=torch.int32, device=cuda_dev)
+    prev_cu = torch.tensor([0, 2, 4], dtype=torch.int32, device=cuda_dev)
+    prev_acc = torch.tensor([5, 1], dtype=torch.int32, device=cuda_dev)   # request 0 claims 6 of its 2 rows
+    slots = torch.tensor([0, 1], dtype=torch.int32, device=cuda_dev)
+    o = torch.zeros((4, 4, 64), dtype=torch.bfloat16, device=cuda_dev)
+    st = torch.zeros(1, dtype=torch.int32, device=cuda_dev)
+    gs.gdn_verify_replay(d, 2, 4, cu, r.q, r.k, r.v, r.g, r.beta, 4, prev_cu, prev_acc, r.k, r.v, r.g, r.beta,
+                         pool, pool.stride(0), 3, slots, slots, o, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) & gs.DEV_ROWS_BAD
+    assert torch.equal(pool[0], before[0])            # refused: slot untouched
+    assert not torch.equal(pool[1], before[1])        # request 1 replayed its 2 rows
