@@ -390,6 +390,12 @@ int gdn_pool_abort(gdn_pool *pool, const gdn_plan *plan, int32_t n);
 
 const char *gdn_status_string(int status);
 
+/* Failure-detection self-test: a kernel waits on an mbarrier that is never
+ * completed, gives up after limit_ns (1 .. 1e9) of device time and sets
+ * GDN_DEV_TIMEOUT in *dev_status -- the same bounded wait every kernel here
+ * uses for its asynchronous copies and tensor-core operations. */
+int gdn_selftest_wait_timeout(uint32_t *dev_status, uint64_t limit_ns, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

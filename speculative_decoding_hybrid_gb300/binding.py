@@ -30,7 +30,7 @@ PLAN_RECURRENT, PLAN_CHUNKED = 0, 1
 
 EXPORTS = ["gdn_decode_step", "gdn_verify", "mtp_accept_workspace_bytes", "mtp_greedy_accept",
            "mtp_greedy_accept_noalloc", "gdn_commit", "gdn_verify_at", "gdn_commit_at", "gdn_materialize",
-           "gdn_verify_replay",
+           "gdn_verify_replay", "gdn_selftest_wait_timeout",
            "gdn_prefill_workspace_bytes", "gdn_chunked_prefill", "gdn_pool_init", "gdn_pool_alloc",
            "gdn_pool_share", "gdn_pool_release", "plan_transaction", "gdn_pool_apply", "gdn_pool_abort",
            "gdn_status_string"]
@@ -103,6 +103,7 @@ def _load():
         "gdn_pool_apply": [ctypes.POINTER(gdn_pool), ctypes.POINTER(gdn_plan), I32],
         "gdn_pool_abort": [ctypes.POINTER(gdn_pool), ctypes.POINTER(gdn_plan), I32],
         "gdn_status_string": [ctypes.c_int],
+        "gdn_selftest_wait_timeout": [P, ctypes.c_uint64, P],
     }
     for name, args in sig.items():
         f = getattr(L, name)
@@ -243,6 +244,11 @@ def gdn_chunked_prefill(d: gdn_dims, nseq, row_capacity, cu_seqlens, max_seqlen,
         ctypes.byref(d), nseq, row_capacity, _ptr(cu_seqlens), max_seqlen, _ptr(q), _ptr(k), _ptr(v), _ptr(g),
         _ptr(beta), _ptr(pool_layer), slot_stride, num_slots, _ptr(src_slot), _ptr(dst_slot), _ptr(o), chunk,
         _ptr(workspace), workspace_bytes, _ptr(dev_status), _stream(stream)))
+
+
+def gdn_selftest_wait_timeout(dev_status, limit_ns: int, stream=None):
+    return _check("gdn_selftest_wait_timeout",
+                  lib.gdn_selftest_wait_timeout(_ptr(dev_status), int(limit_ns), _stream(stream)))
 
 
 # ---------------------------------------------------------------------------

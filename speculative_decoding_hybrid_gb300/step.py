@@ -13,9 +13,11 @@ caller's device tensors.  All arithmetic happens in the library's kernels.
 """
 from __future__ import annotations
 
+import ctypes
 from dataclasses import dataclass
 from typing import List, Optional, Sequence
 
+import numpy as np
 import torch
 
 from . import binding as gs
@@ -104,35 +106,52 @@ class DecodeLoop:
     tables go to the device; ``VerifyStep.run`` verifies, accepts and commits;
     one device-to-host read brings back accept lengths, bonus and emitted
     tokens; the pool then releases the slots that requests moved away from.
+    Host bookkeeping works on numpy views of the planner's buffers.
     """
 
     def __init__(self, vs: VerifyStep, slots: Sequence[int], pool: "gs.Pool", k_max: int = 3,
                  max_len: int = 1 << 30, cur_len: int = 1):
         self.vs = vs
         self.B = len(slots)
-        self.slot = list(slots)
-        self.cur_len = [cur_len] * self.B
-        self.max_len = max_len
+        B = self.B
         self.pool = pool
-        self.plan = gs.Plan(self.B)
-        self.lim = gs.gdn_plan_limits(vs.cap, self.B, k_max)
+        self.plan = gs.Plan(B)
+        self.lim = gs.gdn_plan_limits(vs.cap, B, k_max)
+        self.reqs = (gs.gdn_req * max(B, 1))()
+        self.req_np = np.ctypeslib.as_array(ctypes.cast(self.reqs, ctypes.POINTER(ctypes.c_int32)),
+                                            shape=(max(B, 1), 6))
+        self.req_np[:B, 0] = gs.REQ_DECODE
+        self.req_np[:B, 2] = 0
+        self.req_np[:B, 3] = cur_len
+        self.req_np[:B, 4] = max_len
+        self.req_np[:B, 5] = np.asarray(slots, dtype=np.int32)
         dev = vs.dev
-        self.h_tab = torch.zeros((3, self.B + 1), dtype=torch.int32).pin_memory()
-        self.d_tab = torch.zeros((3, self.B + 1), dtype=torch.int32, device=dev)
-        self.h_out = torch.zeros((2 * self.B + vs.cap,), dtype=torch.int32).pin_memory()
+        self.h_tab = torch.zeros((3, B + 1), dtype=torch.int32).pin_memory()
+        self.h_tab_np = self.h_tab.numpy()
+        self.d_tab = torch.zeros((3, B + 1), dtype=torch.int32, device=dev)
+        self.h_out = torch.zeros((2 * B + vs.cap,), dtype=torch.int32).pin_memory()
+
+    @property
+    def slot(self):
+        return self.req_np[:self.B, 5].tolist()
+
+    @property
+    def cur_len(self):
+        return self.req_np[:self.B, 3].tolist()
 
     def plan_step(self, k_draft: Sequence[int]):
-        reqs = gs.make_reqs([(gs.REQ_DECODE, int(k_draft[i]), 0, self.cur_len[i], self.max_len, self.slot[i])
-                             for i in range(self.B)])
-        st = gs.plan_transaction(reqs, self.B, self.lim, self.pool, self.plan)
+        B = self.B
+        self.req_np[:B, 1] = np.asarray(k_draft, dtype=np.int32)
+        st = gs.plan_transaction(self.reqs, B, self.lim, self.pool, self.plan)
         if st != gs.GDN_OK:
             raise gs.GdnError("plan_transaction", st)
         p = self.plan
-        if p.n_decode != self.B:
-            raise RuntimeError("row budget too small for the batch: %d of %d requests selected" % (p.n_decode, self.B))
-        self.h_tab[0, :self.B + 1] = torch.tensor(p.dec_cu, dtype=torch.int32)
-        self.h_tab[1, :self.B] = torch.tensor(p.dec_src, dtype=torch.int32)
-        self.h_tab[2, :self.B] = torch.tensor(p.dec_dst, dtype=torch.int32)
+        if p.c.n_decode != B:
+            raise RuntimeError("row budget too small for the batch: %d of %d requests selected" % (p.c.n_decode, B))
+        arr = p.arrays
+        self.h_tab_np[0, :B + 1] = arr["dec_cu"][:B + 1]
+        self.h_tab_np[1, :B] = arr["dec_src"][:B]
+        self.h_tab_np[2, :B] = arr["dec_dst"][:B]
         return p
 
     def upload_tables(self, stream=None):
@@ -166,10 +185,10 @@ class DecodeLoop:
         st = gs.gdn_pool_apply(self.pool, self.plan, self.B)
         if st != gs.GDN_OK:
             raise gs.GdnError("gdn_pool_apply", st)
-        dst = self.plan.dst
-        for i in range(self.B):
-            self.slot[i] = dst[i]
-            self.cur_len[i] += int(accept_len[i]) + 1
+        B = self.B
+        self.req_np[:B, 5] = self.plan.arrays["dst"][:B]
+        acc = accept_len.numpy() if hasattr(accept_len, "numpy") else np.asarray(accept_len)
+        self.req_np[:B, 3] += acc[:B].astype(np.int32) + 1
 
 
 class ArenaStep(VerifyStep):

@@ -117,3 +117,20 @@ def test_commit_j_equals_j_plus_1_decode_steps(gs, cuda_dev):
             torch.cuda.synchronize()
             assert torch.equal(vs.pool[r, l], lay[r]), (r, l)
     assert int(vs.status.item()) == 0 and int(st.item()) == 0
+
+
+def test_bounded_wait_gives_up_and_reports(gs, cuda_dev):
+    """The bounded wait behind every asynchronous copy: a barrier that is never
+    completed makes the kernel give up after the limit and report
+    GDN_DEV_TIMEOUT; the context stays usable and a later commit refuses."""
+    import time
+    st = torch.zeros(1, dtype=torch.int32, device=cuda_dev)
+    t0 = time.perf_counter()
+    gs.gdn_selftest_wait_timeout(st, 20_000_000)     # 20 ms
+    torch.cuda.synchronize()
+    assert time.perf_counter() - t0 < 5.0
+    assert int(st.item()) == gs.DEV_TIMEOUT
+    x = torch.arange(4, device=cuda_dev).sum()       # the context still works
+    assert int(x.item()) == 6
+    with pytest.raises(gs.GdnError):
+        gs.gdn_selftest_wait_timeout(st, 0)
