@@ -463,61 +463,81 @@ def run_zero_copy(spec, dev, args, replay=False):
 
 
 def stage_e2e(b: Bench):
-    """Pinned host copies of the ring inputs and one device staging set."""
+    """Pinned host copies of the ring inputs and two device staging sets."""
     from speculative_decoding_hybrid_gb300.step import LayerRows
-    host, nbytes = [], 0
+    host = []
     for i in range(b.spec.ring):
-        hl = []
-        for r in b.rows[i]:
-            t = [x.detach().to("cpu").pin_memory() for x in (r.q, r.k, r.v, r.g, r.beta)]
-            hl.append(t)
+        hl = [[x.detach().to("cpu").pin_memory() for x in (r.q, r.k, r.v, r.g, r.beta)] for r in b.rows[i]]
         host.append((hl, b.logits[i].detach().to("cpu").pin_memory()))
-    stage_rows = [LayerRows(*(torch.empty_like(x) for x in (r.q, r.k, r.v, r.g, r.beta))) for r in b.rows[0]]
-    stage_logits = torch.empty_like(b.logits[0])
-    return host, stage_rows, stage_logits
+    stages = []
+    for _ in range(2):
+        rows = [LayerRows(*(torch.empty_like(x) for x in (r.q, r.k, r.v, r.g, r.beta))) for r in b.rows[0]]
+        stages.append((rows, torch.empty_like(b.logits[0])))
+    return host, stages
 
 
-def run_e2e(b: Bench, host, stage_rows, stage_logits, steps, warmup):
+def run_e2e(b: Bench, host, stages, steps, warmup):
     """Same step through the public API, with every step's inputs copied from
-    pinned host memory and the results read back inside the timed region."""
+    pinned host memory and the results read back inside the timed region.
+    Copies for step s+1 run on a copy stream while step s computes (two
+    device staging sets); a step waits for its own inputs' copy event."""
     spec = b.spec
     saved_rows, saved_logits = b.rows, b.logits
-    b.rows = [stage_rows] * spec.ring
-    b.logits = [stage_logits] * spec.ring
-    h2d = 0
+    copy_stream = torch.cuda.Stream()
+    compute = torch.cuda.current_stream()
+    done = [torch.cuda.Event(), torch.cuda.Event()]
+    free = [torch.cuda.Event(), torch.cuda.Event()]
+    moved_bytes = [0]
 
-    def one():
-        nonlocal h2d
-        ring = b.step_no % spec.ring
-        hl, hlog = host[ring]
-        moved = 0
-        for l in range(spec.layers):
-            dst = stage_rows[l]
-            for x, dt in zip(hl[l], (dst.q, dst.k, dst.v, dst.g, dst.beta)):
-                dt.copy_(x, non_blocking=True)
-                moved += x.numel() * x.element_size()
-        stage_logits.copy_(hlog, non_blocking=True)
-        moved += hlog.numel() * hlog.element_size()
-        n, p = b.step()
-        moved += (p.n_decode + 1) * 3 * 4 + b.cap * 4       # tables + tokens
-        return n, moved
+    def issue_copy(step_no, slot):
+        hl, hlog = host[step_no % spec.ring]
+        rows, logits = stages[slot]
+        with torch.cuda.stream(copy_stream):
+            copy_stream.wait_event(free[slot])  # the staging set's previous reader is done
+            moved = 0
+            for l in range(spec.layers):
+                dst = rows[l]
+                for x, dt in zip(hl[l], (dst.q, dst.k, dst.v, dst.g, dst.beta)):
+                    dt.copy_(x, non_blocking=True)
+                    moved += x.numel() * x.element_size()
+            logits.copy_(hlog, non_blocking=True)
+            moved += hlog.numel() * hlog.element_size()
+            done[slot].record(copy_stream)
+        moved_bytes[0] += moved
+
+    def one(slot):
+        compute.wait_event(done[slot])
+        rows, logits = stages[slot]
+        b.rows = [rows] * spec.ring
+        b.logits = [logits] * spec.ring
+        issue_copy(b.step_no + 1, slot ^ 1)       # next step's inputs, overlapped
+        n, p = b.step()                           # ends with the step's one readback
+        free[slot].record(compute)
+        return n, p
 
     try:
+        for e in free:
+            e.record(compute)
+        slot = 0
+        issue_copy(b.step_no, slot)
         for _ in range(warmup):
-            one()
+            one(slot)
+            slot ^= 1
         torch.cuda.synchronize()
+        moved_bytes[0] = 0
         t0 = time.perf_counter()
         tok = 0
         for _ in range(steps):
-            n, moved = one()
+            n, p = one(slot)
+            slot ^= 1
             tok += n
-            h2d += moved
         torch.cuda.synchronize()
         dt = time.perf_counter() - t0
     finally:
         b.rows, b.logits = saved_rows, saved_logits
+    h2d = moved_bytes[0] / steps + (b.loop.B + 1) * 3 * 4 + b.cap * 4   # inputs + tables + tokens
     d2h = (2 * spec.batch + b.cap) * 4
-    return tok / dt, h2d / steps, d2h
+    return tok / dt, h2d, d2h
 
 
 # ---------------------------------------------------------------------------
@@ -702,9 +722,9 @@ def main():
         b.vs.pool.numel() * 4 / 2 ** 30, b.vs.ckpt.numel() * 4 / 2 ** 30, spec.ring)
     e2e = None
     if not args.no_e2e:
-        host, srows, slog = stage_e2e(b)
-        val, h2d, d2h = run_e2e(b, host, srows, slog, args.e2e_steps, 3)
-        del host, srows, slog
+        host, stages = stage_e2e(b)
+        val, h2d, d2h = run_e2e(b, host, stages, args.e2e_steps, 3)
+        del host, stages
         if world > 1:
             t = torch.tensor([val], device=dev, dtype=torch.float64)
             dist.all_reduce(t)

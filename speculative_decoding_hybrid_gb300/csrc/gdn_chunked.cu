@@ -351,10 +351,40 @@ constexpr uint32_t kQ = 98304;                  // Q             64 rows (t)   x
 constexpr uint32_t kP1 = 114688, kP2 = 122880;  // P parts       64 rows (t)   x  64 (i)
 constexpr uint32_t kK1 = 131072, kK2 = 147456;  // dec K parts  128 rows (d_k) x  64 (i)
 constexpr uint32_t kU1 = 163840, kU2 = 180224;  // U^T parts    128 rows (d_v) x  64 (i)
-constexpr uint32_t kMisc = 196608;              // G, e^G, dec, mbarrier, tensor-memory base, flag
-constexpr size_t kSmem = kMisc + 1024 + 1024;
+constexpr uint32_t kMisc = 196608;              // G, e^G, dec, mbarriers, tensor-memory base, flag
+constexpr uint32_t kRawQ = 197632;              // next chunk's raw q rows (bf16 64 x 128)
+constexpr uint32_t kRawK = 214016;              // next chunk's raw k rows (bf16 64 x 128)
+constexpr uint32_t kRawG = 230400;              // next chunk's g (fp32 x 64)
+constexpr size_t kSmem = kRawG + 256 + 1024;
 constexpr uint32_t kTmemCols = 512;  // Uacc 0..63, Oi 64..127, Oa 128..191, dS 256..383
+// The next chunk's raw W and P (fp32, from the workspace) land in the U and
+// P tile areas, which are free from the end of phase B until they are
+// consumed by the next chunk's staging.
+constexpr uint32_t kRawW = kU1, kRawP = kP1;
 }  // namespace sc
+
+// Prefetch of chunk c's raw inputs: W (32 KB) and P (16 KB) from the
+// workspace, q and k rows (256 B each) by bulk asynchronous copies on one
+// mbarrier, g by 4-byte cp.async.  Called by every thread.
+__device__ __forceinline__ void scan_prefetch(const PrefArgs &a, unsigned char *sm, uint64_t *bar, int s0, int len,
+                                              int seq, int h, int hq, int c) {
+    const int tid = threadIdx.x;
+    const int t0 = s0 + c * kC;
+    const int n = min(kC, len - c * kC);
+    const float *W = ws_w(a, chunk_slot(s0, c, seq), h);
+    if (tid < 32) {
+        if (tid == 0) gdn::mbar_arrive_expect_tx(bar, uint32_t(kC * kD * 4 + kC * kC * 4 + 2 * n * kD * 2));
+        __syncwarp();
+        if (tid == 0) gdn::bulk_g2s(sm + sc::kRawW, W, kC * kD * 4, bar);
+        if (tid == 1) gdn::bulk_g2s(sm + sc::kRawP, W + 2 * kC * kD, kC * kC * 4, bar);
+        for (int t = tid; t < n; t += 32) {
+            gdn::bulk_g2s(sm + sc::kRawQ + t * kD * 2, a.q + (size_t(t0 + t) * a.h_qk + hq) * kD, kD * 2, bar);
+            gdn::bulk_g2s(sm + sc::kRawK + t * kD * 2, a.k + (size_t(t0 + t) * a.h_qk + hq) * kD, kD * 2, bar);
+        }
+    }
+    if (tid < n) gdn::cp_async4(sm + sc::kRawG + tid * 4, a.g + size_t(t0 + tid) * a.h_v + h);
+    gdn::cp_async_commit();
+}
 
 // Two-term bf16 split of 8 consecutive values, packed as two 16-byte chunks.
 __device__ __forceinline__ void split8(const float (&x)[8], uint4 &hi, uint4 &lo) {
@@ -397,11 +427,15 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_chunk_scan_kernel(const PrefA
     float *eG = Gs + kC;
     float *dec = eG + kC;
     uint64_t *bar = reinterpret_cast<uint64_t *>(sm + sc::kMisc + 768);
+    uint64_t *bar_in = reinterpret_cast<uint64_t *>(sm + sc::kMisc + 784);
     uint32_t *tbase = reinterpret_cast<uint32_t *>(sm + sc::kMisc + 776);
     int *flag = reinterpret_cast<int *>(sm + sc::kMisc + 780);
 
     if (warp == 0) tc::tmem_alloc(tbase, sc::kTmemCols);
-    if (tid == 0) gdn::mbar_init(bar, 1);
+    if (tid == 0) {
+        gdn::mbar_init(bar, 1);
+        gdn::mbar_init(bar_in, 1);
+    }
 
     const int q4 = warp & 3, hc = warp >> 2;
     const int arow = 32 * q4 + lane;  // row of S held by this thread
@@ -443,44 +477,79 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_chunk_scan_kernel(const PrefA
     constexpr uint32_t id64 = tc::idesc_bf16(128, 64);
     constexpr uint32_t id128 = tc::idesc_bf16(128, 128);
 
-    uint32_t phase = 0;
+    uint32_t phase = 0, phase_in = 0;
     bool ok = true;
     const int nchunks = (len + kC - 1) / kC;
+    if (nchunks > 0) scan_prefetch(a, sm, bar_in, s0, len, seq, h, hq, 0);
     for (int c = 0; c < nchunks; ++c) {
         const int t0 = s0 + c * kC;
         const int n = min(kC, len - c * kC);
         const float *W = ws_w(a, chunk_slot(s0, c, seq), h);
         const float *Ut = W + kC * kD;
-        const float *P = W + 2 * kC * kD;
-        if (tid < kC) Gs[tid] = tid < n ? a.g[size_t(t0 + tid) * a.h_v + h] : 0.f;
-        __syncthreads();
-        if (tid == 0) {
-            float run = 0.f;
-            for (int t = 0; t < kC; ++t) {
-                run += Gs[t];
-                Gs[t] = run;
-            }
-        }
         float ut[32];  // Ut[t][arow] for t in [32hc, 32hc+32), consumed after phase A
 #pragma unroll
         for (int x = 0; x < 32; ++x) ut[x] = Ut[(32 * hc + x) * kD + arow];
+        // the chunk's raw inputs (prefetched during the previous chunk)
+        gdn::cp_async_wait<0>();
+        if (tid == 0) *flag = gdn::mbar_wait_bounded(bar_in, phase_in) ? 1 : 0;
+        __syncthreads();
+        if (*flag == 0) {
+            ok = false;
+            break;
+        }
+        (void)gdn::mbar_try_wait(bar_in, phase_in);
+        phase_in ^= 1u;
+        const float *graw = reinterpret_cast<const float *>(sm + sc::kRawG);
+        if (tid == 0) {
+            float run = 0.f;
+            for (int t = 0; t < kC; ++t) {
+                run += t < n ? graw[t] : 0.f;
+                Gs[t] = run;
+            }
+        }
         __syncthreads();
         if (tid < kC) {
             eG[tid] = expf(Gs[tid]);
             dec[tid] = tid < n ? expf(Gs[n - 1] - Gs[tid]) : 0.f;
         }
-        __syncthreads();
-        // Stage the chunk's operand tiles.
-        for (int e = tid; e < kC * (kD / 8); e += kThreads) {  // W parts and Q: row t, 8 d_k values
+        // P: raw fp32 in the P area -> registers, then the two bf16 parts in place.
+        float praw[16];
+        {
+            const int t = tid >> 2, i16 = (tid & 3) * 16;
+            const float *pr = reinterpret_cast<const float *>(sm + sc::kRawP) + t * kC + i16;
+#pragma unroll
+            for (int x = 0; x < 16; x += 4) {
+                const float4 v = *reinterpret_cast<const float4 *>(pr + x);
+                praw[x] = v.x; praw[x + 1] = v.y; praw[x + 2] = v.z; praw[x + 3] = v.w;
+            }
+        }
+        __syncthreads();  // every thread holds its P values; eG and dec are ready
+        {
+            const int t = tid >> 2, i16 = (tid & 3) * 16;
+#pragma unroll
+            for (int x = 0; x < 16; x += 8) {
+                float pe[8];
+#pragma unroll
+                for (int y = 0; y < 8; ++y) pe[y] = praw[x + y];
+                uint4 hi, lo;
+                split8(pe, hi, lo);
+                const uint32_t off = tc::swz_off(64, t, i16 + x);
+                *reinterpret_cast<uint4 *>(sm + sc::kP1 + off) = hi;
+                *reinterpret_cast<uint4 *>(sm + sc::kP2 + off) = lo;
+            }
+        }
+        // W parts (raw in the U area) and Q (raw q rows): row t, 8 d_k values.
+        for (int e = tid; e < kC * (kD / 8); e += kThreads) {
             const int t = e >> 4, j8 = (e & 15) * 8;
             float w[8];
             uint4 qv = make_uint4(0, 0, 0, 0);
             if (t < n) {
-                const float4 w0 = *reinterpret_cast<const float4 *>(W + t * kD + j8);
-                const float4 w1 = *reinterpret_cast<const float4 *>(W + t * kD + j8 + 4);
+                const float *wr = reinterpret_cast<const float *>(sm + sc::kRawW) + t * kD + j8;
+                const float4 w0 = *reinterpret_cast<const float4 *>(wr);
+                const float4 w1 = *reinterpret_cast<const float4 *>(wr + 4);
                 w[0] = w0.x; w[1] = w0.y; w[2] = w0.z; w[3] = w0.w;
                 w[4] = w1.x; w[5] = w1.y; w[6] = w1.z; w[7] = w1.w;
-                qv = __ldg(reinterpret_cast<const uint4 *>(a.q + (size_t(t0 + t) * a.h_qk + hq) * kD + j8));
+                qv = *reinterpret_cast<const uint4 *>(sm + sc::kRawQ + (t * kD + j8) * 2);
             } else {
 #pragma unroll
                 for (int y = 0; y < 8; ++y) w[y] = 0.f;
@@ -492,24 +561,16 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_chunk_scan_kernel(const PrefA
             *reinterpret_cast<uint4 *>(sm + sc::kW2 + off) = lo;
             *reinterpret_cast<uint4 *>(sm + sc::kQ + off) = qv;
         }
-        for (int e = tid; e < kC * (kC / 8); e += kThreads) {  // P parts: row t, 8 values of i
-            const int t = e >> 3, i8 = (e & 7) * 8;
-            const float4 p0 = *reinterpret_cast<const float4 *>(P + t * kC + i8);
-            const float4 p1 = *reinterpret_cast<const float4 *>(P + t * kC + i8 + 4);
-            const float pe[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
-            uint4 hi, lo;
-            split8(pe, hi, lo);
-            const uint32_t off = tc::swz_off(64, t, i8);
-            *reinterpret_cast<uint4 *>(sm + sc::kP1 + off) = hi;
-            *reinterpret_cast<uint4 *>(sm + sc::kP2 + off) = lo;
-        }
-        for (int e = tid; e < kD * (kC / 8); e += kThreads) {  // dec o K, transposed: row d_k index j, 8 tokens
-            const int j = e >> 3, i8 = (e & 7) * 8;
+        // dec o K, transposed: a warp takes 32 consecutive d_k indices j of one
+        // group of 8 tokens (conflict-free reads of the raw k rows).
+        for (int e = tid; e < kD * (kC / 8); e += kThreads) {
+            const int j = e & (kD - 1), i8 = (e / kD) * 8;
+            const uint16_t *kr = reinterpret_cast<const uint16_t *>(sm + sc::kRawK);
             float kv[8];
 #pragma unroll
             for (int y = 0; y < 8; ++y) {
                 const int i = i8 + y;
-                kv[y] = i < n ? gdn::bf16_to_f32(a.k[(size_t(t0 + i) * a.h_qk + hq) * kD + j]) * dec[i] : 0.f;
+                kv[y] = i < n ? gdn::bf16_to_f32(kr[i * kD + j]) * dec[i] : 0.f;
             }
             uint4 hi, lo;
             split8(kv, hi, lo);
@@ -595,6 +656,9 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_chunk_scan_kernel(const PrefA
         (void)gdn::mbar_try_wait(bar, phase);
         phase ^= 1u;
         tc::fence_after();
+        // Every input tile is free now: fetch the next chunk's raw inputs while
+        // the outputs and the state update below run.
+        if (c + 1 < nchunks) scan_prefetch(a, sm, bar_in, s0, len, seq, h, hq, c + 1);
         // Outputs of the chunk's tokens.
 #pragma unroll
         for (int part = 0; part < 2; ++part) {
