@@ -50,6 +50,24 @@ struct PrefArgs {
 // with P[t][i] = e^{G_t-G_i} q_t.k_i for i <= t (0 elsewhere and past the chunk).
 constexpr size_t kWsFloats = size_t(2) * kC * kD + size_t(kC) * kC;
 
+// G[t] = g[0] + ... + g[t] over the chunk (g = 0 past its n tokens), by warp 0
+// with a shuffle scan; both prefill kernels use it, so they see the same G.
+__device__ __forceinline__ void chunk_cumsum(const float *g, int n, float *G) {
+    const int lane = threadIdx.x & 31;
+    const float g0 = 2 * lane < n ? g[2 * lane] : 0.f;
+    const float g1 = 2 * lane + 1 < n ? g[2 * lane + 1] : 0.f;
+    const float pair = g0 + g1;
+    float incl = pair;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const float y = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += y;
+    }
+    const float excl = incl - pair;
+    G[2 * lane] = excl + g0;
+    G[2 * lane + 1] = excl + pair;
+}
+
 __device__ __forceinline__ float *ws_w(const PrefArgs &a, int slot, int h) {
     return a.ws + (size_t(slot) * a.h_v + h) * kWsFloats;
 }
@@ -157,12 +175,10 @@ __global__ void __launch_bounds__(kThreads) gdn_chunk_wy_kernel(const PrefArgs a
                 tc::mma_bf16(tm, d, d, idesc, (at | s) ? 1u : 0u);
             }
         tc::commit(bar);
-        float run = 0.f;  // G = cumsum(g) while the MMA runs
-        for (int t = 0; t < kC; ++t) {
-            run += Gs[t];
-            Gs[t] = run;
-        }
-        *flag = gdn::mbar_wait_bounded(bar, 0) ? 1 : 0;
+    }
+    if (warp == 0) {
+        chunk_cumsum(Gs, n, Gs);  // G = cumsum(g) while the MMA runs (in place: each lane owns two entries)
+        if (lane == 0) *flag = gdn::mbar_wait_bounded(bar, 0) ? 1 : 0;
     }
     __syncthreads();
     bool ok = *flag != 0;
@@ -500,13 +516,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_chunk_scan_kernel(const PrefA
         (void)gdn::mbar_try_wait(bar_in, phase_in);
         phase_in ^= 1u;
         const float *graw = reinterpret_cast<const float *>(sm + sc::kRawG);
-        if (tid == 0) {
-            float run = 0.f;
-            for (int t = 0; t < kC; ++t) {
-                run += t < n ? graw[t] : 0.f;
-                Gs[t] = run;
-            }
-        }
+        if (warp == 0) chunk_cumsum(graw, n, Gs);
         __syncthreads();
         if (tid < kC) {
             eG[tid] = expf(Gs[tid]);
