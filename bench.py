@@ -215,6 +215,36 @@ class ClockSampler:
 # workload set-up (device)
 # ---------------------------------------------------------------------------
 
+class timed:
+    """Records a CUDA event pair on the current stream around a block of
+    ``n`` launches into ``ev[name]`` (a list of (start, end, n)); no-op when
+    ``ev`` is None."""
+
+    def __init__(self, ev, name, n):
+        self.ev, self.name, self.n = ev, name, n
+
+    def __enter__(self):
+        if self.ev is not None:
+            self.a = torch.cuda.Event(enable_timing=True)
+            self.a.record()
+
+    def __exit__(self, *exc):
+        if self.ev is not None:
+            b = torch.cuda.Event(enable_timing=True)
+            b.record()
+            self.ev.setdefault(self.name, []).append((self.a, b, self.n))
+        return False
+
+
+def per_launch_ms(ev, name):
+    """Average device time per launch of a kernel class: the event-timed
+    spans over the launches they enclose (back-to-back launches on one
+    stream, so the few-microsecond gaps between them count against it)."""
+    spans = ev.get(name, [])
+    n = sum(x[2] for x in spans)
+    return sum(a.elapsed_time(b) for a, b, _ in spans) / max(n, 1), n
+
+
 class Bench:
     def __init__(self, spec: sy.Spec, dev, rank=0, arena=False, replay=False):
         from speculative_decoding_hybrid_gb300 import binding as gs
@@ -300,110 +330,40 @@ class Bench:
         return ring, p
 
     def step(self, ev=None):
+        """One transaction.  ``ev`` (optional) collects, per kernel class, CUDA
+        event pairs around its launches and the number of launches between
+        them: the verify pair spans every layer's launch of one step."""
         s = self.step_no
         ring, p = self.prepare(s)
         vs, loop = self.vs, self.loop
-        if self.arena:
-            return self._arena_step(ring, p, ev)
+        B = loop.B
+        rows = self.rows[ring]
         if self.replay:
-            return self._replay_step(ring, p, ev)
-        vs.txn = (vs.txn + 1) & 0xFFFFFFFF
-        for l in range(self.spec.layers):
-            if ev is not None:
-                ev["verify"][0].append(torch.cuda.Event(enable_timing=True))
-                ev["verify"][0][-1].record()
-            vs.verify_layer(l, loop.B, loop.cu_rows, loop.src_slot, self.rows[ring][l])
-            if ev is not None:
-                ev["verify"][1].append(torch.cuda.Event(enable_timing=True))
-                ev["verify"][1][-1].record()
-        if ev is not None:
-            ev["accept"][0].append(torch.cuda.Event(enable_timing=True))
-            ev["accept"][0][-1].record()
-        vs.accept(loop.B, loop.cu_rows, self.logits[ring], self.tok_d)
-        if ev is not None:
-            ev["accept"][1].append(torch.cuda.Event(enable_timing=True))
-            ev["accept"][1][-1].record()
-            ev["commit"][0].append(torch.cuda.Event(enable_timing=True))
-            ev["commit"][0][-1].record()
-        vs.commit(loop.B, loop.cu_rows, loop.dst_slot)
-        if ev is not None:
-            ev["commit"][1].append(torch.cuda.Event(enable_timing=True))
-            ev["commit"][1][-1].record()
-        acc, bon, out = loop.readback()
-        n_ver = int(acc.sum().item()) + loop.B
-        loop.finish(acc)
-        self.step_no += 1
-        self.verified += n_ver
-        return n_ver, p
-
-    def _arena_step(self, ring, p, ev=None):
-        """Zero-copy commit: verify from each request's location, point the
-        locations at the accepted checkpoints (no state copy)."""
-        from speculative_decoding_hybrid_gb300 import binding as gs
-        vs, loop = self.vs, self.loop
-        B = loop.B
-        vs.txn = (vs.txn + 1) & 0xFFFFFFFF
-        area = vs.txn & 1
-        for l in range(self.spec.layers):
-            x = self.rows[ring][l]
-            if ev is not None:
-                ev["verify"][0].append(torch.cuda.Event(enable_timing=True))
-                ev["verify"][0][-1].record()
-            gs.gdn_verify_at(vs.d, B, vs.cap, loop.cu_rows, x.q, x.k, x.v, x.g, x.beta, vs.arena, vs.total,
-                             vs.loc[l], vs.areas[area][l], vs.tags(B)[l], vs.txn, vs.o[l], vs.status)
-            if ev is not None:
-                ev["verify"][1].append(torch.cuda.Event(enable_timing=True))
-                ev["verify"][1][-1].record()
-        if ev is not None:
-            ev["accept"][0].append(torch.cuda.Event(enable_timing=True))
-            ev["accept"][0][-1].record()
-        vs.accept(B, loop.cu_rows, self.logits[ring], self.tok_d)
-        if ev is not None:
-            ev["accept"][1].append(torch.cuda.Event(enable_timing=True))
-            ev["accept"][1][-1].record()
-            ev["commit"][0].append(torch.cuda.Event(enable_timing=True))
-            ev["commit"][0][-1].record()
-        gs.gdn_commit_at(vs.d, B, vs.L, vs.cap, loop.cu_rows, vs.accept_len, vs.area_off[area],
-                         vs.ckpt_layer_stride, vs.tags(B), vs.txn, vs.loc, vs.status)
-        if ev is not None:
-            ev["commit"][1].append(torch.cuda.Event(enable_timing=True))
-            ev["commit"][1][-1].record()
-        acc, bon, out = loop.readback()
-        n_ver = int(acc.sum().item()) + B
-        loop.finish(acc)
-        self.step_no += 1
-        self.verified += n_ver
-        return n_ver, p
-
-    def _replay_step(self, ring, p, ev=None):
-        """Compact fixed-state replay: each verify commits the previous
-        transaction's accepted rows into the slot, then verifies the new rows."""
-        from speculative_decoding_hybrid_gb300 import binding as gs
-        vs, loop = self.vs, self.loop
-        B = loop.B
-        vs._advance()
-        prev = vs.prev_rows if vs.prev_rows is not None else self.rows[ring]
-        for l in range(self.spec.layers):
-            x, pr = self.rows[ring][l], prev[l]
-            if ev is not None:
-                ev["verify"][0].append(torch.cuda.Event(enable_timing=True))
-                ev["verify"][0][-1].record()
-            gs.gdn_verify_replay(vs.d, B, vs.cap, loop.cu_rows, x.q, x.k, x.v, x.g, x.beta, vs.cap, vs.prev_cu,
-                                 vs.prev_acc, pr.k, pr.v, pr.g, pr.beta, vs.pool_layer(l), vs.slot_stride,
-                                 vs.num_slots, loop.src_slot, loop.dst_slot, vs.o[l], vs.status)
-            if ev is not None:
-                ev["verify"][1].append(torch.cuda.Event(enable_timing=True))
-                ev["verify"][1][-1].record()
-        if ev is not None:
-            ev["accept"][0].append(torch.cuda.Event(enable_timing=True))
-            ev["accept"][0][-1].record()
-        vs.accept(B, loop.cu_rows, self.logits[ring], self.tok_d)
-        if ev is not None:
-            ev["accept"][1].append(torch.cuda.Event(enable_timing=True))
-            ev["accept"][1][-1].record()
-        vs.prev_cu.copy_(loop.cu_rows[:B + 1], non_blocking=True)
-        vs.prev_rows = self.rows[ring]
-        vs.pending = True
+            vs._advance()
+            with timed(ev, "verify", self.spec.layers):
+                vs._verify_all(B, loop.cu_rows, loop.src_slot, loop.dst_slot, rows)
+            with timed(ev, "accept", 1):
+                vs.accept(B, loop.cu_rows, self.logits[ring], self.tok_d)
+            vs.prev_cu.copy_(loop.cu_rows[:B + 1], non_blocking=True)
+            vs.prev_rows = rows
+            vs.pending = True
+        elif self.arena:
+            vs.txn = (vs.txn + 1) & 0xFFFFFFFF
+            with timed(ev, "verify", self.spec.layers):
+                vs.verify_all_at(B, loop.cu_rows, rows)
+            with timed(ev, "accept", 1):
+                vs.accept(B, loop.cu_rows, self.logits[ring], self.tok_d)
+            with timed(ev, "commit", 1):
+                self.gs.gdn_commit_at(vs.d, B, vs.L, vs.cap, loop.cu_rows, vs.accept_len, vs.area_off[vs.txn & 1],
+                                      vs.ckpt_layer_stride, vs.tags(B), vs.txn, vs.loc, vs.status)
+        else:
+            vs.txn = (vs.txn + 1) & 0xFFFFFFFF
+            with timed(ev, "verify", self.spec.layers):
+                vs.verify_all(B, loop.cu_rows, loop.src_slot, rows)
+            with timed(ev, "accept", 1):
+                vs.accept(B, loop.cu_rows, self.logits[ring], self.tok_d)
+            with timed(ev, "commit", 1):
+                vs.commit(B, loop.cu_rows, loop.dst_slot)
         acc, bon, out = loop.readback()
         n_ver = int(acc.sum().item()) + B
         loop.finish(acc)
@@ -426,16 +386,42 @@ class Bench:
         return verify, commit, accept
 
 
-def run_zero_copy(spec, dev, args, replay=False):
+def run_zero_copy(spec, dev, args, replay=False, graph=False):
     """The same steps with the commit that rewrites locations instead of
     copying states (verify reads from a state arena), or with compact
-    fixed-state replay (no checkpoints)."""
+    fixed-state replay (no checkpoints), optionally launched as one CUDA
+    graph per transaction."""
     b = Bench(spec, dev, 0, arena=not replay, replay=replay)
     b.precompute_drafts(args.warmup + args.steps)
     for _ in range(args.warmup):
         b.step()
     torch.cuda.synchronize()
-    ev = {"verify": ([], []), "accept": ([], []), "commit": ([], [])}
+    if graph:
+        from speculative_decoding_hybrid_gb300.step import ReplayGraphs
+        graphs = ReplayGraphs(b.vs, b.loop, b.rows, b.logits, b.tok_d)
+        start = torch.cuda.Event(enable_timing=True)
+        end = torch.cuda.Event(enable_timing=True)
+        start.record()
+        tok = 0
+        for _ in range(args.steps):
+            s = b.step_no
+            b.prepare(s)
+            graphs.launch(s, b.rows)
+            acc, bon, out = b.loop.readback()
+            tok += int(acc.sum().item()) + b.loop.B
+            b.loop.finish(acc)
+            b.step_no += 1
+        end.record()
+        torch.cuda.synchronize()
+        ms = start.elapsed_time(end)
+        if int(b.vs.status.item()) != 0:
+            raise RuntimeError("graph replay loop status %d" % int(b.vs.status.item()))
+        res = {"value": tok / (ms * 1e-3), "unit": "verified tokens/s", "ms_per_step": ms / args.steps,
+               "launches_per_step": 1, "kernels_per_step": spec.layers + 2}
+        del graphs, b
+        torch.cuda.empty_cache()
+        return res
+    ev = {}
     start = torch.cuda.Event(enable_timing=True)
     end = torch.cuda.Event(enable_timing=True)
     start.record()
@@ -447,9 +433,8 @@ def run_zero_copy(spec, dev, args, replay=False):
     end.record()
     torch.cuda.synchronize()
     ms = start.elapsed_time(end)
-    avg = lambda k: sum(x.elapsed_time(y) for x, y in zip(*ev[k])) / max(len(ev[k][0]), 1)
-    v_ms, c_ms = avg("verify"), avg("commit")
-    n_ver = len(ev["verify"][0])
+    v_ms, n_ver = per_launch_ms(ev, "verify")
+    c_ms, _ = per_launch_ms(ev, "commit")
     peak, _ = load_peaks()
     gbs = vbytes / ((v_ms * n_ver + c_ms * args.steps) * 1e-3) / 1e9
     if int(b.vs.status.item()) != 0:
@@ -679,7 +664,7 @@ def main():
         b.step()
     torch.cuda.synchronize()
 
-    ev = {"verify": ([], []), "accept": ([], []), "commit": ([], [])}
+    ev = {}
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
@@ -703,12 +688,9 @@ def main():
     ms = start.elapsed_time(end)
     ms, tok_all = reduce_across_ranks(ms, tok, dev)
 
-    def avg_ms(name):
-        s, e = ev[name]
-        return sum(a.elapsed_time(bb) for a, bb in zip(s, e)) / max(len(s), 1)
-
-    v_ms, a_ms, c_ms = avg_ms("verify"), avg_ms("accept"), avg_ms("commit")
-    n_ver_launch = len(ev["verify"][0])
+    v_ms, n_ver_launch = per_launch_ms(ev, "verify")
+    a_ms, _ = per_launch_ms(ev, "accept")
+    c_ms, _ = per_launch_ms(ev, "commit")
     peak, peak_kind = load_peaks()
     v_per_launch = vbytes / max(n_ver_launch, 1)
     achieved = v_per_launch / (v_ms * 1e-3) / 1e9
@@ -749,12 +731,14 @@ def main():
     prefill = None
     if not args.no_prefill and args.workload == "paged256":
         prefill = guarded(bench_prefill, dev, sy.prefill_lengths())
-    zero_copy = replay = None
+    zero_copy = replay = replay_graph = None
     if (args.zero_copy or args.replay) and world == 1:
         del b
         torch.cuda.empty_cache()
         if args.replay:
             replay = guarded(run_zero_copy, spec, dev, args, replay=True)
+            torch.cuda.empty_cache()
+            replay_graph = guarded(run_zero_copy, spec, dev, args, replay=True, graph=True)
             torch.cuda.empty_cache()
         if args.zero_copy:
             zero_copy = guarded(run_zero_copy, spec, dev, args)
@@ -793,6 +777,7 @@ def main():
         "prefill": prefill,
         "zero_copy_commit": zero_copy,
         "fixed_state_replay": replay,
+        "fixed_state_replay_cuda_graph": replay_graph,
     }
     print(json.dumps(line), flush=True)
     if world > 1:

@@ -141,6 +141,29 @@ int gdn_verify(const gdn_dims *dims, int32_t B, int32_t row_capacity,
                float *ckpt_layer, uint64_t *ckpt_tag, uint32_t txn,
                gdn_bf16 *o, uint32_t *dev_status, void *stream);
 
+/* Per-layer row inputs for the multi-layer calls below (device pointers). */
+typedef struct gdn_layer_rows {
+    const gdn_bf16 *q, *k, *v;
+    const float *g, *beta;
+} gdn_layer_rows;
+
+/*
+ * gdn_verify_layers -- num_layers gdn_verify calls issued from the library in
+ *   layer order on `stream` (the same kernels, arguments and results as
+ *   calling gdn_verify per layer): layer l reads rows[l] (host array of
+ *   device pointers), the slots at pool + l*layer_stride, writes checkpoints
+ *   at ckpt + l*ckpt_layer_stride, tags at ckpt_tag + l*B and outputs at
+ *   o + l*o_layer_stride.  For callers that hold every layer's inputs (a
+ *   multi-layer verifier, a benchmark): it removes the per-layer host call.
+ *   Stops at the first layer whose call fails and returns that status.
+ */
+int gdn_verify_layers(const gdn_dims *dims, int32_t num_layers, int32_t B, int32_t row_capacity,
+                      const int32_t *cu_rows, const gdn_layer_rows *rows,
+                      const float *pool, int64_t slot_stride, int64_t layer_stride,
+                      int32_t num_slots, const int32_t *src_slot,
+                      float *ckpt, int64_t ckpt_layer_stride, uint64_t *ckpt_tag, uint32_t txn,
+                      gdn_bf16 *o, int64_t o_layer_stride, uint32_t *dev_status, void *stream);
+
 /*
  * mtp_greedy_accept -- greedy acceptance ([NATIVE] greedy requests; [ENGINE]
  * Quality follow-up: verification-row selection and per-request bonus;
@@ -293,6 +316,32 @@ int gdn_verify_replay(const gdn_dims *dims, int32_t B, int32_t row_capacity,
                       float *pool_layer, int64_t slot_stride, int32_t num_slots,
                       const int32_t *src_slot, const int32_t *dst_slot,
                       gdn_bf16 *o, uint32_t *dev_status, void *stream);
+
+/*
+ * gdn_verify_at_layers -- num_layers gdn_verify_at calls in layer order:
+ *   layer l reads rows[l], the start-state offsets src_off + l*B (a [layer]
+ *   [request] table), writes checkpoints at ckpt + l*ckpt_layer_stride,
+ *   tags at ckpt_tag + l*B and outputs at o + l*o_layer_stride.  Same
+ *   contract as the per-layer call; stops at the first failing layer.
+ */
+int gdn_verify_at_layers(const gdn_dims *dims, int32_t num_layers, int32_t B, int32_t row_capacity,
+                         const int32_t *cu_rows, const gdn_layer_rows *rows,
+                         const float *state_base, int64_t state_elems_total, const int64_t *src_off,
+                         float *ckpt, int64_t ckpt_layer_stride, uint64_t *ckpt_tag, uint32_t txn,
+                         gdn_bf16 *o, int64_t o_layer_stride, uint32_t *dev_status, void *stream);
+
+/*
+ * gdn_verify_replay_layers -- num_layers gdn_verify_replay calls in layer
+ *   order (rows[l] and prev_rows[l] per layer, slots at pool + l*layer_stride,
+ *   outputs at o + l*o_layer_stride); same contract as the per-layer call.
+ */
+int gdn_verify_replay_layers(const gdn_dims *dims, int32_t num_layers, int32_t B, int32_t row_capacity,
+                             const int32_t *cu_rows, const gdn_layer_rows *rows,
+                             int32_t prev_capacity, const int32_t *prev_cu_rows,
+                             const int32_t *prev_accept_len, const gdn_layer_rows *prev_rows,
+                             float *pool, int64_t slot_stride, int64_t layer_stride, int32_t num_slots,
+                             const int32_t *src_slot, const int32_t *dst_slot,
+                             gdn_bf16 *o, int64_t o_layer_stride, uint32_t *dev_status, void *stream);
 
 /*
  * gdn_chunked_prefill -- chunked (WY/UT) GatedDeltaNet prefill of one layer

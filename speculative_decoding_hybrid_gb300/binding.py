@@ -30,7 +30,8 @@ PLAN_RECURRENT, PLAN_CHUNKED = 0, 1
 
 EXPORTS = ["gdn_decode_step", "gdn_verify", "mtp_accept_workspace_bytes", "mtp_greedy_accept",
            "mtp_greedy_accept_noalloc", "gdn_commit", "gdn_verify_at", "gdn_commit_at", "gdn_materialize",
-           "gdn_verify_replay", "gdn_selftest_wait_timeout",
+           "gdn_verify_replay", "gdn_selftest_wait_timeout", "gdn_verify_layers", "gdn_verify_at_layers",
+           "gdn_verify_replay_layers",
            "gdn_prefill_workspace_bytes", "gdn_chunked_prefill", "gdn_pool_init", "gdn_pool_alloc",
            "gdn_pool_share", "gdn_pool_release", "plan_transaction", "gdn_pool_apply", "gdn_pool_abort",
            "gdn_status_string"]
@@ -49,6 +50,18 @@ class gdn_dims(ctypes.Structure):
 
 class mtp_stats(ctypes.Structure):
     _fields_ = [(n, ctypes.c_uint64) for n in ("proposed", "evaluated", "accepted", "emitted", "steps")]
+
+
+class gdn_layer_rows(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in ("q", "k", "v", "g", "beta")]
+
+
+def layer_rows_array(rows) -> ctypes.Array:
+    """Host array of gdn_layer_rows from objects with q, k, v, g, beta tensors."""
+    arr = (gdn_layer_rows * max(len(rows), 1))()
+    for i, r in enumerate(rows):
+        arr[i] = gdn_layer_rows(_ptr(r.q), _ptr(r.k), _ptr(r.v), _ptr(r.g), _ptr(r.beta))
+    return arr
 
 
 class gdn_req(ctypes.Structure):
@@ -103,6 +116,9 @@ def _load():
         "gdn_pool_apply": [ctypes.POINTER(gdn_pool), ctypes.POINTER(gdn_plan), I32],
         "gdn_pool_abort": [ctypes.POINTER(gdn_pool), ctypes.POINTER(gdn_plan), I32],
         "gdn_status_string": [ctypes.c_int],
+        "gdn_verify_layers": [DP, I32, I32, I32, P, P, P, I64, I64, I32, P, P, I64, P, U32, P, I64, P, P],
+        "gdn_verify_at_layers": [DP, I32, I32, I32, P, P, P, I64, P, P, I64, P, U32, P, I64, P, P],
+        "gdn_verify_replay_layers": [DP, I32, I32, I32, P, P, I32, P, P, P, P, I64, I64, I32, P, P, P, I64, P, P],
         "gdn_selftest_wait_timeout": [P, ctypes.c_uint64, P],
     }
     for name, args in sig.items():
@@ -244,6 +260,34 @@ def gdn_chunked_prefill(d: gdn_dims, nseq, row_capacity, cu_seqlens, max_seqlen,
         ctypes.byref(d), nseq, row_capacity, _ptr(cu_seqlens), max_seqlen, _ptr(q), _ptr(k), _ptr(v), _ptr(g),
         _ptr(beta), _ptr(pool_layer), slot_stride, num_slots, _ptr(src_slot), _ptr(dst_slot), _ptr(o), chunk,
         _ptr(workspace), workspace_bytes, _ptr(dev_status), _stream(stream)))
+
+
+def gdn_verify_layers(d: gdn_dims, num_layers, B, row_capacity, cu_rows, rows, pool, slot_stride, layer_stride,
+                      num_slots, src_slot, ckpt, ckpt_layer_stride, ckpt_tag, txn, o, o_layer_stride, dev_status,
+                      stream=None):
+    """``rows``: a ctypes array from layer_rows_array (kept alive by the caller)."""
+    return _check("gdn_verify_layers", lib.gdn_verify_layers(
+        ctypes.byref(d), num_layers, B, row_capacity, _ptr(cu_rows), ctypes.cast(rows, ctypes.c_void_p), _ptr(pool),
+        slot_stride, layer_stride, num_slots, _ptr(src_slot), _ptr(ckpt), ckpt_layer_stride, _ptr(ckpt_tag), txn,
+        _ptr(o), o_layer_stride, _ptr(dev_status), _stream(stream)))
+
+
+def gdn_verify_at_layers(d: gdn_dims, num_layers, B, row_capacity, cu_rows, rows, state_base, state_elems_total,
+                         src_off, ckpt, ckpt_layer_stride, ckpt_tag, txn, o, o_layer_stride, dev_status, stream=None):
+    return _check("gdn_verify_at_layers", lib.gdn_verify_at_layers(
+        ctypes.byref(d), num_layers, B, row_capacity, _ptr(cu_rows), ctypes.cast(rows, ctypes.c_void_p),
+        _ptr(state_base), state_elems_total, _ptr(src_off), _ptr(ckpt), ckpt_layer_stride, _ptr(ckpt_tag), txn,
+        _ptr(o), o_layer_stride, _ptr(dev_status), _stream(stream)))
+
+
+def gdn_verify_replay_layers(d: gdn_dims, num_layers, B, row_capacity, cu_rows, rows, prev_capacity, prev_cu_rows,
+                             prev_accept_len, prev_rows, pool, slot_stride, layer_stride, num_slots, src_slot,
+                             dst_slot, o, o_layer_stride, dev_status, stream=None):
+    return _check("gdn_verify_replay_layers", lib.gdn_verify_replay_layers(
+        ctypes.byref(d), num_layers, B, row_capacity, _ptr(cu_rows), ctypes.cast(rows, ctypes.c_void_p),
+        prev_capacity, _ptr(prev_cu_rows), _ptr(prev_accept_len), ctypes.cast(prev_rows, ctypes.c_void_p),
+        _ptr(pool), slot_stride, layer_stride, num_slots, _ptr(src_slot), _ptr(dst_slot), _ptr(o), o_layer_stride,
+        _ptr(dev_status), _stream(stream)))
 
 
 def gdn_selftest_wait_timeout(dev_status, limit_ns: int, stream=None):

@@ -64,6 +64,27 @@ class VerifyStep:
         self.layer_stride = pool.stride(1)
         self.ckpt_layer_stride = self.ckpt.stride(0) if checkpoints else 0
         self.txn = 0
+        self._rows_cache = {}
+
+    def rows_array(self, layer_rows: Sequence[LayerRows]):
+        """The host gdn_layer_rows array of a list of per-layer inputs, built
+        once per list (the list is kept alive with its array)."""
+        hit = self._rows_cache.get(id(layer_rows))
+        if hit is None or hit[0] is not layer_rows:
+            if len(self._rows_cache) > 64:
+                self._rows_cache.clear()
+            hit = (layer_rows, gs.layer_rows_array(layer_rows))
+            self._rows_cache[id(layer_rows)] = hit
+        return hit[1]
+
+    def verify_all(self, B: int, cu_rows: torch.Tensor, src_slot: torch.Tensor, layer_rows: Sequence[LayerRows],
+                   stream=None):
+        """Every layer's gdn_verify, issued by one library call."""
+        assert len(layer_rows) == self.L
+        gs.gdn_verify_layers(self.d, self.L, B, self.cap, cu_rows, self.rows_array(layer_rows), self.pool,
+                             self.slot_stride, self.layer_stride, self.num_slots, src_slot, self.ckpt,
+                             self.ckpt_layer_stride, self.tags(B), self.txn, self.o, self.o.stride(0), self.status,
+                             stream)
 
     def tags(self, B: int) -> torch.Tensor:
         """Checkpoint tags laid out [layer][request] for a batch of B requests."""
@@ -92,8 +113,7 @@ class VerifyStep:
             layer_rows: Sequence[LayerRows], logits: torch.Tensor, tokens: torch.Tensor, stream=None):
         """One transaction: verify every layer, accept, commit.  Asynchronous."""
         self.txn = (self.txn + 1) & 0xFFFFFFFF
-        for l in range(self.L):
-            self.verify_layer(l, B, cu_rows, src_slot, layer_rows[l], stream)
+        self.verify_all(B, cu_rows, src_slot, layer_rows, stream)
         self.accept(B, cu_rows, logits, tokens, stream)
         self.commit(B, cu_rows, dst_slot, stream)
 
@@ -230,15 +250,19 @@ class ArenaStep(VerifyStep):
             tokens: torch.Tensor, stream=None):
         assert B == self.B
         self.txn = (self.txn + 1) & 0xFFFFFFFF
-        area = self.txn & 1
-        base = self.areas[area]
-        for l in range(self.L):
-            x = layer_rows[l]
-            gs.gdn_verify_at(self.d, B, self.cap, cu_rows, x.q, x.k, x.v, x.g, x.beta, self.arena, self.total,
-                             self.loc[l], base[l], self.tags(B)[l], self.txn, self.o[l], self.status, stream)
+        self.verify_all_at(B, cu_rows, layer_rows, stream)
         self.accept(B, cu_rows, logits, tokens, stream)
+        area = self.txn & 1
         gs.gdn_commit_at(self.d, B, self.L, self.cap, cu_rows, self.accept_len, self.area_off[area],
                          self.ckpt_layer_stride, self.tags(B), self.txn, self.loc, self.status, stream)
+
+    def verify_all_at(self, B: int, cu_rows: torch.Tensor, layer_rows: Sequence[LayerRows], stream=None):
+        """Every layer's gdn_verify_at for transaction self.txn (checkpoints
+        into area txn % 2), issued by one library call."""
+        assert B == self.B and len(layer_rows) == self.L
+        gs.gdn_verify_at_layers(self.d, self.L, B, self.cap, cu_rows, self.rows_array(layer_rows), self.arena,
+                                self.total, self.loc, self.areas[self.txn & 1], self.ckpt_layer_stride,
+                                self.tags(B), self.txn, self.o, self.o.stride(0), self.status, stream)
 
     def materialize(self, dst_slot: torch.Tensor, stream=None):
         gs.gdn_materialize(self.d, self.B, self.L, self.arena, self.total, self.loc, self.pool, self.slot_stride,
@@ -271,11 +295,11 @@ class ReplayStep(VerifyStep):
 
     def _verify_all(self, B, cu_rows, src_slot, dst_slot, layer_rows, stream=None):
         prev = self.prev_rows if self.prev_rows is not None else layer_rows
-        for l in range(self.L):
-            x, p = layer_rows[l], prev[l]
-            gs.gdn_verify_replay(self.d, B, self.cap, cu_rows, x.q, x.k, x.v, x.g, x.beta, self.cap, self.prev_cu,
-                                 self.prev_acc, p.k, p.v, p.g, p.beta, self.pool_layer(l), self.slot_stride,
-                                 self.num_slots, src_slot, dst_slot, self.o[l], self.status, stream)
+        assert len(layer_rows) == self.L and len(prev) == self.L
+        gs.gdn_verify_replay_layers(self.d, self.L, B, self.cap, cu_rows, self.rows_array(layer_rows), self.cap,
+                                    self.prev_cu, self.prev_acc, self.rows_array(prev), self.pool, self.slot_stride,
+                                    self.layer_stride, self.num_slots, src_slot, dst_slot, self.o, self.o.stride(0),
+                                    self.status, stream)
 
     def run(self, B: int, cu_rows: torch.Tensor, src_slot: torch.Tensor, dst_slot: torch.Tensor,
             layer_rows: Sequence[LayerRows], logits: torch.Tensor, tokens: torch.Tensor, stream=None):
@@ -296,3 +320,51 @@ class ReplayStep(VerifyStep):
         self._verify_all(self.B, self.no_rows, src_slot, dst_slot, self.prev_rows, stream)
         self.prev_acc.fill_(-1)
         self.pending = False
+
+
+class ReplayGraphs:
+    """CUDA-graph capture of replay transactions (one graph per input set).
+
+    A replay transaction has no per-step scalar arguments: everything it
+    reads lives in fixed device buffers (the loop's row/slot tables, the
+    tokens, the two accept-length buffers that alternate by transaction
+    parity).  With an even number of input sets cycled in order, the input
+    set index i fixes the whole launch sequence of a transaction -- 30 x
+    gdn_verify_replay (this set's rows, the previous set's accepted rows),
+    the greedy accept, and the copy of the row table for the next replay --
+    so each set gets one graph, replayed with a single launch.  The caller
+    uploads the tables and tokens before ``launch`` and reads back after."""
+
+    def __init__(self, rs: ReplayStep, loop: "DecodeLoop", ring_rows: Sequence[Sequence[LayerRows]],
+                 ring_logits: Sequence[torch.Tensor], tokens: torch.Tensor):
+        assert len(ring_rows) % 2 == 0, "the accept buffers alternate: use an even number of input sets"
+        self.rs, self.loop = rs, loop
+        self.n = len(ring_rows)
+        self.graphs = []
+        B = loop.B
+        stream = torch.cuda.Stream()
+        stream.wait_stream(torch.cuda.current_stream())
+        saved = (rs.prev_acc, rs.accept_len, rs.prev_rows, rs.pending)
+        try:
+            for i in range(self.n):
+                rs.prev_acc, rs.accept_len = rs.acc_bufs[(i + 1) % 2], rs.acc_bufs[i % 2]
+                rs.prev_rows = ring_rows[(i - 1) % self.n]
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=stream):
+                    rs._verify_all(B, loop.cu_rows, loop.src_slot, loop.dst_slot, ring_rows[i])
+                    rs.accept(B, loop.cu_rows, ring_logits[i], tokens)
+                    rs.prev_cu.copy_(loop.cu_rows[:B + 1], non_blocking=True)
+                self.graphs.append(g)
+        finally:
+            rs.prev_acc, rs.accept_len, rs.prev_rows, rs.pending = saved
+        torch.cuda.current_stream().wait_stream(stream)
+
+    def launch(self, step_no: int, ring_rows: Sequence[Sequence[LayerRows]]):
+        """Transaction number ``step_no`` (its input set is step_no % n)."""
+        i = step_no % self.n
+        rs = self.rs
+        rs.prev_acc, rs.accept_len = rs.acc_bufs[(i + 1) % 2], rs.acc_bufs[i % 2]
+        self.graphs[i].replay()
+        rs.prev_rows = ring_rows[i]
+        rs.pending = True
+

@@ -56,3 +56,19 @@ def test_host_checks_need_no_gpu(lib):
         == gs.GDN_ERR_SHAPE
     assert gs.status_string(gs.GDN_ERR_DUP_SLOT) == "duplicate destination slot"
     assert gs.mtp_accept_workspace_bytes(1024, 151936) >= 1024 * 8
+
+
+def test_multi_layer_calls_check_arguments_before_launching(lib):
+    from speculative_decoding_hybrid_gb300 import binding as gs
+    d = gs.dims(16, 32, 128, 128)
+    verify = lambda n, rows: gs.lib.gdn_verify_layers(ctypes.byref(d), n, 1, 4, None, rows, None, 0, 0, 1, None,
+                                                      None, 0, None, 0, None, 0, None, None)
+    assert verify(-1, None) == gs.GDN_ERR_ARG
+    assert verify(0, None) == gs.GDN_OK          # nothing to issue
+    assert verify(2, None) == gs.GDN_ERR_NULL
+    at = gs.lib.gdn_verify_at_layers(ctypes.byref(d), 3, 1, 4, None, None, None, 0, None, None, 0, None, 0, None,
+                                     0, None, None)
+    assert at == gs.GDN_ERR_NULL
+    rp = gs.lib.gdn_verify_replay_layers(ctypes.byref(d), -2, 1, 4, None, None, 4, None, None, None, None, 0, 0, 1,
+                                         None, None, None, 0, None, None)
+    assert rp == gs.GDN_ERR_ARG

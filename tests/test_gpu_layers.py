@@ -1,0 +1,115 @@
+"""The multi-layer calls (gdn_verify_layers, gdn_verify_at_layers,
+gdn_verify_replay_layers) issue the per-layer calls in layer order: every
+output, checkpoint, tag and slot they write is bit-for-bit what the
+layer-by-layer calls write on the same inputs."""
+import pytest
+import torch
+
+import gdnsynth as sy
+from gpu_util import build_lib
+
+pytestmark = pytest.mark.gpu
+
+DIMS = sy.Dims(4, 8, 128, 128)
+L, B, NUM_SLOTS = 3, 5, 9
+
+
+@pytest.fixture(scope="module")
+def gs(cuda_dev):
+    build_lib()
+    from speculative_decoding_hybrid_gb300 import binding
+    return binding
+
+
+def _inputs(cuda_dev, seed):
+    from speculative_decoding_hybrid_gb300.step import LayerRows
+    ks = [3, 0, 2, 1, 3]
+    cu = [0]
+    for k in ks:
+        cu.append(cu[-1] + k + 1)
+    cap = B * 4
+    rows = []
+    for l in range(L):
+        r = sy.rows(sy.generator(seed + l), cap, DIMS, cuda_dev)
+        rows.append(LayerRows(r.q, r.k, r.v, r.g, r.beta))
+    pool = sy.state(sy.generator(seed + 50), (NUM_SLOTS, L, DIMS.h_v, DIMS.d_v, DIMS.d_k)).to(cuda_dev)
+    src = torch.tensor([4, 4, 0, 7, 2], dtype=torch.int32, device=cuda_dev)   # requests 0 and 1 share slot 4
+    dst = torch.tensor([8, 1, 0, 7, 2], dtype=torch.int32, device=cuda_dev)   # the shared slot is only read
+    cu_t = torch.tensor(cu, dtype=torch.int32, device=cuda_dev)
+    return cap, cu_t, rows, pool, src, dst
+
+
+def test_verify_layers_matches_per_layer_calls(gs, cuda_dev):
+    from speculative_decoding_hybrid_gb300.step import VerifyStep
+    d = gs.dims(DIMS.h_qk, DIMS.h_v, DIMS.d_k, DIMS.d_v)
+    cap, cu, rows, pool, src, _ = _inputs(cuda_dev, 11)
+    a = VerifyStep(d, L, NUM_SLOTS, cap, B, 64, cuda_dev, pool=pool.clone())
+    b = VerifyStep(d, L, NUM_SLOTS, cap, B, 64, cuda_dev, pool=pool.clone())
+    for vs in (a, b):
+        vs.ckpt.zero_()
+        vs.o.zero_()
+        vs.txn = 7
+    for l in range(L):
+        a.verify_layer(l, B, cu, src, rows[l])
+    b.verify_all(B, cu, src, rows)
+    torch.cuda.synchronize()
+    R = int(cu[-1])
+    assert int(a.status.item()) == 0 and int(b.status.item()) == 0
+    assert torch.equal(a.o[:, :R], b.o[:, :R])
+    assert torch.equal(a.ckpt[:, :R], b.ckpt[:, :R])
+    assert torch.equal(a.tags(B), b.tags(B))
+    assert torch.equal(a.pool, b.pool) and torch.equal(b.pool, pool)     # verify leaves the slots alone
+
+
+def test_verify_at_layers_matches_per_layer_calls(gs, cuda_dev):
+    from speculative_decoding_hybrid_gb300.step import ArenaStep
+    d = gs.dims(DIMS.h_qk, DIMS.h_v, DIMS.d_k, DIMS.d_v)
+    cap, cu, rows, pool, src, _ = _inputs(cuda_dev, 21)
+    slots = src.tolist()
+    steps = []
+    for _ in range(2):
+        st = ArenaStep(d, L, NUM_SLOTS, cap, B, 64, cuda_dev)
+        st.pool.copy_(pool)
+        st.point_at_slots(slots)
+        st.arena[st.area_off[0]:].zero_()
+        st.o.zero_()
+        st.txn = 4
+        steps.append(st)
+    a, b = steps
+    for l in range(L):
+        x = rows[l]
+        gs.gdn_verify_at(a.d, B, a.cap, cu, x.q, x.k, x.v, x.g, x.beta, a.arena, a.total, a.loc[l],
+                         a.areas[a.txn & 1][l], a.tags(B)[l], a.txn, a.o[l], a.status)
+    b.verify_all_at(B, cu, rows)
+    torch.cuda.synchronize()
+    R = int(cu[-1])
+    assert int(a.status.item()) == 0 and int(b.status.item()) == 0
+    assert torch.equal(a.o[:, :R], b.o[:, :R])
+    assert torch.equal(a.areas[0][:, :R], b.areas[0][:, :R])
+    assert torch.equal(a.tags(B), b.tags(B))
+
+
+def test_verify_replay_layers_matches_per_layer_calls(gs, cuda_dev):
+    from speculative_decoding_hybrid_gb300.step import ReplayStep
+    d = gs.dims(DIMS.h_qk, DIMS.h_v, DIMS.d_k, DIMS.d_v)
+    cap, cu, rows, pool, src, dst = _inputs(cuda_dev, 31)
+    _, _, prev_rows, _, _, _ = _inputs(cuda_dev, 41)
+    prev_acc = torch.tensor([2, 0, 1, 0, 3], dtype=torch.int32, device=cuda_dev)
+    a = ReplayStep(d, L, NUM_SLOTS, cap, B, 64, cuda_dev, pool=pool.clone())
+    b = ReplayStep(d, L, NUM_SLOTS, cap, B, 64, cuda_dev, pool=pool.clone())
+    for rs in (a, b):
+        rs.prev_cu.copy_(cu)
+        rs.prev_acc.copy_(prev_acc)
+        rs.prev_rows = prev_rows
+        rs.o.zero_()
+    for l in range(L):
+        x, p = rows[l], prev_rows[l]
+        gs.gdn_verify_replay(a.d, B, a.cap, cu, x.q, x.k, x.v, x.g, x.beta, a.cap, a.prev_cu, a.prev_acc, p.k, p.v,
+                             p.g, p.beta, a.pool_layer(l), a.slot_stride, a.num_slots, src, dst, a.o[l], a.status)
+    b._verify_all(B, cu, src, dst, rows)
+    torch.cuda.synchronize()
+    R = int(cu[-1])
+    assert int(a.status.item()) == 0 and int(b.status.item()) == 0
+    assert torch.equal(a.o[:, :R], b.o[:, :R])
+    assert torch.equal(a.pool, b.pool)
+    assert not torch.equal(b.pool, pool)                                    # the replay wrote the slots

@@ -93,3 +93,64 @@ def test_replay_refuses_more_accepted_rows_than_existed(gs, cuda_dev):
     assert int(st.item()) & gs.DEV_ROWS_BAD
     assert torch.equal(pool[0], before[0])            # refused: slot untouched
     assert not torch.equal(pool[1], before[1])        # request 1 replayed its 2 rows
+
+
+def test_replay_graphs_match_eager_transactions(gs, cuda_dev):
+    """One CUDA graph per input set replays a whole transaction (30 verify
+    launches in the paged workload, 2 here) with identical results."""
+    from speculative_decoding_hybrid_gb300.step import DecodeLoop, LayerRows, ReplayGraphs, ReplayStep
+    dims = sy.Dims(4, 8, 128, 128)
+    d = gs.dims(dims.h_qk, dims.h_v, dims.d_k, dims.d_v)
+    L, B, num_slots, vocab, ring, steps = 2, 5, 8, 2048, 4, 9
+    cap = B * 4
+    init = sy.state(sy.generator(8), (num_slots, L, dims.h_v, dims.d_v, dims.d_k)).to(cuda_dev)
+    slots = [0, 1, 2, 3, 4]
+    mk = lambda: gs.Pool(num_slots)
+    pools = []
+    for _ in range(2):
+        p = mk()
+        for _ in range(5):
+            p.alloc()
+        pools.append(p)
+    eager = ReplayStep(d, L, num_slots, cap, B, vocab, cuda_dev, pool=init.clone())
+    graph = ReplayStep(d, L, num_slots, cap, B, vocab, cuda_dev, pool=init.clone())
+    le, lg_ = DecodeLoop(eager, slots, pools[0]), DecodeLoop(graph, slots, pools[1])
+    rows = [[LayerRows(*(t for t in (r.q, r.k, r.v, r.g, r.beta)))
+             for r in (sy.rows(sy.generator(100 * i + l), cap, dims, cuda_dev) for l in range(L))] for i in range(ring)]
+    logits = [sy.logits(sy.generator(200 + i), cap, vocab, 2.0, cuda_dev) for i in range(ring)]
+    tok_e = torch.zeros(cap, dtype=torch.int32, device=cuda_dev)
+    tok_g = torch.zeros(cap, dtype=torch.int32, device=cuda_dev)
+    lg_.plan_step([3] * B)          # the tables the graphs read exist before capture
+    lg_.upload_tables()
+    graphs = ReplayGraphs(graph, lg_, rows, [x[0] for x in logits], tok_g)
+    # restart the graph loop's planner state (the capture executed nothing)
+    lg_.pool = pools[1] = mk()
+    for _ in range(5):
+        lg_.pool.alloc()
+    lg_.req_np[:B, 3] = 1
+    for s in range(steps):
+        i = s % ring
+        ks = [3, 2, 3, 1, 3]
+        pe, pg = le.plan_step(ks), lg_.plan_step(ks)
+        assert pe.dec_cu == pg.dec_cu
+        tk = sum(sy.drafts(sy.generator(300 + s), logits[i][1].tolist(), ks, vocab, 0.85), [])
+        tk = torch.tensor(tk + [0] * (cap - len(tk)), dtype=torch.int32)
+        tok_e.copy_(tk)
+        tok_g.copy_(tk)
+        le.upload_tables()
+        eager.run(B, le.cu_rows, le.src_slot, le.dst_slot, rows[i], logits[i][0], tok_e)
+        ae = le.readback()[0].clone()
+        lg_.upload_tables()
+        graphs.launch(s, rows)
+        ag = lg_.readback()[0].clone()
+        assert torch.equal(ae, ag), s
+        R = pe.dec_cu[-1]
+        assert torch.equal(eager.o[:, :R], graph.o[:, :R]), s
+        le.finish(ae)
+        lg_.finish(ag)
+    cur = torch.tensor(le.slot, dtype=torch.int32, device=cuda_dev)
+    eager.flush(cur, cur)
+    graph.flush(cur, cur)
+    torch.cuda.synchronize()
+    assert int(eager.status.item()) == 0 and int(graph.status.item()) == 0
+    assert torch.equal(eager.pool, graph.pool)
