@@ -128,6 +128,70 @@ def bench_prefill(dev, lengths, reps=5, warmup=3):
             "workspace_gb": ws_bytes / 1e9}
 
 
+def bench_mixed(dev, lengths, n_decode=256, layers=30, reps=3, warmup=1, vocab=151936):
+    """One mixed transaction over every layer: the prefill set (chunked,
+    publishing final states) and n_decode decode requests asking for K=3,
+    which the planner defers to one row each (verify + accept + commit).
+    Timed with the prefills on a side stream (overlapped) and in order on
+    one stream.  Every layer reads the same prefill input set (1.6 GB, larger
+    than L2) and its own decode rows."""
+    from speculative_decoding_hybrid_gb300 import binding as gs
+    from speculative_decoding_hybrid_gb300.step import LayerRows, MixedTransaction, VerifyStep
+    dims = sy.DIMS_FULL
+    d = gs.dims(dims.h_qk, dims.h_v, dims.d_k, dims.d_v)
+    n = len(lengths)
+    num_slots = n_decode + n + 8
+    pool_c = gs.Pool(num_slots)
+    dec_slots = [pool_c.alloc() for _ in range(n_decode)]
+    cont = [pool_c.alloc() for _ in range(n - n // 2)]       # continued prefixes
+    reqs = [(gs.REQ_PREFILL, 0, L, 0, 1 << 30, -1) for L in lengths[:n // 2]] + \
+           [(gs.REQ_PREFILL, 0, L, 64, 1 << 30, s) for L, s in zip(lengths[n // 2:], cont)] + \
+           [(gs.REQ_DECODE, 3, 0, 100, 1 << 30, s) for s in dec_slots]
+    R = sum(lengths)
+    plan = gs.Plan(len(reqs))
+    st = gs.plan_transaction(gs.make_reqs(reqs), len(reqs), gs.gdn_plan_limits(R + 4 * n_decode, len(reqs), 3),
+                             pool_c, plan)
+    if st != gs.GDN_OK or plan.c.n_decode != n_decode or plan.c.n_prefill != n:
+        raise RuntimeError("mixed plan: status %d" % st)
+    pool = torch.empty((num_slots, layers, dims.h_v, dims.d_v, dims.d_k), dtype=torch.float32, device=dev)
+    sy.state(sy.generator(5, dev), pool.shape, dev, out=pool)
+    vs = VerifyStep(d, layers, num_slots, n_decode, n_decode, vocab, dev, pool=pool)
+    rows, cu, _ = sy.prefill_inputs(lengths, dims, seed=3, device=dev)
+    pre = [LayerRows(rows.q, rows.k, rows.v, rows.g, rows.beta)] * layers
+    dec = []
+    for l in range(layers):
+        x = sy.rows(sy.generator(sy.mix_seed(6, l), dev), n_decode, dims, dev)
+        dec.append(LayerRows(x.q, x.k, x.v, x.g, x.beta))
+    lg, _ = sy.logits(sy.generator(7, dev), n_decode, vocab, 2.0, dev)
+    tok = torch.zeros(n_decode, dtype=torch.int32, device=dev)
+    o = torch.empty((R, dims.h_v, dims.d_v), dtype=torch.bfloat16, device=dev)
+    res = {"prefill_tokens": R, "sequences": n, "decode_requests": n_decode, "layers": layers,
+           "deferred_drafts": plan.deferred}
+    for overlap in (True, False):
+        mt = MixedTransaction(vs, n, R, overlap=overlap)
+        mt.upload(plan)
+        for _ in range(warmup):
+            mt.run(plan, dec, pre, [o] * layers, lg, tok)
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(reps):
+            mt.run(plan, dec, pre, [o] * layers, lg, tok)
+        b.record()
+        torch.cuda.synchronize()
+        ms = a.elapsed_time(b) / reps
+        res["ms_overlapped" if overlap else "ms_in_order"] = ms
+        del mt
+    if int(vs.status.item()) != 0:
+        raise RuntimeError("mixed transaction status %d" % int(vs.status.item()))
+    ms = res["ms_overlapped"]
+    res["tokens_per_s"] = (R + n_decode) / (ms * 1e-3)
+    res["alg_tflops_prefill"] = prefill_flops(lengths, dims.h_v) * layers / (ms * 1e-3) / 1e12
+    del vs, pool
+    torch.cuda.empty_cache()
+    return res
+
+
 def rank_spec(spec: sy.Spec, rank: int) -> sy.Spec:
     """Requests are independent problems: rank r runs its own batch, drawn
     with its own seed (weak scaling, no data-path exchange)."""
@@ -728,9 +792,10 @@ def main():
             torch.cuda.synchronize()
             return {"error": "%s: %s" % (type(e).__name__, e)}
 
-    prefill = None
+    prefill = mixed = None
     if not args.no_prefill and args.workload == "paged256":
         prefill = guarded(bench_prefill, dev, sy.prefill_lengths())
+        mixed = guarded(bench_mixed, dev, sy.prefill_lengths())
     zero_copy = replay = replay_graph = None
     if (args.zero_copy or args.replay) and world == 1:
         del b
@@ -775,6 +840,7 @@ def main():
         "cpu_baseline": cpu,
         "acceptance": {"verified_tokens": tok, "requests": spec.batch},
         "prefill": prefill,
+        "mixed_transaction": mixed,
         "zero_copy_commit": zero_copy,
         "fixed_state_replay": replay,
         "fixed_state_replay_cuda_graph": replay_graph,

@@ -368,3 +368,88 @@ class ReplayGraphs:
         rs.prev_rows = ring_rows[i]
         rs.pending = True
 
+
+class MixedTransaction:
+    """One planned transaction that holds both prefill sequences and decode
+    requests, for every layer.
+
+    The planner has already deferred every draft of such a transaction (each
+    decode request verifies one row) and given every writer a destination
+    slot that no other request of the transaction reads, so the two halves
+    touch disjoint state: the prefills (``gdn_chunked_prefill`` per layer,
+    publishing only final states) run on a side stream while the decode half
+    (verify of every layer, greedy accept, commit) runs on the caller's
+    stream.  Before returning, the caller's stream waits for the side stream,
+    so whatever is queued next (the readback, the next transaction's verify
+    of a just-prefilled sequence) sees the published states.  With
+    ``overlap=False`` both halves run in order on the caller's stream.
+    """
+
+    def __init__(self, vs: VerifyStep, max_seqs: int, max_prefill_rows: int, chunk: int = 64,
+                 overlap: bool = True):
+        self.vs = vs
+        self.max_seqs = max_seqs
+        self.max_rows = max_prefill_rows
+        self.chunk = chunk
+        self.overlap = overlap
+        self.ws_bytes = gs.gdn_prefill_workspace_bytes(vs.d, max_seqs, max_prefill_rows)
+        self.ws = torch.empty((max(self.ws_bytes, 8),), dtype=torch.uint8, device=vs.dev)
+        n = max(vs.max_batch, max_seqs)
+        self.h_tab = torch.zeros((6, n + 1), dtype=torch.int32).pin_memory()
+        self.h_np = self.h_tab.numpy()
+        self.d_tab = torch.zeros((6, n + 1), dtype=torch.int32, device=vs.dev)
+        self.side = torch.cuda.Stream(device=vs.dev) if overlap else None
+        self.done = torch.cuda.Event()
+
+    def upload(self, plan: "gs.Plan", stream=None):
+        """Copies the plan's decode (cu, src, dst) and prefill (cu, src, dst)
+        tables to the device on the caller's stream."""
+        a, c = plan.arrays, plan.c
+        B, P = c.n_decode, c.n_prefill
+        if B > self.vs.max_batch or P > self.max_seqs:
+            raise ValueError("plan larger than the transaction buffers")
+        if P and a["pre_cu"][P] > self.max_rows:
+            raise ValueError("prefill rows exceed the workspace")
+        self.h_np[0, :B + 1] = a["dec_cu"][:B + 1]
+        self.h_np[1, :B] = a["dec_src"][:B]
+        self.h_np[2, :B] = a["dec_dst"][:B]
+        self.h_np[3, :P + 1] = a["pre_cu"][:P + 1]
+        self.h_np[4, :P] = a["pre_src"][:P]
+        self.h_np[5, :P] = a["pre_dst"][:P]
+        self.d_tab.copy_(self.h_tab, non_blocking=True)
+
+    def prefill_layers(self, plan: "gs.Plan", pre_rows: Sequence[LayerRows], pre_o, stream=None):
+        vs, c = self.vs, plan.c
+        P = c.n_prefill
+        pre_cu = plan.arrays["pre_cu"]
+        R = int(pre_cu[P])
+        max_len = int(max(pre_cu[i + 1] - pre_cu[i] for i in range(P)))
+        for l in range(vs.L):
+            x = pre_rows[l]
+            gs.gdn_chunked_prefill(vs.d, P, R, self.d_tab[3], max_len, x.q, x.k, x.v, x.g, x.beta, vs.pool_layer(l),
+                                   vs.slot_stride, vs.num_slots, self.d_tab[4, :P], self.d_tab[5, :P], pre_o[l],
+                                   self.chunk, self.ws, self.ws_bytes, vs.status, stream)
+
+    def run(self, plan: "gs.Plan", dec_rows: Sequence[LayerRows], pre_rows: Sequence[LayerRows], pre_o,
+            logits: torch.Tensor, tokens: torch.Tensor):
+        """Queues the transaction (after ``upload``).  ``pre_o[l]`` receives
+        layer l's prefill outputs; decode outputs land in ``vs.o``."""
+        vs, c = self.vs, plan.c
+        B, P = c.n_decode, c.n_prefill
+        main = torch.cuda.current_stream(vs.dev)
+        if P:
+            if self.overlap:
+                self.side.wait_stream(main)          # tables and inputs are queued on the caller's stream
+                with torch.cuda.stream(self.side):
+                    self.prefill_layers(plan, pre_rows, pre_o)
+                self.done.record(self.side)
+            else:
+                self.prefill_layers(plan, pre_rows, pre_o)
+        if B:
+            vs.txn = (vs.txn + 1) & 0xFFFFFFFF
+            cu, src, dst = self.d_tab[0], self.d_tab[1, :B], self.d_tab[2, :B]
+            vs.verify_all(B, cu, src, dec_rows)
+            vs.accept(B, cu, logits, tokens)
+            vs.commit(B, cu, dst)
+        if P and self.overlap:
+            main.wait_event(self.done)
