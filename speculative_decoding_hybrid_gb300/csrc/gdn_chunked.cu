@@ -12,9 +12,9 @@
 // Two kernels, both on the 5th-generation tensor cores (tcgen05).
 //  (1) gdn_chunk_wy_kernel -- one CTA per (chunk, v-head), all chunks of all
 //      sequences at once (state-independent): [K;Q] K^T, the unit
-//      lower-triangular inverse T in 16x16 blocks, W and Ut, and the masked,
-//      decayed P = M o Q K^T; W, Ut and P go to the workspace (fp32, 80 KB
-//      per chunk and head).
+//      lower-triangular inverse T in 16x16 blocks, W and Ut, the masked,
+//      decayed P = M o Q K^T and dec o K; they go to the workspace already in
+//      the scan's operand-tile layout (128.25 KB per chunk and head).
 //  (2) gdn_chunk_scan_kernel -- one CTA per (sequence, v-head): the only
 //      sequential part.  The state stays on chip across the sequence's
 //      chunks; per chunk it forms U, the outputs and the next state.
@@ -46,12 +46,25 @@ struct PrefArgs {
     uint32_t *status;
 };
 
-// Workspace per (chunk slot, v-head): W [C][D], Ut [C][D] and P [C][C], fp32,
-// with P[t][i] = e^{G_t-G_i} q_t.k_i for i <= t (0 elsewhere and past the chunk).
-constexpr size_t kWsFloats = size_t(2) * kC * kD + size_t(kC) * kC;
+// Workspace per (chunk slot, v-head): everything the scan needs for one chunk,
+// written by the per-chunk kernel in the scan's own shared-memory layout so
+// that the scan fetches it with bulk copies and starts its products at once.
+// Operand tiles are 128-byte-swizzled K-major bf16 tiles (tc.cuh); "parts"
+// are the two-term bf16 split x = x1 + x2, x1 = bf16(x), x2 = bf16(x - x1).
+namespace blob {
+constexpr uint32_t kW1 = 0, kW2 = 16384;     // W = T diag(beta e^G) K parts: 64 rows (t) x 128 (d_k)
+constexpr uint32_t kQ = 32768;               // Q (exact bf16):               64 rows (t) x 128 (d_k)
+constexpr uint32_t kP1 = 49152, kP2 = 57344; // P = M o Q K^T parts:         64 rows (t) x  64 (i)
+constexpr uint32_t kK1 = 65536, kK2 = 81920; // (dec o K)^T parts:          128 rows (d_k) x 64 (i)
+constexpr uint32_t kTiles = 98304;           // bytes of operand tiles (one contiguous block)
+constexpr uint32_t kUt = 98304;              // Ut = T diag(beta) V, fp32 [t][d_v]
+constexpr uint32_t kEG = 131072;             // e^{G_t}, fp32 x 64
+constexpr uint32_t kBytes = 131328;
+}  // namespace blob
+constexpr size_t kWsFloats = blob::kBytes / 4;
 
 // G[t] = g[0] + ... + g[t] over the chunk (g = 0 past its n tokens), by warp 0
-// with a shuffle scan; both prefill kernels use it, so they see the same G.
+// with a shuffle scan.
 __device__ __forceinline__ void chunk_cumsum(const float *g, int n, float *G) {
     const int lane = threadIdx.x & 31;
     const float g0 = 2 * lane < n ? g[2 * lane] : 0.f;
@@ -68,31 +81,45 @@ __device__ __forceinline__ void chunk_cumsum(const float *g, int n, float *G) {
     G[2 * lane + 1] = excl + pair;
 }
 
-__device__ __forceinline__ float *ws_w(const PrefArgs &a, int slot, int h) {
-    return a.ws + (size_t(slot) * a.h_v + h) * kWsFloats;
+__device__ __forceinline__ unsigned char *ws_blob(const PrefArgs &a, int slot, int h) {
+    return reinterpret_cast<unsigned char *>(a.ws) + (size_t(slot) * a.h_v + h) * blob::kBytes;
+}
+
+// Two-term bf16 split of 8 consecutive values, packed as two 16-byte chunks.
+__device__ __forceinline__ void split8(const float *x, uint4 &hi, uint4 &lo) {
+    uint32_t h[4], l[4];
+#pragma unroll
+    for (int p = 0; p < 4; ++p) {
+        const uint16_t h0 = gdn::f32_to_bf16(x[2 * p]), h1 = gdn::f32_to_bf16(x[2 * p + 1]);
+        const uint16_t l0 = gdn::f32_to_bf16(x[2 * p] - gdn::bf16_to_f32(h0));
+        const uint16_t l1 = gdn::f32_to_bf16(x[2 * p + 1] - gdn::bf16_to_f32(h1));
+        h[p] = uint32_t(h0) | (uint32_t(h1) << 16);
+        l[p] = uint32_t(l0) | (uint32_t(l1) << 16);
+    }
+    hi = make_uint4(h[0], h[1], h[2], h[3]);
+    lo = make_uint4(l[0], l[1], l[2], l[3]);
 }
 
 // ---------------------------------------------------------------------------
 // (1) per-chunk WY/UT quantities on the tensor cores (tcgen05, kind::f16)
 // ---------------------------------------------------------------------------
-// Shared-memory map (bytes from a 1024-aligned base).  Operand tiles are
-// 128-byte-swizzled K-major bf16 tiles (tc.cuh):
-//   A1   [K; Q]   128 rows (tokens, then q rows) x 128 (d_k)      32 KB
-//   KT   K^T      128 rows (d_k) x 64 (tokens)                   16 KB
-//   VT   V^T      128 rows (d_v) x 64 (tokens)                   16 KB
-//   TB   T diag(beta e^G), hi and lo bf16 parts, 64 x 64 each  2 x 8 KB
-//   TV   T diag(beta),     hi and lo                           2 x 8 KB
+// Shared-memory map (bytes from a 1024-aligned base), bf16 K-major tiles:
+//   A1   [K; Q]          128 rows (tokens, then q rows) x 128 (d_k)   32 KB
+//   KV   [K^T; V^T]      256 rows (d_k, then d_v) x 64 (tokens)       32 KB
+//   AB   [T diag(beta e^G); T diag(beta)], hi and lo parts,
+//                        128 rows (t, twice) x 64 (i)              2 x 16 KB
 //   (the fp32 matrix A -> T, [64][65], and the 16x16 block scratch of the
-//    inversion live in the TB/TV area before those tiles are written)
-//   misc G, beta, e^G, mbarrier, tensor-memory base, flags
-// Tensor memory (256 columns): D1 = [K;Q] K^T at columns 0..63 (rows 0..63:
-// K K^T, rows 64..127: Q K^T, which becomes P for the scan), D2 = W^T at
-// 64..127, D3 = Ut^T at 128..191 (lane = d index).
+//    inversion live in the AB area before those tiles are written)
+//   misc G, beta, e^G, mbarrier, tensor-memory base, flag, dec
+// Tensor memory (256 columns): first D1 = [K;Q] K^T at columns 0..63 (rows
+// 0..63: K K^T, rows 64..127: Q K^T), then D2 = AB [K^T; V^T]^T at 0..255:
+// rows 0..63 x columns 0..127 hold W, rows 64..127 x columns 128..255 hold Ut
+// (the two cross blocks are not used).
 namespace wy {
 constexpr uint32_t kA1 = 0, kKT = 32768, kVT = 49152, kT = 65536, kMisc = 98304;
-constexpr uint32_t kTbHi = kT, kTbLo = kT + 8192, kTvHi = kT + 16384, kTvLo = kT + 24576;
+constexpr uint32_t kAbHi = kT, kAbLo = kT + 16384;
 constexpr uint32_t kXScratch = kT + 16640;  // after the fp32 [64][65] matrix
-constexpr size_t kSmem = kMisc + 1024 + 1024;  // + alignment slack
+constexpr size_t kSmem = kMisc + 2048 + 1024;  // + alignment slack
 constexpr uint32_t kTmemCols = 256;
 }  // namespace wy
 
@@ -114,6 +141,7 @@ __global__ void __launch_bounds__(kThreads) gdn_chunk_wy_kernel(const PrefArgs a
     const int n = min(kC, len - c * kC);
     const int hq = h / a.grp;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    unsigned char *out = ws_blob(a, chunk_slot(s0, c, seq), h);
 
     extern __shared__ unsigned char smraw[];
     const uint32_t raw_u = gdn::smem_u32(smraw);
@@ -127,12 +155,14 @@ __global__ void __launch_bounds__(kThreads) gdn_chunk_wy_kernel(const PrefArgs a
     uint64_t *bar = reinterpret_cast<uint64_t *>(sm + wy::kMisc + 768);
     uint32_t *tbase = reinterpret_cast<uint32_t *>(sm + wy::kMisc + 776);
     int *flag = reinterpret_cast<int *>(sm + wy::kMisc + 780);
+    float *dec = reinterpret_cast<float *>(sm + wy::kMisc + 1024);
 
     if (warp == 0) tc::tmem_alloc(tbase, wy::kTmemCols);
     if (tid == 0) gdn::mbar_init(bar, 1);
 
-    // Stage K, Q (rows of A1), K^T and V^T as bf16 operand tiles; rows past n are zero.
-    // A warp covers 32 consecutive tokens of one 8-column group, so the
+    // Stage K, Q (rows of A1), K^T and V^T as bf16 operand tiles; rows past n
+    // are zero.  Q also goes to the workspace as the scan's 64-row Q tile.  A
+    // warp covers 32 consecutive tokens of one 8-column group, so the
     // transposed stores of a warp land in one row of K^T / V^T (no bank conflicts).
     for (int e = tid; e < kC * (kD / 8); e += kThreads) {
         const int t = e % kC, c8 = (e / kC) * 8;
@@ -144,6 +174,7 @@ __global__ void __launch_bounds__(kThreads) gdn_chunk_wy_kernel(const PrefArgs a
         }
         *reinterpret_cast<uint4 *>(sm + wy::kA1 + tc::swz_off(128, t, c8)) = kv;
         *reinterpret_cast<uint4 *>(sm + wy::kA1 + tc::swz_off(128, kC + t, c8)) = qv;
+        *reinterpret_cast<uint4 *>(out + blob::kQ + tc::swz_off(64, t, c8)) = qv;
         const uint32_t kw[4] = {kv.x, kv.y, kv.z, kv.w};
         const uint32_t vw[4] = {vv.x, vv.y, vv.z, vv.w};
 #pragma unroll
@@ -164,7 +195,7 @@ __global__ void __launch_bounds__(kThreads) gdn_chunk_wy_kernel(const PrefArgs a
     tc::fence_after();
     const uint32_t tm = *tbase;
 
-    // D1 = A1 K^T: rows 0..63 are K K^T (rows 64..127, Q K^T, are not used here).
+    // D1 = A1 K^T: rows 0..63 are K K^T, rows 64..127 are Q K^T.
     if (tid == 0) {
         constexpr uint32_t idesc = tc::idesc_bf16(128, 64);
 #pragma unroll
@@ -185,11 +216,15 @@ __global__ void __launch_bounds__(kThreads) gdn_chunk_wy_kernel(const PrefArgs a
     if (ok) {
         (void)gdn::mbar_try_wait(bar, 0);
         tc::fence_after();
-        if (tid < kC) eG[tid] = expf(Gs[tid]);
+        if (tid < kC) {
+            eG[tid] = expf(Gs[tid]);
+            dec[tid] = tid < n ? expf(Gs[n - 1] - Gs[tid]) : 0.f;
+            reinterpret_cast<float *>(out + blob::kEG)[tid] = eG[tid];
+        }
         // Rows 0..63: A[t][i] = beta_t e^{G_t-G_i} (k_t.k_i), i < t.
-        // Rows 64..127: P[t][i] = e^{G_t-G_i} (q_t.k_i), i <= t, to the workspace.
+        // Rows 64..127: P[t][i] = e^{G_t-G_i} (q_t.k_i), i <= t, split into
+        // its two parts straight into the workspace tiles.
         const int q4 = warp & 3, hc = warp >> 2;
-        float *Pw = ws_w(a, chunk_slot(s0, c, seq), h) + 2 * kC * kD;
         const int t = 32 * (q4 & 1) + lane;
 #pragma unroll
         for (int part = 0; part < 2; ++part) {
@@ -203,22 +238,41 @@ __global__ void __launch_bounds__(kThreads) gdn_chunk_wy_kernel(const PrefArgs a
                     Af[t * (kC + 1) + i] = (i < t && t < n) ? Bs[t] * expf(Gs[t] - Gs[i]) * v16[x] : 0.f;
                 }
             } else {
+                float pe[16];
 #pragma unroll
-                for (int x = 0; x < 16; x += 4) {
-                    float4 pv;
-                    float *pe = &pv.x;
+                for (int x = 0; x < 16; ++x) {
+                    const int i = col0 + x;
+                    pe[x] = (i <= t && t < n) ? expf(Gs[t] - Gs[i]) * v16[x] : 0.f;
+                }
 #pragma unroll
-                    for (int y = 0; y < 4; ++y) {
-                        const int i = col0 + x + y;
-                        pe[y] = (i <= t && t < n) ? expf(Gs[t] - Gs[i]) * v16[x + y] : 0.f;
-                    }
-                    *reinterpret_cast<float4 *>(Pw + t * kC + col0 + x) = pv;
+                for (int x = 0; x < 16; x += 8) {
+                    uint4 hi, lo;
+                    split8(pe + x, hi, lo);
+                    const uint32_t off = tc::swz_off(64, t, col0 + x);
+                    *reinterpret_cast<uint4 *>(out + blob::kP1 + off) = hi;
+                    *reinterpret_cast<uint4 *>(out + blob::kP2 + off) = lo;
                 }
             }
         }
     }
     __syncthreads();
     if (ok) {
+        // (dec o K)^T parts for the scan's state update: the K^T tile already
+        // has the scan's layout, so 16-byte piece e of the tile (row j = e/8)
+        // is scaled by dec over its 8 tokens and stored at the same offset.
+        for (int e = tid; e < kD * kC / 8; e += kThreads) {
+            const int j = e >> 3, i8 = ((e & 7) ^ (j & 7)) * 8;
+            const uint4 kr = *reinterpret_cast<const uint4 *>(sm + wy::kKT + e * 16);
+            const uint32_t kw[4] = {kr.x, kr.y, kr.z, kr.w};
+            float kv[8];
+#pragma unroll
+            for (int y = 0; y < 8; ++y)
+                kv[y] = gdn::bf16_to_f32(uint16_t(y & 1 ? kw[y >> 1] >> 16 : kw[y >> 1] & 0xffffu)) * dec[i8 + y];
+            uint4 hi, lo;
+            split8(kv, hi, lo);
+            *reinterpret_cast<uint4 *>(out + blob::kK1 + e * 16) = hi;
+            *reinterpret_cast<uint4 *>(out + blob::kK2 + e * 16) = lo;
+        }
         // (I + A)^{-1} by 16x16 blocks.  Diagonal blocks: column substitution.
         float col[16];
         const int blk = tid >> 4, cc = tid & 15;
@@ -256,7 +310,7 @@ __global__ void __launch_bounds__(kThreads) gdn_chunk_wy_kernel(const PrefArgs a
             }
             __syncthreads();
         }
-        // T_b = T diag(beta e^G), T_v = T diag(beta), each split into bf16 hi + lo.
+        // AB rows t: T diag(beta e^G); rows 64 + t: T diag(beta); hi and lo parts.
         const int t = tid >> 2, i0 = (tid & 3) * 16;
         float tv[16];
 #pragma unroll
@@ -264,35 +318,21 @@ __global__ void __launch_bounds__(kThreads) gdn_chunk_wy_kernel(const PrefArgs a
         __syncthreads();  // every T entry is read before the tiles overwrite it
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
-            uint32_t bh[4], bl[4], vh[4], vl[4];
+            float xb[8], xv[8];
 #pragma unroll
-            for (int p = 0; p < 4; ++p) {
-                uint32_t wbh = 0, wbl = 0, wvh = 0, wvl = 0;
-#pragma unroll
-                for (int e2 = 0; e2 < 2; ++e2) {
-                    const int x = half * 8 + p * 2 + e2;
-                    const int i = i0 + x;
-                    const float xb = tv[x] * Bs[i] * eG[i];
-                    const float xv = tv[x] * Bs[i];
-                    const uint16_t hb = gdn::f32_to_bf16(xb);
-                    const uint16_t lb = gdn::f32_to_bf16(xb - gdn::bf16_to_f32(hb));
-                    const uint16_t hv = gdn::f32_to_bf16(xv);
-                    const uint16_t lv = gdn::f32_to_bf16(xv - gdn::bf16_to_f32(hv));
-                    wbh |= uint32_t(hb) << (16 * e2);
-                    wbl |= uint32_t(lb) << (16 * e2);
-                    wvh |= uint32_t(hv) << (16 * e2);
-                    wvl |= uint32_t(lv) << (16 * e2);
-                }
-                bh[p] = wbh;
-                bl[p] = wbl;
-                vh[p] = wvh;
-                vl[p] = wvl;
+            for (int y = 0; y < 8; ++y) {
+                const int i = i0 + half * 8 + y;
+                xv[y] = tv[half * 8 + y] * Bs[i];
+                xb[y] = xv[y] * eG[i];
             }
-            const uint32_t off = tc::swz_off(64, t, i0 + half * 8);
-            *reinterpret_cast<uint4 *>(sm + wy::kTbHi + off) = make_uint4(bh[0], bh[1], bh[2], bh[3]);
-            *reinterpret_cast<uint4 *>(sm + wy::kTbLo + off) = make_uint4(bl[0], bl[1], bl[2], bl[3]);
-            *reinterpret_cast<uint4 *>(sm + wy::kTvHi + off) = make_uint4(vh[0], vh[1], vh[2], vh[3]);
-            *reinterpret_cast<uint4 *>(sm + wy::kTvLo + off) = make_uint4(vl[0], vl[1], vl[2], vl[3]);
+            uint4 bh, bl, vh, vl;
+            split8(xb, bh, bl);
+            split8(xv, vh, vl);
+            const uint32_t ob = tc::swz_off(128, t, i0 + half * 8), ov = tc::swz_off(128, kC + t, i0 + half * 8);
+            *reinterpret_cast<uint4 *>(sm + wy::kAbHi + ob) = bh;
+            *reinterpret_cast<uint4 *>(sm + wy::kAbLo + ob) = bl;
+            *reinterpret_cast<uint4 *>(sm + wy::kAbHi + ov) = vh;
+            *reinterpret_cast<uint4 *>(sm + wy::kAbLo + ov) = vl;
         }
         gdn::fence_proxy_async_smem();
         tc::fence_before();
@@ -300,16 +340,13 @@ __global__ void __launch_bounds__(kThreads) gdn_chunk_wy_kernel(const PrefArgs a
     __syncthreads();
     if (ok && tid == 0) {
         tc::fence_after();
-        // D2 = K^T (T_b)^T = W^T, D3 = V^T (T_v)^T = Ut^T; hi and lo parts accumulate.
-        constexpr uint32_t idesc = tc::idesc_bf16(128, 64);
+        // D2 = AB [K^T; V^T]^T (M = 128, N = 256); hi and lo parts accumulate.
+        constexpr uint32_t idesc = tc::idesc_bf16(128, 256);
 #pragma unroll
         for (int s = 0; s < 4; ++s) {
-            const uint64_t ak = tc::smem_desc(sb + wy::kKT + s * 32);
-            const uint64_t av = tc::smem_desc(sb + wy::kVT + s * 32);
-            tc::mma_bf16(tm + 64, ak, tc::smem_desc(sb + wy::kTbHi + s * 32), idesc, s ? 1u : 0u);
-            tc::mma_bf16(tm + 64, ak, tc::smem_desc(sb + wy::kTbLo + s * 32), idesc, 1u);
-            tc::mma_bf16(tm + 128, av, tc::smem_desc(sb + wy::kTvHi + s * 32), idesc, s ? 1u : 0u);
-            tc::mma_bf16(tm + 128, av, tc::smem_desc(sb + wy::kTvLo + s * 32), idesc, 1u);
+            const uint64_t b = tc::smem_desc(sb + wy::kKT + s * 32);
+            tc::mma_bf16(tm, tc::smem_desc(sb + wy::kAbHi + s * 32), b, idesc, s ? 1u : 0u);
+            tc::mma_bf16(tm, tc::smem_desc(sb + wy::kAbLo + s * 32), b, idesc, 1u);
         }
         tc::commit(bar);
         *flag = gdn::mbar_wait_bounded(bar, 1) ? 1 : 0;
@@ -319,20 +356,36 @@ __global__ void __launch_bounds__(kThreads) gdn_chunk_wy_kernel(const PrefArgs a
     if (ok) {
         (void)gdn::mbar_try_wait(bar, 1);
         tc::fence_after();
-        float *W = ws_w(a, chunk_slot(s0, c, seq), h);
-        float *Ut = W + kC * kD;
         const int q4 = warp & 3, hc = warp >> 2;
-        const int j = 32 * q4 + lane;  // d index = accumulator lane
+        const int t = 32 * (q4 & 1) + lane;  // token row = accumulator lane (mod 64)
+        const uint32_t lane_base = uint32_t(32 * q4) << 16;
+        if (q4 < 2) {
+            // W row t -> its two bf16 parts in the scan's W tiles
 #pragma unroll
-        for (int part = 0; part < 2; ++part) {
-            const int col0 = 32 * hc + 16 * part;
-            float w16[16], u16[16];
-            tc::ld16(tm + (uint32_t(32 * q4) << 16) + 64u + uint32_t(col0), w16);
-            tc::ld16(tm + (uint32_t(32 * q4) << 16) + 128u + uint32_t(col0), u16);
+            for (int part = 0; part < 4; ++part) {
+                const int col = 64 * hc + 16 * part;
+                float w16[16];
+                tc::ld16(tm + lane_base + uint32_t(col), w16);
 #pragma unroll
-            for (int x = 0; x < 16; ++x) {
-                W[(col0 + x) * kD + j] = w16[x];
-                Ut[(col0 + x) * kD + j] = u16[x];
+                for (int x = 0; x < 16; x += 8) {
+                    uint4 hi, lo;
+                    split8(w16 + x, hi, lo);
+                    const uint32_t off = tc::swz_off(64, t, col + x);
+                    *reinterpret_cast<uint4 *>(out + blob::kW1 + off) = hi;
+                    *reinterpret_cast<uint4 *>(out + blob::kW2 + off) = lo;
+                }
+            }
+        } else {
+            // Ut row t, fp32
+            float *Ut = reinterpret_cast<float *>(out + blob::kUt) + t * kD;
+#pragma unroll
+            for (int part = 0; part < 4; ++part) {
+                const int col = 64 * hc + 16 * part;
+                float u16[16];
+                tc::ld16(tm + lane_base + 128u + uint32_t(col), u16);
+#pragma unroll
+                for (int x = 0; x < 16; x += 4)
+                    *reinterpret_cast<float4 *>(Ut + col + x) = make_float4(u16[x], u16[x + 1], u16[x + 2], u16[x + 3]);
             }
         }
     } else if (tid == 0) {
@@ -349,72 +402,38 @@ __global__ void __launch_bounds__(kThreads) gdn_chunk_wy_kernel(const PrefArgs a
 // One CTA per (sequence, v-head); the 128 value rows of S are the M = 128
 // side of every product, so each thread owns one row of S (lane quadrant of
 // its warp) and half of its columns.  The FP32 master copy of S stays in
-// registers for the whole sequence.  Every operand that is not exactly bf16
-// is split into two bf16 parts, x = x1 + x2 with x1 = bf16(x) and
-// x2 = bf16(x - x1) (about 2^-16 relative), and a product keeps the three
-// leading terms a1 b1 + a1 b2 + a2 b1; q and k are exact bf16.  Per chunk:
+// registers for the whole sequence.  S and U are split into two bf16 parts
+// here; W, P and dec o K arrive split from the per-chunk kernel; a product
+// keeps the three leading terms a1 b1 + a1 b2 + a2 b1; q and k are exact
+// bf16.  Per chunk:
 //   phase A:  Uacc = S W^T         (M128 N64  K128)  -> U^T = Ut^T - Uacc
 //             Oi   = S Q^T         (M128 N64  K128)
 //   phase B:  Oa   = U^T P^T       (M128 N64  K64)
 //             dS   = U^T (dec o K) (M128 N128 K64),   S <- e^{G_last} S + dS
-//   o_t = q_scale (e^{G_t} Oi[:,t] + Oa[:,t]),  dec_i = e^{G_last - G_i},
-// with P, W and Ut from the per-chunk kernel's workspace.
+//   o_t = q_scale (e^{G_t} Oi[:,t] + Oa[:,t]),  dec_i = e^{G_last - G_i}.
 // Shared-memory map (bytes from a 1024-aligned base), bf16 K-major tiles:
 namespace sc {
-constexpr uint32_t kS1 = 0, kS2 = 32768;        // S parts      128 rows (d_v) x 128 (d_k)
-constexpr uint32_t kW1 = 65536, kW2 = 81920;    // W parts       64 rows (t)   x 128 (d_k)
-constexpr uint32_t kQ = 98304;                  // Q             64 rows (t)   x 128 (d_k)
-constexpr uint32_t kP1 = 114688, kP2 = 122880;  // P parts       64 rows (t)   x  64 (i)
-constexpr uint32_t kK1 = 131072, kK2 = 147456;  // dec K parts  128 rows (d_k) x  64 (i)
-constexpr uint32_t kU1 = 163840, kU2 = 180224;  // U^T parts    128 rows (d_v) x  64 (i)
-constexpr uint32_t kMisc = 196608;              // G, e^G, dec, mbarriers, tensor-memory base, flag
-constexpr uint32_t kRawQ = 197632;              // next chunk's raw q rows (bf16 64 x 128)
-constexpr uint32_t kRawK = 214016;              // next chunk's raw k rows (bf16 64 x 128)
-constexpr uint32_t kRawG = 230400;              // next chunk's g (fp32 x 64)
-constexpr size_t kSmem = kRawG + 256 + 1024;
+constexpr uint32_t kS1 = 0, kS2 = 32768;  // S parts       128 rows (d_v) x 128 (d_k)
+constexpr uint32_t kTiles = 65536;        // the chunk's W, Q, P and dec o K tiles, in the workspace layout
+constexpr uint32_t kW1 = kTiles + blob::kW1, kW2 = kTiles + blob::kW2, kQ = kTiles + blob::kQ;
+constexpr uint32_t kP1 = kTiles + blob::kP1, kP2 = kTiles + blob::kP2;
+constexpr uint32_t kK1 = kTiles + blob::kK1, kK2 = kTiles + blob::kK2;
+constexpr uint32_t kU1 = kTiles + blob::kTiles, kU2 = kU1 + 16384;  // U^T parts 128 rows (d_v) x 64 (i)
+constexpr uint32_t kMisc = kU2 + 16384;   // e^G (two chunks' worth), mbarriers, tensor-memory base, flag
+constexpr size_t kSmem = kMisc + 1024 + 1024;
 constexpr uint32_t kTmemCols = 512;  // Uacc 0..63, Oi 64..127, Oa 128..191, dS 256..383
-// The next chunk's raw W and P (fp32, from the workspace) land in the U and
-// P tile areas, which are free from the end of phase B until they are
-// consumed by the next chunk's staging.
-constexpr uint32_t kRawW = kU1, kRawP = kP1;
 }  // namespace sc
 
-// Prefetch of chunk c's raw inputs: W (32 KB) and P (16 KB) from the
-// workspace, q and k rows (256 B each) by bulk asynchronous copies on one
-// mbarrier, g by 4-byte cp.async.  Called by every thread.
-__device__ __forceinline__ void scan_prefetch(const PrefArgs &a, unsigned char *sm, uint64_t *bar, int s0, int len,
-                                              int seq, int h, int hq, int c) {
-    const int tid = threadIdx.x;
-    const int t0 = s0 + c * kC;
-    const int n = min(kC, len - c * kC);
-    const float *W = ws_w(a, chunk_slot(s0, c, seq), h);
-    if (tid < 32) {
-        if (tid == 0) gdn::mbar_arrive_expect_tx(bar, uint32_t(kC * kD * 4 + kC * kC * 4 + 2 * n * kD * 2));
-        __syncwarp();
-        if (tid == 0) gdn::bulk_g2s(sm + sc::kRawW, W, kC * kD * 4, bar);
-        if (tid == 1) gdn::bulk_g2s(sm + sc::kRawP, W + 2 * kC * kD, kC * kC * 4, bar);
-        for (int t = tid; t < n; t += 32) {
-            gdn::bulk_g2s(sm + sc::kRawQ + t * kD * 2, a.q + (size_t(t0 + t) * a.h_qk + hq) * kD, kD * 2, bar);
-            gdn::bulk_g2s(sm + sc::kRawK + t * kD * 2, a.k + (size_t(t0 + t) * a.h_qk + hq) * kD, kD * 2, bar);
-        }
-    }
-    if (tid < n) gdn::cp_async4(sm + sc::kRawG + tid * 4, a.g + size_t(t0 + tid) * a.h_v + h);
-    gdn::cp_async_commit();
-}
-
-// Two-term bf16 split of 8 consecutive values, packed as two 16-byte chunks.
-__device__ __forceinline__ void split8(const float (&x)[8], uint4 &hi, uint4 &lo) {
-    uint32_t h[4], l[4];
-#pragma unroll
-    for (int p = 0; p < 4; ++p) {
-        const uint16_t h0 = gdn::f32_to_bf16(x[2 * p]), h1 = gdn::f32_to_bf16(x[2 * p + 1]);
-        const uint16_t l0 = gdn::f32_to_bf16(x[2 * p] - gdn::bf16_to_f32(h0));
-        const uint16_t l1 = gdn::f32_to_bf16(x[2 * p + 1] - gdn::bf16_to_f32(h1));
-        h[p] = uint32_t(h0) | (uint32_t(h1) << 16);
-        l[p] = uint32_t(l0) | (uint32_t(l1) << 16);
-    }
-    hi = make_uint4(h[0], h[1], h[2], h[3]);
-    lo = make_uint4(l[0], l[1], l[2], l[3]);
+// Fetch of chunk c's tiles (96 KB, six bulk copies) and e^G (256 B) into
+// e^G buffer c % 2, all on one mbarrier.  Called by warp 0.
+__device__ __forceinline__ void scan_prefetch(const PrefArgs &a, unsigned char *sm, uint64_t *bar, int s0, int seq,
+                                              int h, int c) {
+    const int lane = threadIdx.x & 31;
+    const unsigned char *src = ws_blob(a, chunk_slot(s0, c, seq), h);
+    if (lane == 0) gdn::mbar_arrive_expect_tx(bar, blob::kTiles + 256u);
+    __syncwarp();
+    if (lane < 6) gdn::bulk_g2s(sm + sc::kTiles + lane * 16384, src + lane * 16384, 16384u, bar);
+    if (lane == 6) gdn::bulk_g2s(sm + sc::kMisc + (c & 1) * 256, src + blob::kEG, 256u, bar);
 }
 
 __global__ void __launch_bounds__(kThreads, 1) gdn_chunk_scan_kernel(const PrefArgs a) {
@@ -433,15 +452,11 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_chunk_scan_kernel(const PrefA
         if (h == 0 && tid == 0) gdn::set_status(a.status, bad);
         return;
     }
-    const int hq = h / a.grp;
 
     extern __shared__ unsigned char smraw[];
     const uint32_t raw_u = gdn::smem_u32(smraw);
     unsigned char *sm = smraw + (((raw_u + 1023u) & ~1023u) - raw_u);
     const uint32_t sb = gdn::smem_u32(sm);
-    float *Gs = reinterpret_cast<float *>(sm + sc::kMisc);
-    float *eG = Gs + kC;
-    float *dec = eG + kC;
     uint64_t *bar = reinterpret_cast<uint64_t *>(sm + sc::kMisc + 768);
     uint64_t *bar_in = reinterpret_cast<uint64_t *>(sm + sc::kMisc + 784);
     uint32_t *tbase = reinterpret_cast<uint32_t *>(sm + sc::kMisc + 776);
@@ -475,18 +490,16 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_chunk_scan_kernel(const PrefA
     auto write_S = [&]() {
 #pragma unroll
         for (int x = 0; x < 8; ++x) {
-            float e[8];
-#pragma unroll
-            for (int y = 0; y < 8; ++y) e[y] = sv[8 * x + y];
             uint4 hi, lo;
-            split8(e, hi, lo);
+            split8(sv + 8 * x, hi, lo);
             const uint32_t off = tc::swz_off(128, arow, 64 * hc + 8 * x);
             *reinterpret_cast<uint4 *>(sm + sc::kS1 + off) = hi;
             *reinterpret_cast<uint4 *>(sm + sc::kS2 + off) = lo;
         }
+        gdn::fence_proxy_async_smem();
+        tc::fence_before();
     };
     write_S();
-    tc::fence_before();
     __syncthreads();
     tc::fence_after();
     const uint32_t tm = *tbase;
@@ -496,17 +509,15 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_chunk_scan_kernel(const PrefA
     uint32_t phase = 0, phase_in = 0;
     bool ok = true;
     const int nchunks = (len + kC - 1) / kC;
-    if (nchunks > 0) scan_prefetch(a, sm, bar_in, s0, len, seq, h, hq, 0);
+    if (nchunks > 0 && warp == 0) scan_prefetch(a, sm, bar_in, s0, seq, h, 0);
     for (int c = 0; c < nchunks; ++c) {
         const int t0 = s0 + c * kC;
         const int n = min(kC, len - c * kC);
-        const float *W = ws_w(a, chunk_slot(s0, c, seq), h);
-        const float *Ut = W + kC * kD;
+        const float *Ut = reinterpret_cast<const float *>(ws_blob(a, chunk_slot(s0, c, seq), h) + blob::kUt);
         float ut[32];  // Ut[t][arow] for t in [32hc, 32hc+32), consumed after phase A
 #pragma unroll
         for (int x = 0; x < 32; ++x) ut[x] = Ut[(32 * hc + x) * kD + arow];
-        // the chunk's raw inputs (prefetched during the previous chunk)
-        gdn::cp_async_wait<0>();
+        // The chunk's tiles (fetched during the previous chunk); S parts are written.
         if (tid == 0) *flag = gdn::mbar_wait_bounded(bar_in, phase_in) ? 1 : 0;
         __syncthreads();
         if (*flag == 0) {
@@ -515,82 +526,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_chunk_scan_kernel(const PrefA
         }
         (void)gdn::mbar_try_wait(bar_in, phase_in);
         phase_in ^= 1u;
-        const float *graw = reinterpret_cast<const float *>(sm + sc::kRawG);
-        if (warp == 0) chunk_cumsum(graw, n, Gs);
-        __syncthreads();
-        if (tid < kC) {
-            eG[tid] = expf(Gs[tid]);
-            dec[tid] = tid < n ? expf(Gs[n - 1] - Gs[tid]) : 0.f;
-        }
-        // P: raw fp32 in the P area -> registers, then the two bf16 parts in place.
-        float praw[16];
-        {
-            const int t = tid >> 2, i16 = (tid & 3) * 16;
-            const float *pr = reinterpret_cast<const float *>(sm + sc::kRawP) + t * kC + i16;
-#pragma unroll
-            for (int x = 0; x < 16; x += 4) {
-                const float4 v = *reinterpret_cast<const float4 *>(pr + x);
-                praw[x] = v.x; praw[x + 1] = v.y; praw[x + 2] = v.z; praw[x + 3] = v.w;
-            }
-        }
-        __syncthreads();  // every thread holds its P values; eG and dec are ready
-        {
-            const int t = tid >> 2, i16 = (tid & 3) * 16;
-#pragma unroll
-            for (int x = 0; x < 16; x += 8) {
-                float pe[8];
-#pragma unroll
-                for (int y = 0; y < 8; ++y) pe[y] = praw[x + y];
-                uint4 hi, lo;
-                split8(pe, hi, lo);
-                const uint32_t off = tc::swz_off(64, t, i16 + x);
-                *reinterpret_cast<uint4 *>(sm + sc::kP1 + off) = hi;
-                *reinterpret_cast<uint4 *>(sm + sc::kP2 + off) = lo;
-            }
-        }
-        // W parts (raw in the U area) and Q (raw q rows): row t, 8 d_k values.
-        for (int e = tid; e < kC * (kD / 8); e += kThreads) {
-            const int t = e >> 4, j8 = (e & 15) * 8;
-            float w[8];
-            uint4 qv = make_uint4(0, 0, 0, 0);
-            if (t < n) {
-                const float *wr = reinterpret_cast<const float *>(sm + sc::kRawW) + t * kD + j8;
-                const float4 w0 = *reinterpret_cast<const float4 *>(wr);
-                const float4 w1 = *reinterpret_cast<const float4 *>(wr + 4);
-                w[0] = w0.x; w[1] = w0.y; w[2] = w0.z; w[3] = w0.w;
-                w[4] = w1.x; w[5] = w1.y; w[6] = w1.z; w[7] = w1.w;
-                qv = *reinterpret_cast<const uint4 *>(sm + sc::kRawQ + (t * kD + j8) * 2);
-            } else {
-#pragma unroll
-                for (int y = 0; y < 8; ++y) w[y] = 0.f;
-            }
-            uint4 hi, lo;
-            split8(w, hi, lo);
-            const uint32_t off = tc::swz_off(64, t, j8);
-            *reinterpret_cast<uint4 *>(sm + sc::kW1 + off) = hi;
-            *reinterpret_cast<uint4 *>(sm + sc::kW2 + off) = lo;
-            *reinterpret_cast<uint4 *>(sm + sc::kQ + off) = qv;
-        }
-        // dec o K, transposed: a warp takes 32 consecutive d_k indices j of one
-        // group of 8 tokens (conflict-free reads of the raw k rows).
-        for (int e = tid; e < kD * (kC / 8); e += kThreads) {
-            const int j = e & (kD - 1), i8 = (e / kD) * 8;
-            const uint16_t *kr = reinterpret_cast<const uint16_t *>(sm + sc::kRawK);
-            float kv[8];
-#pragma unroll
-            for (int y = 0; y < 8; ++y) {
-                const int i = i8 + y;
-                kv[y] = i < n ? gdn::bf16_to_f32(kr[i * kD + j]) * dec[i] : 0.f;
-            }
-            uint4 hi, lo;
-            split8(kv, hi, lo);
-            const uint32_t off = tc::swz_off(128, j, i8);
-            *reinterpret_cast<uint4 *>(sm + sc::kK1 + off) = hi;
-            *reinterpret_cast<uint4 *>(sm + sc::kK2 + off) = lo;
-        }
-        gdn::fence_proxy_async_smem();
-        tc::fence_before();
-        __syncthreads();
+        const float *eG = reinterpret_cast<const float *>(sm + sc::kMisc + (c & 1) * 256);
         // Phase A: Uacc = S W^T, Oi = S Q^T.
         if (tid == 0) {
             tc::fence_after();
@@ -666,9 +602,9 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_chunk_scan_kernel(const PrefA
         (void)gdn::mbar_try_wait(bar, phase);
         phase ^= 1u;
         tc::fence_after();
-        // Every input tile is free now: fetch the next chunk's raw inputs while
-        // the outputs and the state update below run.
-        if (c + 1 < nchunks) scan_prefetch(a, sm, bar_in, s0, len, seq, h, hq, c + 1);
+        // Every tile is free now: fetch the next chunk's while the outputs and
+        // the state update below run.
+        if (c + 1 < nchunks && warp == 0) scan_prefetch(a, sm, bar_in, s0, seq, h, c + 1);
         // Outputs of the chunk's tokens.
 #pragma unroll
         for (int part = 0; part < 2; ++part) {
@@ -694,7 +630,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_chunk_scan_kernel(const PrefA
             for (int x = 0; x < 16; ++x) sv[16 * part + x] = fmaf(egl, sv[16 * part + x], v16[x]);
         }
         write_S();
-        // (the next chunk's staging ends with the proxy fence and barrier the MMAs need)
+        // (the barrier after the next chunk's tile wait orders these stores before its MMAs)
     }
     if (ok) {
         float4 *dp = reinterpret_cast<float4 *>(a.pool + size_t(dst) * a.slot_stride + row_off);
@@ -740,6 +676,7 @@ extern "C" int gdn_chunked_prefill(const gdn_dims *dims, int32_t nseq, int32_t r
         return GDN_ERR_ARG;
     const size_t need = gdn_prefill_workspace_bytes(dims, nseq, row_capacity);
     if (!workspace || workspace_bytes < need) return GDN_ERR_WORKSPACE;
+    if (!gdn_host::aligned16(workspace)) return GDN_ERR_ARG;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     PrefArgs a{};
     a.cu = cu_seqlens;
