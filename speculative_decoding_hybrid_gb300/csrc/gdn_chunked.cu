@@ -57,7 +57,7 @@ constexpr uint32_t kQ = 32768;               // Q (exact bf16):               64
 constexpr uint32_t kP1 = 49152, kP2 = 57344; // P = M o Q K^T parts:         64 rows (t) x  64 (i)
 constexpr uint32_t kK1 = 65536, kK2 = 81920; // (dec o K)^T parts:          128 rows (d_k) x 64 (i)
 constexpr uint32_t kTiles = 98304;           // bytes of operand tiles (one contiguous block)
-constexpr uint32_t kUt = 98304;              // Ut = T diag(beta) V, fp32 [t][d_v]
+constexpr uint32_t kUt = 98304;              // Ut = T diag(beta) V, fp32 [t][d_v] (pieces permuted, ut_index)
 constexpr uint32_t kEG = 131072;             // e^{G_t}, fp32 x 64
 constexpr uint32_t kBytes = 131328;
 }  // namespace blob
@@ -108,9 +108,13 @@ __device__ __forceinline__ void split8(const float *x, uint4 &hi, uint4 &lo) {
 //   KV   [K^T; V^T]      256 rows (d_k, then d_v) x 64 (tokens)       32 KB
 //   AB   [T diag(beta e^G); T diag(beta)], hi and lo parts,
 //                        128 rows (t, twice) x 64 (i)              2 x 16 KB
-//   (the fp32 matrix A -> T, [64][65], and the 16x16 block scratch of the
-//    inversion live in the AB area before those tiles are written)
+//   (the fp32 matrix A -> T, [64][65], lives in the AB area before those
+//    tiles are written)
 //   misc G, beta, e^G, mbarrier, tensor-memory base, flag, dec
+// Outputs are staged in areas whose operands have been consumed and leave by
+// bulk copies: the Q tile is rows 64..127 of both A1 atoms as they stand; the
+// P parts replace rows 0..63 of the two A1 atoms after the first product; the
+// W parts replace [K^T; V^T] and Ut replaces AB after the second.
 // Tensor memory (256 columns): first D1 = [K;Q] K^T at columns 0..63 (rows
 // 0..63: K K^T, rows 64..127: Q K^T), then D2 = AB [K^T; V^T]^T at 0..255:
 // rows 0..63 x columns 0..127 hold W, rows 64..127 x columns 128..255 hold Ut
@@ -118,15 +122,18 @@ __device__ __forceinline__ void split8(const float *x, uint4 &hi, uint4 &lo) {
 namespace wy {
 constexpr uint32_t kA1 = 0, kKT = 32768, kVT = 49152, kT = 65536, kMisc = 98304;
 constexpr uint32_t kAbHi = kT, kAbLo = kT + 16384;
-constexpr uint32_t kXScratch = kT + 16640;  // after the fp32 [64][65] matrix
+constexpr uint32_t kStP1 = kA1, kStP2 = kA1 + 16384;  // 8 KB each
+constexpr uint32_t kStW1 = kKT, kStW2 = kVT;          // 16 KB each
+constexpr uint32_t kStUt = kT;                        // 32 KB
 constexpr size_t kSmem = kMisc + 2048 + 1024;  // + alignment slack
 constexpr uint32_t kTmemCols = 256;
 }  // namespace wy
 
-__device__ __forceinline__ float tri_T(const float *Af, int x, int y) {
-    // unit lower-triangular T stored as its strict lower part
-    return x == y ? 1.f : (x > y ? Af[x * (kC + 1) + y] : 0.f);
-}
+// Ut in the workspace: fp32 rows t of 128 values whose 16-byte pieces are
+// permuted within each 128-byte segment by (piece ^ (t & 7)), so that the
+// per-chunk kernel stages it without bank conflicts while a warp of the scan
+// still reads 32 consecutive values of one row from one segment.
+__host__ __device__ constexpr int ut_index(int t, int j) { return t * kD + ((((j >> 2) ^ (t & 7))) << 2) + (j & 3); }
 
 __global__ void __launch_bounds__(kThreads) gdn_chunk_wy_kernel(const PrefArgs a) {
     const int seq = blockIdx.x / a.max_chunks;
@@ -148,7 +155,6 @@ __global__ void __launch_bounds__(kThreads) gdn_chunk_wy_kernel(const PrefArgs a
     unsigned char *sm = smraw + (((raw_u + 1023u) & ~1023u) - raw_u);
     const uint32_t sb = gdn::smem_u32(sm);
     float *Af = reinterpret_cast<float *>(sm + wy::kT);
-    float *Xs = reinterpret_cast<float *>(sm + wy::kXScratch);
     float *Gs = reinterpret_cast<float *>(sm + wy::kMisc);
     float *Bs = Gs + kC;
     float *eG = Bs + kC;
@@ -161,33 +167,47 @@ __global__ void __launch_bounds__(kThreads) gdn_chunk_wy_kernel(const PrefArgs a
     if (tid == 0) gdn::mbar_init(bar, 1);
 
     // Stage K, Q (rows of A1), K^T and V^T as bf16 operand tiles; rows past n
-    // are zero.  Q also goes to the workspace as the scan's 64-row Q tile.  A
-    // warp covers 32 consecutive tokens of one 8-column group, so the
-    // transposed stores of a warp land in one row of K^T / V^T (no bank conflicts).
-    for (int e = tid; e < kC * (kD / 8); e += kThreads) {
-        const int t = e % kC, c8 = (e / kC) * 8;
-        uint4 kv = make_uint4(0, 0, 0, 0), qv = kv, vv = kv;
-        if (t < n) {
-            kv = __ldg(reinterpret_cast<const uint4 *>(a.k + (size_t(t0 + t) * a.h_qk + hq) * kD + c8));
-            qv = __ldg(reinterpret_cast<const uint4 *>(a.q + (size_t(t0 + t) * a.h_qk + hq) * kD + c8));
-            vv = __ldg(reinterpret_cast<const uint4 *>(a.v + (size_t(t0 + t) * a.h_v + h) * kD + c8));
-        }
-        *reinterpret_cast<uint4 *>(sm + wy::kA1 + tc::swz_off(128, t, c8)) = kv;
-        *reinterpret_cast<uint4 *>(sm + wy::kA1 + tc::swz_off(128, kC + t, c8)) = qv;
-        *reinterpret_cast<uint4 *>(out + blob::kQ + tc::swz_off(64, t, c8)) = qv;
-        const uint32_t kw[4] = {kv.x, kv.y, kv.z, kv.w};
-        const uint32_t vw[4] = {vv.x, vv.y, vv.z, vv.w};
+    // are zero.  Every load is issued before the first store.  A warp covers
+    // 32 consecutive tokens of one 8-column group, so the transposed stores of
+    // a warp land in one row of K^T / V^T (no bank conflicts).
+    {
+        uint4 kv[4], qv[4], vv[4];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const uint16_t ke = uint16_t(i & 1 ? kw[i >> 1] >> 16 : kw[i >> 1] & 0xffffu);
-            const uint16_t ve = uint16_t(i & 1 ? vw[i >> 1] >> 16 : vw[i >> 1] & 0xffffu);
-            *reinterpret_cast<uint16_t *>(sm + wy::kKT + tc::swz_off(128, c8 + i, t)) = ke;
-            *reinterpret_cast<uint16_t *>(sm + wy::kVT + tc::swz_off(128, c8 + i, t)) = ve;
+        for (int it = 0; it < 4; ++it) {
+            const int e = tid + it * kThreads;
+            const int t = e % kC, c8 = (e / kC) * 8;
+            kv[it] = qv[it] = vv[it] = make_uint4(0, 0, 0, 0);
+            if (t < n) {
+                kv[it] = __ldg(reinterpret_cast<const uint4 *>(a.k + (size_t(t0 + t) * a.h_qk + hq) * kD + c8));
+                qv[it] = __ldg(reinterpret_cast<const uint4 *>(a.q + (size_t(t0 + t) * a.h_qk + hq) * kD + c8));
+                vv[it] = __ldg(reinterpret_cast<const uint4 *>(a.v + (size_t(t0 + t) * a.h_v + h) * kD + c8));
+            }
         }
-    }
-    if (tid < kC) {
-        Bs[tid] = tid < n ? a.beta[size_t(t0 + tid) * a.h_v + h] : 0.f;
-        Gs[tid] = tid < n ? a.g[size_t(t0 + tid) * a.h_v + h] : 0.f;
+        float bt = 0.f, gt = 0.f;
+        if (tid < n) {
+            bt = a.beta[size_t(t0 + tid) * a.h_v + h];
+            gt = a.g[size_t(t0 + tid) * a.h_v + h];
+        }
+#pragma unroll
+        for (int it = 0; it < 4; ++it) {
+            const int e = tid + it * kThreads;
+            const int t = e % kC, c8 = (e / kC) * 8;
+            *reinterpret_cast<uint4 *>(sm + wy::kA1 + tc::swz_off(128, t, c8)) = kv[it];
+            *reinterpret_cast<uint4 *>(sm + wy::kA1 + tc::swz_off(128, kC + t, c8)) = qv[it];
+            const uint32_t kw[4] = {kv[it].x, kv[it].y, kv[it].z, kv[it].w};
+            const uint32_t vw[4] = {vv[it].x, vv[it].y, vv[it].z, vv[it].w};
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const uint16_t ke = uint16_t(i & 1 ? kw[i >> 1] >> 16 : kw[i >> 1] & 0xffffu);
+                const uint16_t ve = uint16_t(i & 1 ? vw[i >> 1] >> 16 : vw[i >> 1] & 0xffffu);
+                *reinterpret_cast<uint16_t *>(sm + wy::kKT + tc::swz_off(128, c8 + i, t)) = ke;
+                *reinterpret_cast<uint16_t *>(sm + wy::kVT + tc::swz_off(128, c8 + i, t)) = ve;
+            }
+        }
+        if (tid < kC) {
+            Bs[tid] = bt;
+            Gs[tid] = gt;
+        }
     }
     gdn::fence_proxy_async_smem();
     tc::fence_before();
@@ -221,9 +241,10 @@ __global__ void __launch_bounds__(kThreads) gdn_chunk_wy_kernel(const PrefArgs a
             dec[tid] = tid < n ? expf(Gs[n - 1] - Gs[tid]) : 0.f;
             reinterpret_cast<float *>(out + blob::kEG)[tid] = eG[tid];
         }
-        // Rows 0..63: A[t][i] = beta_t e^{G_t-G_i} (k_t.k_i), i < t.
-        // Rows 64..127: P[t][i] = e^{G_t-G_i} (q_t.k_i), i <= t, split into
-        // its two parts straight into the workspace tiles.
+        // Rows 0..63: A[t][i] = beta_t e^{G_t-G_i} (k_t.k_i), i < t (0 elsewhere).
+        // Rows 64..127: P[t][i] = e^{G_t-G_i} (q_t.k_i), i <= t, split into its
+        // two parts in the staging area (rows 0..63 of the A1 atoms: the K rows,
+        // consumed by the product above).
         const int q4 = warp & 3, hc = warp >> 2;
         const int t = 32 * (q4 & 1) + lane;
 #pragma unroll
@@ -249,13 +270,22 @@ __global__ void __launch_bounds__(kThreads) gdn_chunk_wy_kernel(const PrefArgs a
                     uint4 hi, lo;
                     split8(pe + x, hi, lo);
                     const uint32_t off = tc::swz_off(64, t, col0 + x);
-                    *reinterpret_cast<uint4 *>(out + blob::kP1 + off) = hi;
-                    *reinterpret_cast<uint4 *>(out + blob::kP2 + off) = lo;
+                    *reinterpret_cast<uint4 *>(sm + wy::kStP1 + off) = hi;
+                    *reinterpret_cast<uint4 *>(sm + wy::kStP2 + off) = lo;
                 }
             }
         }
+        gdn::fence_proxy_async_smem();
     }
     __syncthreads();
+    if (ok && tid == 0) {
+        // Q tile (rows 64..127 of both A1 atoms) and the P parts.
+        gdn::bulk_s2g(out + blob::kQ, sm + wy::kA1 + 8192, 8192u);
+        gdn::bulk_s2g(out + blob::kQ + 8192, sm + wy::kA1 + 16384 + 8192, 8192u);
+        gdn::bulk_s2g(out + blob::kP1, sm + wy::kStP1, 8192u);
+        gdn::bulk_s2g(out + blob::kP2, sm + wy::kStP2, 8192u);
+        gdn::bulk_commit();
+    }
     if (ok) {
         // (dec o K)^T parts for the scan's state update: the K^T tile already
         // has the scan's layout, so 16-byte piece e of the tile (row j = e/8)
@@ -273,48 +303,35 @@ __global__ void __launch_bounds__(kThreads) gdn_chunk_wy_kernel(const PrefArgs a
             *reinterpret_cast<uint4 *>(out + blob::kK1 + e * 16) = hi;
             *reinterpret_cast<uint4 *>(out + blob::kK2 + e * 16) = lo;
         }
-        // (I + A)^{-1} by 16x16 blocks.  Diagonal blocks: column substitution.
-        float col[16];
-        const int blk = tid >> 4, cc = tid & 15;
-        if (tid < kC) {
+        // T = (I + A)^{-1} by forward substitution, column by column: T[t][j]
+        // = delta_tj - sum_{i<t} A[t][i] T[i][j].  Four threads own a column j
+        // (rows 4m + q, m = 0..15); when row t is final its owner broadcasts
+        // T[t][j] to the other three, and every thread adds A[r][t] T[t][j] to
+        // the running sums of its later rows r (A is 0 on and above the diagonal).
+        {
+            const int j = tid >> 2, q = tid & 3;
+            float p[16];
 #pragma unroll
-            for (int r = 0; r < 16; ++r) col[r] = (r == cc) ? 1.f : 0.f;
-            for (int r = cc + 1; r < 16; ++r) {
-                float acc = 0.f;
-                for (int m = cc; m < r; ++m) acc = fmaf(Af[(16 * blk + r) * (kC + 1) + 16 * blk + m], col[m], acc);
-                col[r] = -acc;
+            for (int m = 0; m < 16; ++m) p[m] = 0.f;
+#pragma unroll
+            for (int t = 0; t < kC; ++t) {
+                const int mt = t >> 2;
+                float v = t == j ? 1.f : (t > j ? -p[mt] : 0.f);  // meaningful in the owner's lane
+                v = __shfl_sync(0xffffffffu, v, (lane & ~3) | (t & 3));
+                if (q == (t & 3)) p[mt] = v;
+#pragma unroll
+                for (int m = mt; m < 16; ++m) p[m] = fmaf(Af[(4 * m + q) * (kC + 1) + t], v, p[m]);
             }
+            __syncthreads();  // every A entry is read before T overwrites it
+#pragma unroll
+            for (int m = 0; m < 16; ++m) Af[(4 * m + q) * (kC + 1) + j] = p[m];
         }
         __syncthreads();
-        if (tid < kC)
-            for (int r = cc + 1; r < 16; ++r) Af[(16 * blk + r) * (kC + 1) + 16 * blk + cc] = col[r];
-        __syncthreads();
-        // Off-diagonal blocks, one block row at a time:
-        //   T_{bi,bj} = -T_{bi,bi} sum_{bk=bj}^{bi-1} A_{bi,bk} T_{bk,bj}
-        for (int bi = 1; bi < 4; ++bi) {
-            for (int idx = tid; idx < bi * 256; idx += kThreads) {
-                const int bj = idx >> 8, r = (idx >> 4) & 15, cj = idx & 15;
-                float acc = 0.f;
-                for (int bk = bj; bk < bi; ++bk)
-                    for (int m = 0; m < 16; ++m)
-                        acc = fmaf(Af[(16 * bi + r) * (kC + 1) + 16 * bk + m], tri_T(Af, 16 * bk + m, 16 * bj + cj), acc);
-                Xs[idx] = acc;
-            }
-            __syncthreads();
-            for (int idx = tid; idx < bi * 256; idx += kThreads) {
-                const int bj = idx >> 8, r = (idx >> 4) & 15, cj = idx & 15;
-                float acc = 0.f;
-                for (int m = 0; m <= r; ++m)
-                    acc = fmaf(tri_T(Af, 16 * bi + r, 16 * bi + m), Xs[(bj << 8) + (m << 4) + cj], acc);
-                Af[(16 * bi + r) * (kC + 1) + 16 * bj + cj] = -acc;
-            }
-            __syncthreads();
-        }
         // AB rows t: T diag(beta e^G); rows 64 + t: T diag(beta); hi and lo parts.
         const int t = tid >> 2, i0 = (tid & 3) * 16;
         float tv[16];
 #pragma unroll
-        for (int x = 0; x < 16; ++x) tv[x] = tri_T(Af, t, i0 + x);
+        for (int x = 0; x < 16; ++x) tv[x] = Af[t * (kC + 1) + i0 + x];
         __syncthreads();  // every T entry is read before the tiles overwrite it
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
@@ -360,7 +377,7 @@ __global__ void __launch_bounds__(kThreads) gdn_chunk_wy_kernel(const PrefArgs a
         const int t = 32 * (q4 & 1) + lane;  // token row = accumulator lane (mod 64)
         const uint32_t lane_base = uint32_t(32 * q4) << 16;
         if (q4 < 2) {
-            // W row t -> its two bf16 parts in the scan's W tiles
+            // W row t -> its two bf16 parts, staged where [K^T; V^T] was
 #pragma unroll
             for (int part = 0; part < 4; ++part) {
                 const int col = 64 * hc + 16 * part;
@@ -371,13 +388,13 @@ __global__ void __launch_bounds__(kThreads) gdn_chunk_wy_kernel(const PrefArgs a
                     uint4 hi, lo;
                     split8(w16 + x, hi, lo);
                     const uint32_t off = tc::swz_off(64, t, col + x);
-                    *reinterpret_cast<uint4 *>(out + blob::kW1 + off) = hi;
-                    *reinterpret_cast<uint4 *>(out + blob::kW2 + off) = lo;
+                    *reinterpret_cast<uint4 *>(sm + wy::kStW1 + off) = hi;
+                    *reinterpret_cast<uint4 *>(sm + wy::kStW2 + off) = lo;
                 }
             }
         } else {
-            // Ut row t, fp32
-            float *Ut = reinterpret_cast<float *>(out + blob::kUt) + t * kD;
+            // Ut row t, fp32, staged where AB was
+            float *Ut = reinterpret_cast<float *>(sm + wy::kStUt);
 #pragma unroll
             for (int part = 0; part < 4; ++part) {
                 const int col = 64 * hc + 16 * part;
@@ -385,14 +402,26 @@ __global__ void __launch_bounds__(kThreads) gdn_chunk_wy_kernel(const PrefArgs a
                 tc::ld16(tm + lane_base + 128u + uint32_t(col), u16);
 #pragma unroll
                 for (int x = 0; x < 16; x += 4)
-                    *reinterpret_cast<float4 *>(Ut + col + x) = make_float4(u16[x], u16[x + 1], u16[x + 2], u16[x + 3]);
+                    *reinterpret_cast<float4 *>(Ut + ut_index(t, col + x)) =
+                        make_float4(u16[x], u16[x + 1], u16[x + 2], u16[x + 3]);
             }
         }
+        gdn::fence_proxy_async_smem();
     } else if (tid == 0) {
         gdn::set_status(a.status, GDN_DEV_TIMEOUT);
     }
     tc::fence_before();
     __syncthreads();
+    if (tid == 0) {
+        if (ok) {
+            gdn::bulk_s2g(out + blob::kW1, sm + wy::kStW1, 16384u);
+            gdn::bulk_s2g(out + blob::kW2, sm + wy::kStW2, 16384u);
+            gdn::bulk_s2g(out + blob::kUt, sm + wy::kStUt, 16384u);
+            gdn::bulk_s2g(out + blob::kUt + 16384, sm + wy::kStUt + 16384, 16384u);
+            gdn::bulk_commit();
+        }
+        gdn::bulk_wait_all();  // this CTA's stores are complete before its shared memory is released
+    }
     if (warp == 0) tc::tmem_dealloc(tm, wy::kTmemCols);
 }
 
@@ -516,7 +545,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_chunk_scan_kernel(const PrefA
         const float *Ut = reinterpret_cast<const float *>(ws_blob(a, chunk_slot(s0, c, seq), h) + blob::kUt);
         float ut[32];  // Ut[t][arow] for t in [32hc, 32hc+32), consumed after phase A
 #pragma unroll
-        for (int x = 0; x < 32; ++x) ut[x] = Ut[(32 * hc + x) * kD + arow];
+        for (int x = 0; x < 32; ++x) ut[x] = Ut[ut_index(32 * hc + x, arow)];
         // The chunk's tiles (fetched during the previous chunk); S parts are written.
         if (tid == 0) *flag = gdn::mbar_wait_bounded(bar_in, phase_in) ? 1 : 0;
         __syncthreads();
