@@ -41,7 +41,8 @@ struct PrefArgs {
     int64_t slot_stride;
     const int32_t *src_slot, *dst_slot;
     uint16_t *o;
-    float *ws;  // [slot][h_v][2][C][D]
+    float *ws;             // per (chunk slot, v-head) blobs, see namespace blob
+    const int32_t *order;  // sequences by decreasing length (written by gdn_seq_order_kernel)
     float q_scale;
     uint32_t *status;
 };
@@ -278,14 +279,6 @@ __global__ void __launch_bounds__(kThreads) gdn_chunk_wy_kernel(const PrefArgs a
         gdn::fence_proxy_async_smem();
     }
     __syncthreads();
-    if (ok && tid == 0) {
-        // Q tile (rows 64..127 of both A1 atoms) and the P parts.
-        gdn::bulk_s2g(out + blob::kQ, sm + wy::kA1 + 8192, 8192u);
-        gdn::bulk_s2g(out + blob::kQ + 8192, sm + wy::kA1 + 16384 + 8192, 8192u);
-        gdn::bulk_s2g(out + blob::kP1, sm + wy::kStP1, 8192u);
-        gdn::bulk_s2g(out + blob::kP2, sm + wy::kStP2, 8192u);
-        gdn::bulk_commit();
-    }
     if (ok) {
         // (dec o K)^T parts for the scan's state update: the K^T tile already
         // has the scan's layout, so 16-byte piece e of the tile (row j = e/8)
@@ -414,6 +407,11 @@ __global__ void __launch_bounds__(kThreads) gdn_chunk_wy_kernel(const PrefArgs a
     __syncthreads();
     if (tid == 0) {
         if (ok) {
+            // Q tile (rows 64..127 of both A1 atoms), P, W and Ut parts.
+            gdn::bulk_s2g(out + blob::kQ, sm + wy::kA1 + 8192, 8192u);
+            gdn::bulk_s2g(out + blob::kQ + 8192, sm + wy::kA1 + 16384 + 8192, 8192u);
+            gdn::bulk_s2g(out + blob::kP1, sm + wy::kStP1, 8192u);
+            gdn::bulk_s2g(out + blob::kP2, sm + wy::kStP2, 8192u);
             gdn::bulk_s2g(out + blob::kW1, sm + wy::kStW1, 16384u);
             gdn::bulk_s2g(out + blob::kW2, sm + wy::kStW2, 16384u);
             gdn::bulk_s2g(out + blob::kUt, sm + wy::kStUt, 16384u);
@@ -450,24 +448,32 @@ constexpr uint32_t kK1 = kTiles + blob::kK1, kK2 = kTiles + blob::kK2;
 constexpr uint32_t kU1 = kTiles + blob::kTiles, kU2 = kU1 + 16384;  // U^T parts 128 rows (d_v) x 64 (i)
 constexpr uint32_t kMisc = kU2 + 16384;   // e^G (two chunks' worth), mbarriers, tensor-memory base, flag
 constexpr size_t kSmem = kMisc + 1024 + 1024;
-constexpr uint32_t kTmemCols = 512;  // Uacc 0..63, Oi 64..127, Oa 128..191, dS 256..383
+constexpr uint32_t kTmemCols = 512;  // Uacc 0..63, dS 256..383, Oi/Oa two buffers
 }  // namespace sc
 
-// Fetch of chunk c's tiles (96 KB, six bulk copies) and e^G (256 B) into
-// e^G buffer c % 2, all on one mbarrier.  Called by warp 0.
-__device__ __forceinline__ void scan_prefetch(const PrefArgs &a, unsigned char *sm, uint64_t *bar, int s0, int seq,
-                                              int h, int c) {
-    const int lane = threadIdx.x & 31;
+// Fetches of chunk c's workspace blob, issued by one thread: part A (the W
+// and Q tiles, 48 KB) is needed by the chunk's first products and may land
+// once the previous chunk's first products are done; part B (P and dec o K,
+// 48 KB, and e^G into buffer c % 2) is needed from the second products on.
+__device__ __forceinline__ void scan_fetch_a(const PrefArgs &a, unsigned char *sm, uint64_t *bar, int s0, int seq,
+                                             int h, int c) {
     const unsigned char *src = ws_blob(a, chunk_slot(s0, c, seq), h);
-    if (lane == 0) gdn::mbar_arrive_expect_tx(bar, blob::kTiles + 256u);
-    __syncwarp();
-    if (lane < 6) gdn::bulk_g2s(sm + sc::kTiles + lane * 16384, src + lane * 16384, 16384u, bar);
-    if (lane == 6) gdn::bulk_g2s(sm + sc::kMisc + (c & 1) * 256, src + blob::kEG, 256u, bar);
+    gdn::fence_proxy_async_smem();
+    gdn::mbar_arrive_expect_tx(bar, 3u * 16384u);
+    for (int i = 0; i < 3; ++i) gdn::bulk_g2s(sm + sc::kTiles + i * 16384, src + i * 16384, 16384u, bar);
+}
+__device__ __forceinline__ void scan_fetch_b(const PrefArgs &a, unsigned char *sm, uint64_t *bar, int s0, int seq,
+                                             int h, int c) {
+    const unsigned char *src = ws_blob(a, chunk_slot(s0, c, seq), h);
+    gdn::fence_proxy_async_smem();
+    gdn::mbar_arrive_expect_tx(bar, 3u * 16384u + 256u);
+    for (int i = 3; i < 6; ++i) gdn::bulk_g2s(sm + sc::kTiles + i * 16384, src + i * 16384, 16384u, bar);
+    gdn::bulk_g2s(sm + sc::kMisc + (c & 1) * 256, src + blob::kEG, 256u, bar);
 }
 
 __global__ void __launch_bounds__(kThreads, 1) gdn_chunk_scan_kernel(const PrefArgs a) {
     const int h = blockIdx.x % a.h_v;
-    const int seq = blockIdx.x / a.h_v;
+    const int seq = a.order[blockIdx.x / a.h_v];  // longest sequences start first
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int s0 = a.cu[seq];
     const int s1 = a.cu[seq + 1];
@@ -486,15 +492,21 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_chunk_scan_kernel(const PrefA
     const uint32_t raw_u = gdn::smem_u32(smraw);
     unsigned char *sm = smraw + (((raw_u + 1023u) & ~1023u) - raw_u);
     const uint32_t sb = gdn::smem_u32(sm);
-    uint64_t *bar = reinterpret_cast<uint64_t *>(sm + sc::kMisc + 768);
-    uint64_t *bar_in = reinterpret_cast<uint64_t *>(sm + sc::kMisc + 784);
+    uint64_t *bar_u = reinterpret_cast<uint64_t *>(sm + sc::kMisc + 768);   // Uacc done
+    uint64_t *bar_ia = reinterpret_cast<uint64_t *>(sm + sc::kMisc + 784);  // W, Q tiles arrived
+    uint64_t *bar_b = reinterpret_cast<uint64_t *>(sm + sc::kMisc + 792);   // phase B done
+    uint64_t *bar_o = reinterpret_cast<uint64_t *>(sm + sc::kMisc + 800);   // Oi done
+    uint64_t *bar_ib = reinterpret_cast<uint64_t *>(sm + sc::kMisc + 808);  // P, dec o K, e^G arrived
     uint32_t *tbase = reinterpret_cast<uint32_t *>(sm + sc::kMisc + 776);
     int *flag = reinterpret_cast<int *>(sm + sc::kMisc + 780);
 
     if (warp == 0) tc::tmem_alloc(tbase, sc::kTmemCols);
     if (tid == 0) {
-        gdn::mbar_init(bar, 1);
-        gdn::mbar_init(bar_in, 1);
+        gdn::mbar_init(bar_u, 1);
+        gdn::mbar_init(bar_ia, 1);
+        gdn::mbar_init(bar_b, 1);
+        gdn::mbar_init(bar_o, 1);
+        gdn::mbar_init(bar_ib, 1);
     }
 
     const int q4 = warp & 3, hc = warp >> 2;
@@ -534,55 +546,77 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_chunk_scan_kernel(const PrefA
     const uint32_t tm = *tbase;
     constexpr uint32_t id64 = tc::idesc_bf16(128, 64);
     constexpr uint32_t id128 = tc::idesc_bf16(128, 128);
-
-    uint32_t phase = 0, phase_in = 0;
-    bool ok = true;
-    const int nchunks = (len + kC - 1) / kC;
-    if (nchunks > 0 && warp == 0) scan_prefetch(a, sm, bar_in, s0, seq, h, 0);
-    for (int c = 0; c < nchunks; ++c) {
-        const int t0 = s0 + c * kC;
-        const int n = min(kC, len - c * kC);
+    // Tensor-memory columns: Uacc 0..63, dS 256..383, and Oi / Oa of chunk c
+    // in buffer c % 2 (the outputs of chunk c are read while chunk c + 1's
+    // first products run).
+    auto oi_col = [](int b) { return uint32_t(64 + 128 * b); };
+    auto oa_col = [](int b) { return uint32_t(128 + 256 * b); };
+    // Phase A of chunk c (thread 0): Uacc = S W^T, committed to bar_u, then
+    // Oi = S Q^T (finished before phase B's commit fires).
+    auto issue_phase_a = [&](int c) {
+        tc::fence_after();
+#pragma unroll
+        for (int at = 0; at < 2; ++at)
+#pragma unroll
+            for (int s = 0; s < 4; ++s) {
+                const uint32_t ka = at * 16384 + s * 32, kb = at * 8192 + s * 32;
+                const uint64_t a1 = tc::smem_desc(sb + sc::kS1 + ka), a2 = tc::smem_desc(sb + sc::kS2 + ka);
+                const uint64_t w1 = tc::smem_desc(sb + sc::kW1 + kb), w2 = tc::smem_desc(sb + sc::kW2 + kb);
+                tc::mma_bf16(tm, a1, w1, id64, (at | s) ? 1u : 0u);
+                tc::mma_bf16(tm, a1, w2, id64, 1u);
+                tc::mma_bf16(tm, a2, w1, id64, 1u);
+            }
+        tc::commit(bar_u);
+        const uint32_t oi = tm + oi_col(c & 1);
+#pragma unroll
+        for (int at = 0; at < 2; ++at)
+#pragma unroll
+            for (int s = 0; s < 4; ++s) {
+                const uint32_t ka = at * 16384 + s * 32, kb = at * 8192 + s * 32;
+                const uint64_t a1 = tc::smem_desc(sb + sc::kS1 + ka), a2 = tc::smem_desc(sb + sc::kS2 + ka);
+                const uint64_t qd = tc::smem_desc(sb + sc::kQ + kb);
+                tc::mma_bf16(oi, a1, qd, id64, (at | s) ? 1u : 0u);
+                tc::mma_bf16(oi, a2, qd, id64, 1u);
+            }
+        tc::commit(bar_o);
+    };
+    // Per-thread Ut values of chunk c: Ut[t][arow] for t in [32hc, 32hc+32).
+    float ut[32];
+    auto load_ut = [&](int c) {
         const float *Ut = reinterpret_cast<const float *>(ws_blob(a, chunk_slot(s0, c, seq), h) + blob::kUt);
-        float ut[32];  // Ut[t][arow] for t in [32hc, 32hc+32), consumed after phase A
 #pragma unroll
         for (int x = 0; x < 32; ++x) ut[x] = Ut[ut_index(32 * hc + x, arow)];
-        // The chunk's tiles (fetched during the previous chunk); S parts are written.
-        if (tid == 0) *flag = gdn::mbar_wait_bounded(bar_in, phase_in) ? 1 : 0;
-        __syncthreads();
-        if (*flag == 0) {
-            ok = false;
-            break;
-        }
-        (void)gdn::mbar_try_wait(bar_in, phase_in);
-        phase_in ^= 1u;
-        const float *eG = reinterpret_cast<const float *>(sm + sc::kMisc + (c & 1) * 256);
-        // Phase A: Uacc = S W^T, Oi = S Q^T.
+    };
+
+    uint32_t par_u = 0, par_b = 0, par_o = 0, par_ia = 0, par_ib = 0;
+    bool ok = true;
+    const int nchunks = (len + kC - 1) / kC;
+    if (nchunks > 0) {
+        load_ut(0);
         if (tid == 0) {
-            tc::fence_after();
-#pragma unroll
-            for (int at = 0; at < 2; ++at)
-#pragma unroll
-                for (int s = 0; s < 4; ++s) {
-                    const uint32_t ka = at * 16384 + s * 32, kb = at * 8192 + s * 32;
-                    const uint64_t a1 = tc::smem_desc(sb + sc::kS1 + ka), a2 = tc::smem_desc(sb + sc::kS2 + ka);
-                    const uint64_t w1 = tc::smem_desc(sb + sc::kW1 + kb), w2 = tc::smem_desc(sb + sc::kW2 + kb);
-                    const uint64_t qd = tc::smem_desc(sb + sc::kQ + kb);
-                    tc::mma_bf16(tm, a1, w1, id64, (at | s) ? 1u : 0u);
-                    tc::mma_bf16(tm, a1, w2, id64, 1u);
-                    tc::mma_bf16(tm, a2, w1, id64, 1u);
-                    tc::mma_bf16(tm + 64, a1, qd, id64, (at | s) ? 1u : 0u);
-                    tc::mma_bf16(tm + 64, a2, qd, id64, 1u);
-                }
-            tc::commit(bar);
-            *flag = gdn::mbar_wait_bounded(bar, phase) ? 1 : 0;
+            scan_fetch_a(a, sm, bar_ia, s0, seq, h, 0);
+            scan_fetch_b(a, sm, bar_ib, s0, seq, h, 0);
+            const bool got = gdn::mbar_wait_bounded(bar_ia, par_ia);
+            *flag = got ? 1 : 0;
+            if (got) issue_phase_a(0);
         }
+        par_ia ^= 1u;
+        __syncthreads();
+        ok = *flag != 0;
+    }
+    for (int c = 0; ok && c < nchunks; ++c) {
+        const int t0 = s0 + c * kC;
+        const int n = min(kC, len - c * kC);
+        const bool more = c + 1 < nchunks;
+        const float *eG = reinterpret_cast<const float *>(sm + sc::kMisc + (c & 1) * 256);
+        // Uacc of this chunk.
+        if (tid == 0) *flag = gdn::mbar_wait_bounded(bar_u, par_u) ? 1 : 0;
+        par_u ^= 1u;
         __syncthreads();
         if (*flag == 0) {
             ok = false;
             break;
         }
-        (void)gdn::mbar_try_wait(bar, phase);
-        phase ^= 1u;
         tc::fence_after();
         // U^T[arow][t] = Ut[t][arow] - Uacc[arow][t], split into two bf16 parts.
 #pragma unroll
@@ -605,50 +639,44 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_chunk_scan_kernel(const PrefA
         gdn::fence_proxy_async_smem();
         tc::fence_before();
         __syncthreads();
-        // Phase B: Oa = U^T P^T, dS = U^T (dec o K).
+        // Phase B: Oa = U^T P^T, dS = U^T (dec o K), once this chunk's P and
+        // dec o K have arrived; meanwhile the next chunk's W and Q are fetched
+        // as soon as this chunk's Oi is done with W and Q.
         if (tid == 0) {
-            tc::fence_after();
+            bool good = gdn::mbar_wait_bounded(bar_ib, par_ib);
+            if (good) {
+                tc::fence_after();
+                const uint32_t oa = tm + oa_col(c & 1);
 #pragma unroll
-            for (int s = 0; s < 4; ++s) {
-                const uint64_t u1 = tc::smem_desc(sb + sc::kU1 + s * 32), u2 = tc::smem_desc(sb + sc::kU2 + s * 32);
-                const uint64_t p1 = tc::smem_desc(sb + sc::kP1 + s * 32), p2 = tc::smem_desc(sb + sc::kP2 + s * 32);
-                const uint64_t k1 = tc::smem_desc(sb + sc::kK1 + s * 32), k2 = tc::smem_desc(sb + sc::kK2 + s * 32);
-                tc::mma_bf16(tm + 128, u1, p1, id64, s ? 1u : 0u);
-                tc::mma_bf16(tm + 128, u1, p2, id64, 1u);
-                tc::mma_bf16(tm + 128, u2, p1, id64, 1u);
-                tc::mma_bf16(tm + 256, u1, k1, id128, s ? 1u : 0u);
-                tc::mma_bf16(tm + 256, u1, k2, id128, 1u);
-                tc::mma_bf16(tm + 256, u2, k1, id128, 1u);
+                for (int s = 0; s < 4; ++s) {
+                    const uint64_t u1 = tc::smem_desc(sb + sc::kU1 + s * 32), u2 = tc::smem_desc(sb + sc::kU2 + s * 32);
+                    const uint64_t p1 = tc::smem_desc(sb + sc::kP1 + s * 32), p2 = tc::smem_desc(sb + sc::kP2 + s * 32);
+                    const uint64_t k1 = tc::smem_desc(sb + sc::kK1 + s * 32), k2 = tc::smem_desc(sb + sc::kK2 + s * 32);
+                    tc::mma_bf16(oa, u1, p1, id64, s ? 1u : 0u);
+                    tc::mma_bf16(oa, u1, p2, id64, 1u);
+                    tc::mma_bf16(oa, u2, p1, id64, 1u);
+                    tc::mma_bf16(tm + 256, u1, k1, id128, s ? 1u : 0u);
+                    tc::mma_bf16(tm + 256, u1, k2, id128, 1u);
+                    tc::mma_bf16(tm + 256, u2, k1, id128, 1u);
+                }
+                tc::commit(bar_b);
             }
-            tc::commit(bar);
-            *flag = gdn::mbar_wait_bounded(bar, phase) ? 1 : 0;
+            good = good && gdn::mbar_wait_bounded(bar_o, par_o);
+            if (good && more) scan_fetch_a(a, sm, bar_ia, s0, seq, h, c + 1);
+            good = good && gdn::mbar_wait_bounded(bar_b, par_b);
+            *flag = good ? 1 : 0;
         }
+        par_ib ^= 1u;
+        par_o ^= 1u;
+        par_b ^= 1u;
         __syncthreads();
         if (*flag == 0) {
             ok = false;
             break;
         }
-        (void)gdn::mbar_try_wait(bar, phase);
-        phase ^= 1u;
         tc::fence_after();
-        // Every tile is free now: fetch the next chunk's while the outputs and
-        // the state update below run.
-        if (c + 1 < nchunks && warp == 0) scan_prefetch(a, sm, bar_in, s0, seq, h, c + 1);
-        // Outputs of the chunk's tokens.
-#pragma unroll
-        for (int part = 0; part < 2; ++part) {
-            float oi[16], oa[16];
-            const int col0 = 32 * hc + 16 * part;
-            tc::ld16(tm + lane_base + 64u + uint32_t(col0), oi);
-            tc::ld16(tm + lane_base + 128u + uint32_t(col0), oa);
-#pragma unroll
-            for (int x = 0; x < 16; ++x) {
-                const int t = col0 + x;
-                if (t < n)
-                    a.o[(size_t(t0 + t) * a.h_v + h) * kD + arow] =
-                        gdn::f32_to_bf16(a.q_scale * fmaf(eG[t], oi[x], oa[x]));
-            }
-        }
+        // Every product of this chunk is done: P and dec o K are free for the next chunk's.
+        if (more && tid == 0) scan_fetch_b(a, sm, bar_ib, s0, seq, h, c + 1);
         // S <- e^{G_last} S + dS (FP32 master), then its bf16 parts.
         const float egl = eG[n - 1];
 #pragma unroll
@@ -659,7 +687,33 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_chunk_scan_kernel(const PrefA
             for (int x = 0; x < 16; ++x) sv[16 * part + x] = fmaf(egl, sv[16 * part + x], v16[x]);
         }
         write_S();
-        // (the barrier after the next chunk's tile wait orders these stores before its MMAs)
+        if (more) {
+            load_ut(c + 1);
+            if (tid == 0) *flag = gdn::mbar_wait_bounded(bar_ia, par_ia) ? 1 : 0;
+            par_ia ^= 1u;
+            __syncthreads();  // the S parts are written and the next chunk's W and Q have arrived
+            if (*flag == 0) {
+                ok = false;
+                break;
+            }
+            if (tid == 0) issue_phase_a(c + 1);
+        }
+        // Outputs of this chunk's tokens, while the next chunk's first products run.
+#pragma unroll
+        for (int part = 0; part < 2; ++part) {
+            float oi[16], oa[16];
+            const int col0 = 32 * hc + 16 * part;
+            tc::ld16(tm + lane_base + oi_col(c & 1) + uint32_t(col0), oi);
+            tc::ld16(tm + lane_base + oa_col(c & 1) + uint32_t(col0), oa);
+#pragma unroll
+            for (int x = 0; x < 16; ++x) {
+                const int t = col0 + x;
+                if (t < n)
+                    a.o[(size_t(t0 + t) * a.h_v + h) * kD + arow] =
+                        gdn::f32_to_bf16(a.q_scale * fmaf(eG[t], oi[x], oa[x]));
+            }
+        }
+        tc::fence_before();
     }
     if (ok) {
         float4 *dp = reinterpret_cast<float4 *>(a.pool + size_t(dst) * a.slot_stride + row_off);
@@ -673,15 +727,33 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_chunk_scan_kernel(const PrefA
     if (warp == 0) tc::tmem_dealloc(tm, sc::kTmemCols);
 }
 
+// order[r] = the sequence with the r-th largest length (ties by index), so
+// that the scan's longest dependency chains are scheduled in its first wave.
+__global__ void gdn_seq_order_kernel(const int32_t *cu, int nseq, int32_t *order) {
+    for (int i = threadIdx.x; i < nseq; i += blockDim.x) {
+        const int li = cu[i + 1] - cu[i];
+        int r = 0;
+        for (int j = 0; j < nseq; ++j) {
+            const int lj = cu[j + 1] - cu[j];
+            r += (lj > li || (lj == li && j < i)) ? 1 : 0;
+        }
+        order[r] = i;
+    }
+}
+
 constexpr size_t kWySmem = wy::kSmem;
 constexpr size_t kScanSmem = sc::kSmem;
 
 }  // namespace
 
-extern "C" size_t gdn_prefill_workspace_bytes(const gdn_dims *dims, int32_t nseq, int32_t row_capacity) {
-    if (!dims || nseq < 0 || row_capacity < 0) return 0;
+static size_t blobs_bytes(const gdn_dims *dims, int32_t nseq, int32_t row_capacity) {
     const size_t slots = size_t((row_capacity + kC - 1) / kC) + size_t(nseq);
     return slots * size_t(dims->h_v) * kWsFloats * sizeof(float);
+}
+
+extern "C" size_t gdn_prefill_workspace_bytes(const gdn_dims *dims, int32_t nseq, int32_t row_capacity) {
+    if (!dims || nseq < 0 || row_capacity < 0) return 0;
+    return blobs_bytes(dims, nseq, row_capacity) + (size_t(nseq) * 4 + 15) / 16 * 16;
 }
 
 extern "C" int gdn_chunked_prefill(const gdn_dims *dims, int32_t nseq, int32_t row_capacity,
@@ -727,6 +799,9 @@ extern "C" int gdn_chunked_prefill(const gdn_dims *dims, int32_t nseq, int32_t r
     a.dst_slot = dst_slot;
     a.o = o;
     a.ws = static_cast<float *>(workspace);
+    int32_t *order = reinterpret_cast<int32_t *>(static_cast<unsigned char *>(workspace) +
+                                                 blobs_bytes(dims, nseq, row_capacity));
+    a.order = order;
     a.q_scale = dims->q_scale;
     a.status = dev_status;
     if (cudaFuncSetAttribute(gdn_chunk_wy_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kWySmem)) !=
@@ -734,6 +809,8 @@ extern "C" int gdn_chunked_prefill(const gdn_dims *dims, int32_t nseq, int32_t r
         cudaFuncSetAttribute(gdn_chunk_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kScanSmem)) !=
             cudaSuccess)
         return GDN_ERR_CUDA;
+    gdn_seq_order_kernel<<<1, nseq < 1024 ? (nseq + 31) / 32 * 32 : 1024, 0, st>>>(cu_seqlens, nseq, order);
+    if (cudaGetLastError() != cudaSuccess) return GDN_ERR_CUDA;
     if (a.max_chunks > 0) {
         const long long gx = (long long)nseq * a.max_chunks;
         if (gx > 0x7fffffffLL || dims->h_v > 65535) return GDN_ERR_ARG;
