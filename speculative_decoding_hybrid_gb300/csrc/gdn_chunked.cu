@@ -28,7 +28,8 @@ namespace {
 
 constexpr int kC = 64;         // chunk length
 constexpr int kD = 128;        // d_k = d_v supported by this kernel pair
-constexpr int kThreads = 256;
+constexpr int kThreads = 256;       // per-chunk kernel
+constexpr int kScanThreads = 512;   // scan: 4 warps per tensor-memory lane quadrant
 
 __device__ __forceinline__ int chunk_slot(int seq_start, int c, int seq) { return (seq_start + kC * c) / kC + seq; }
 
@@ -86,16 +87,20 @@ __device__ __forceinline__ unsigned char *ws_blob(const PrefArgs &a, int slot, i
     return reinterpret_cast<unsigned char *>(a.ws) + (size_t(slot) * a.h_v + h) * blob::kBytes;
 }
 
+// x0 and x1 rounded to nearest-even bf16, packed with x0 in the low half.
+__device__ __forceinline__ uint32_t pack_bf16x2(float x0, float x1) {
+    uint32_t d;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(x1), "f"(x0));
+    return d;
+}
+
 // Two-term bf16 split of 8 consecutive values, packed as two 16-byte chunks.
 __device__ __forceinline__ void split8(const float *x, uint4 &hi, uint4 &lo) {
     uint32_t h[4], l[4];
 #pragma unroll
     for (int p = 0; p < 4; ++p) {
-        const uint16_t h0 = gdn::f32_to_bf16(x[2 * p]), h1 = gdn::f32_to_bf16(x[2 * p + 1]);
-        const uint16_t l0 = gdn::f32_to_bf16(x[2 * p] - gdn::bf16_to_f32(h0));
-        const uint16_t l1 = gdn::f32_to_bf16(x[2 * p + 1] - gdn::bf16_to_f32(h1));
-        h[p] = uint32_t(h0) | (uint32_t(h1) << 16);
-        l[p] = uint32_t(l0) | (uint32_t(l1) << 16);
+        h[p] = pack_bf16x2(x[2 * p], x[2 * p + 1]);
+        l[p] = pack_bf16x2(x[2 * p] - __uint_as_float(h[p] << 16), x[2 * p + 1] - __uint_as_float(h[p] & 0xffff0000u));
     }
     hi = make_uint4(h[0], h[1], h[2], h[3]);
     lo = make_uint4(l[0], l[1], l[2], l[3]);
@@ -428,7 +433,7 @@ __global__ void __launch_bounds__(kThreads) gdn_chunk_wy_kernel(const PrefArgs a
 // ---------------------------------------------------------------------------
 // One CTA per (sequence, v-head); the 128 value rows of S are the M = 128
 // side of every product, so each thread owns one row of S (lane quadrant of
-// its warp) and half of its columns.  The FP32 master copy of S stays in
+// its warp) and a quarter of its columns (16 warps).  The FP32 master copy of S stays in
 // registers for the whole sequence.  S and U are split into two bf16 parts
 // here; W, P and dec o K arrive split from the per-chunk kernel; a product
 // keeps the three leading terms a1 b1 + a1 b2 + a2 b1; q and k are exact
@@ -471,7 +476,7 @@ __device__ __forceinline__ void scan_fetch_b(const PrefArgs &a, unsigned char *s
     gdn::bulk_g2s(sm + sc::kMisc + (c & 1) * 256, src + blob::kEG, 256u, bar);
 }
 
-__global__ void __launch_bounds__(kThreads, 1) gdn_chunk_scan_kernel(const PrefArgs a) {
+__global__ void __launch_bounds__(kScanThreads, 1) gdn_chunk_scan_kernel(const PrefArgs a) {
     const int h = blockIdx.x % a.h_v;
     const int seq = a.order[blockIdx.x / a.h_v];  // longest sequences start first
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -509,15 +514,15 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_chunk_scan_kernel(const PrefA
         gdn::mbar_init(bar_ib, 1);
     }
 
-    const int q4 = warp & 3, hc = warp >> 2;
-    const int arow = 32 * q4 + lane;  // row of S held by this thread
+    const int q4 = warp & 3, cq = warp >> 2;  // lane quadrant, column quarter
+    const int arow = 32 * q4 + lane;          // row of S held by this thread
     const uint32_t lane_base = uint32_t(32 * q4) << 16;
-    const size_t row_off = size_t(h) * kD * kD + size_t(arow) * kD + 64 * hc;
-    float sv[64];  // S[arow][64hc .. 64hc+63], FP32 master
+    const size_t row_off = size_t(h) * kD * kD + size_t(arow) * kD + 32 * cq;
+    float sv[32];  // S[arow][32cq .. 32cq+31], FP32 master
     if (src >= 0) {
         const float4 *sp = reinterpret_cast<const float4 *>(a.pool + size_t(src) * a.slot_stride + row_off);
 #pragma unroll
-        for (int x = 0; x < 16; ++x) {
+        for (int x = 0; x < 8; ++x) {
             const float4 v = sp[x];
             sv[4 * x] = v.x;
             sv[4 * x + 1] = v.y;
@@ -526,14 +531,14 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_chunk_scan_kernel(const PrefA
         }
     } else {
 #pragma unroll
-        for (int x = 0; x < 64; ++x) sv[x] = 0.f;
+        for (int x = 0; x < 32; ++x) sv[x] = 0.f;
     }
     auto write_S = [&]() {
 #pragma unroll
-        for (int x = 0; x < 8; ++x) {
+        for (int x = 0; x < 4; ++x) {
             uint4 hi, lo;
             split8(sv + 8 * x, hi, lo);
-            const uint32_t off = tc::swz_off(128, arow, 64 * hc + 8 * x);
+            const uint32_t off = tc::swz_off(128, arow, 32 * cq + 8 * x);
             *reinterpret_cast<uint4 *>(sm + sc::kS1 + off) = hi;
             *reinterpret_cast<uint4 *>(sm + sc::kS2 + off) = lo;
         }
@@ -549,6 +554,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_chunk_scan_kernel(const PrefA
     // Tensor-memory columns: Uacc 0..63, dS 256..383, and Oi / Oa of chunk c
     // in buffer c % 2 (the outputs of chunk c are read while chunk c + 1's
     // first products run).
+    const uint64_t dsc = tc::smem_desc(sb);  // descriptors of the fixed tiles: tc::desc_at(dsc, offset)
     auto oi_col = [](int b) { return uint32_t(64 + 128 * b); };
     auto oa_col = [](int b) { return uint32_t(128 + 256 * b); };
     // Phase A of chunk c (thread 0): Uacc = S W^T, committed to bar_u, then
@@ -560,8 +566,8 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_chunk_scan_kernel(const PrefA
 #pragma unroll
             for (int s = 0; s < 4; ++s) {
                 const uint32_t ka = at * 16384 + s * 32, kb = at * 8192 + s * 32;
-                const uint64_t a1 = tc::smem_desc(sb + sc::kS1 + ka), a2 = tc::smem_desc(sb + sc::kS2 + ka);
-                const uint64_t w1 = tc::smem_desc(sb + sc::kW1 + kb), w2 = tc::smem_desc(sb + sc::kW2 + kb);
+                const uint64_t a1 = tc::desc_at(dsc, sc::kS1 + ka), a2 = tc::desc_at(dsc, sc::kS2 + ka);
+                const uint64_t w1 = tc::desc_at(dsc, sc::kW1 + kb), w2 = tc::desc_at(dsc, sc::kW2 + kb);
                 tc::mma_bf16(tm, a1, w1, id64, (at | s) ? 1u : 0u);
                 tc::mma_bf16(tm, a1, w2, id64, 1u);
                 tc::mma_bf16(tm, a2, w1, id64, 1u);
@@ -573,19 +579,19 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_chunk_scan_kernel(const PrefA
 #pragma unroll
             for (int s = 0; s < 4; ++s) {
                 const uint32_t ka = at * 16384 + s * 32, kb = at * 8192 + s * 32;
-                const uint64_t a1 = tc::smem_desc(sb + sc::kS1 + ka), a2 = tc::smem_desc(sb + sc::kS2 + ka);
-                const uint64_t qd = tc::smem_desc(sb + sc::kQ + kb);
+                const uint64_t a1 = tc::desc_at(dsc, sc::kS1 + ka), a2 = tc::desc_at(dsc, sc::kS2 + ka);
+                const uint64_t qd = tc::desc_at(dsc, sc::kQ + kb);
                 tc::mma_bf16(oi, a1, qd, id64, (at | s) ? 1u : 0u);
                 tc::mma_bf16(oi, a2, qd, id64, 1u);
             }
         tc::commit(bar_o);
     };
-    // Per-thread Ut values of chunk c: Ut[t][arow] for t in [32hc, 32hc+32).
-    float ut[32];
+    // Per-thread Ut values of chunk c: Ut[t][arow] for t in [16cq, 16cq+16).
+    float ut[16];
     auto load_ut = [&](int c) {
         const float *Ut = reinterpret_cast<const float *>(ws_blob(a, chunk_slot(s0, c, seq), h) + blob::kUt);
 #pragma unroll
-        for (int x = 0; x < 32; ++x) ut[x] = Ut[ut_index(32 * hc + x, arow)];
+        for (int x = 0; x < 16; ++x) ut[x] = Ut[ut_index(16 * cq + x, arow)];
     };
 
     uint32_t par_u = 0, par_b = 0, par_o = 0, par_ia = 0, par_ib = 0;
@@ -619,16 +625,15 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_chunk_scan_kernel(const PrefA
         }
         tc::fence_after();
         // U^T[arow][t] = Ut[t][arow] - Uacc[arow][t], split into two bf16 parts.
-#pragma unroll
-        for (int part = 0; part < 2; ++part) {
+        {
             float v16[16];
-            const int col0 = 32 * hc + 16 * part;
+            const int col0 = 16 * cq;
             tc::ld16(tm + lane_base + uint32_t(col0), v16);
 #pragma unroll
             for (int x = 0; x < 16; x += 8) {
                 float u[8];
 #pragma unroll
-                for (int y = 0; y < 8; ++y) u[y] = ut[16 * part + x + y] - v16[x + y];
+                for (int y = 0; y < 8; ++y) u[y] = ut[x + y] - v16[x + y];
                 uint4 hi, lo;
                 split8(u, hi, lo);
                 const uint32_t off = tc::swz_off(128, arow, col0 + x);
@@ -649,9 +654,9 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_chunk_scan_kernel(const PrefA
                 const uint32_t oa = tm + oa_col(c & 1);
 #pragma unroll
                 for (int s = 0; s < 4; ++s) {
-                    const uint64_t u1 = tc::smem_desc(sb + sc::kU1 + s * 32), u2 = tc::smem_desc(sb + sc::kU2 + s * 32);
-                    const uint64_t p1 = tc::smem_desc(sb + sc::kP1 + s * 32), p2 = tc::smem_desc(sb + sc::kP2 + s * 32);
-                    const uint64_t k1 = tc::smem_desc(sb + sc::kK1 + s * 32), k2 = tc::smem_desc(sb + sc::kK2 + s * 32);
+                    const uint64_t u1 = tc::desc_at(dsc, sc::kU1 + s * 32), u2 = tc::desc_at(dsc, sc::kU2 + s * 32);
+                    const uint64_t p1 = tc::desc_at(dsc, sc::kP1 + s * 32), p2 = tc::desc_at(dsc, sc::kP2 + s * 32);
+                    const uint64_t k1 = tc::desc_at(dsc, sc::kK1 + s * 32), k2 = tc::desc_at(dsc, sc::kK2 + s * 32);
                     tc::mma_bf16(oa, u1, p1, id64, s ? 1u : 0u);
                     tc::mma_bf16(oa, u1, p2, id64, 1u);
                     tc::mma_bf16(oa, u2, p1, id64, 1u);
@@ -680,9 +685,9 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_chunk_scan_kernel(const PrefA
         // S <- e^{G_last} S + dS (FP32 master), then its bf16 parts.
         const float egl = eG[n - 1];
 #pragma unroll
-        for (int part = 0; part < 4; ++part) {
+        for (int part = 0; part < 2; ++part) {
             float v16[16];
-            tc::ld16(tm + lane_base + 256u + uint32_t(64 * hc + 16 * part), v16);
+            tc::ld16(tm + lane_base + 256u + uint32_t(32 * cq + 16 * part), v16);
 #pragma unroll
             for (int x = 0; x < 16; ++x) sv[16 * part + x] = fmaf(egl, sv[16 * part + x], v16[x]);
         }
@@ -699,10 +704,9 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_chunk_scan_kernel(const PrefA
             if (tid == 0) issue_phase_a(c + 1);
         }
         // Outputs of this chunk's tokens, while the next chunk's first products run.
-#pragma unroll
-        for (int part = 0; part < 2; ++part) {
+        {
             float oi[16], oa[16];
-            const int col0 = 32 * hc + 16 * part;
+            const int col0 = 16 * cq;
             tc::ld16(tm + lane_base + oi_col(c & 1) + uint32_t(col0), oi);
             tc::ld16(tm + lane_base + oa_col(c & 1) + uint32_t(col0), oa);
 #pragma unroll
@@ -718,7 +722,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_chunk_scan_kernel(const PrefA
     if (ok) {
         float4 *dp = reinterpret_cast<float4 *>(a.pool + size_t(dst) * a.slot_stride + row_off);
 #pragma unroll
-        for (int x = 0; x < 16; ++x) dp[x] = make_float4(sv[4 * x], sv[4 * x + 1], sv[4 * x + 2], sv[4 * x + 3]);
+        for (int x = 0; x < 8; ++x) dp[x] = make_float4(sv[4 * x], sv[4 * x + 1], sv[4 * x + 2], sv[4 * x + 3]);
     } else if (tid == 0) {
         gdn::set_status(a.status, GDN_DEV_TIMEOUT);
     }
@@ -818,6 +822,6 @@ extern "C" int gdn_chunked_prefill(const gdn_dims *dims, int32_t nseq, int32_t r
         if (cudaGetLastError() != cudaSuccess) return GDN_ERR_CUDA;
     }
     const long long gs = (long long)nseq * dims->h_v;
-    gdn_chunk_scan_kernel<<<unsigned(gs), kThreads, kScanSmem, st>>>(a);
+    gdn_chunk_scan_kernel<<<unsigned(gs), kScanThreads, kScanSmem, st>>>(a);
     return gdn_host::launch_status(cudaGetLastError());
 }

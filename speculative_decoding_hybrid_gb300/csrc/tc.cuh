@@ -55,6 +55,11 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr) {
     return d;
 }
 
+// Descriptor of the tile `off` bytes after the one `base` describes (off a
+// multiple of 16, the start address staying below 256 KB): only the start
+// field changes.
+__device__ __forceinline__ uint64_t desc_at(uint64_t base, uint32_t off) { return base + (off >> 4); }
+
 // Instruction descriptor for kind::f16 with bf16 A/B, fp32 D, both K-major.
 __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
     return (1u << 4)                       // D format: f32
