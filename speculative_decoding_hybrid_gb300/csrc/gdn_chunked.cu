@@ -57,7 +57,7 @@ namespace blob {
 constexpr uint32_t kW1 = 0, kW2 = 16384;     // W = T diag(beta e^G) K parts: 64 rows (t) x 128 (d_k)
 constexpr uint32_t kQ = 32768;               // Q (exact bf16):               64 rows (t) x 128 (d_k)
 constexpr uint32_t kP1 = 49152, kP2 = 57344; // P = M o Q K^T parts:         64 rows (t) x  64 (i)
-constexpr uint32_t kK1 = 65536, kK2 = 81920; // (dec o K)^T parts:          128 rows (d_k) x 64 (i)
+constexpr uint32_t kK1 = 65536, kK2 = 81920; // dec o K parts, MN-major B:  64 rows (i) x 128 (d_k)
 constexpr uint32_t kTiles = 98304;           // bytes of operand tiles (one contiguous block)
 constexpr uint32_t kUt = 98304;              // Ut = T diag(beta) V, fp32 [t][d_v] (pieces permuted, ut_index)
 constexpr uint32_t kEG = 131072;             // e^{G_t}, fp32 x 64
@@ -109,28 +109,35 @@ __device__ __forceinline__ void split8(const float *x, uint4 &hi, uint4 &lo) {
 // ---------------------------------------------------------------------------
 // (1) per-chunk WY/UT quantities on the tensor cores (tcgen05, kind::f16)
 // ---------------------------------------------------------------------------
-// Shared-memory map (bytes from a 1024-aligned base), bf16 K-major tiles:
-//   A1   [K; Q]          128 rows (tokens, then q rows) x 128 (d_k)   32 KB
-//   KV   [K^T; V^T]      256 rows (d_k, then d_v) x 64 (tokens)       32 KB
+// Shared-memory map (bytes from a 1024-aligned base), bf16 128-byte-swizzled tiles:
+//   A1   [K; Q]   128 rows (tokens, then q rows) x 128 (d_k), K-major   32 KB
+//   VN   V        64 rows (tokens) x 128 (d_v) in two 64-column atoms 16 KB
+//                 apart, right after A1: with the K rows of A1 this is
+//                 [K | V] as an MN-major B operand (N = 256, 64-element
+//                 blocks 16 KB apart), so no transposed copy is needed
 //   AB   [T diag(beta e^G); T diag(beta)], hi and lo parts,
-//                        128 rows (t, twice) x 64 (i)              2 x 16 KB
+//                 128 rows (t, twice) x 64 (i), K-major                2 x 16 KB
 //   (the fp32 matrix A -> T, [64][65], lives in the AB area before those
 //    tiles are written)
 //   misc G, beta, e^G, mbarrier, tensor-memory base, flag, dec
-// Outputs are staged in areas whose operands have been consumed and leave by
-// bulk copies: the Q tile is rows 64..127 of both A1 atoms as they stand; the
-// P parts replace rows 0..63 of the two A1 atoms after the first product; the
-// W parts replace [K^T; V^T] and Ut replaces AB after the second.
+// Outputs are staged and leave by bulk copies issued at the very end (stores
+// in flight hold back the tensor cores): the Q tile is rows 64..127 of both A1
+// atoms as they stand; the P parts go to the unused halves of the VN atoms;
+// after the second product the W parts replace VN and Ut replaces AB.
 // Tensor memory (256 columns): first D1 = [K;Q] K^T at columns 0..63 (rows
-// 0..63: K K^T, rows 64..127: Q K^T), then D2 = AB [K^T; V^T]^T at 0..255:
+// 0..63: K K^T, rows 64..127: Q K^T), then D2 = AB [K | V] at 0..255:
 // rows 0..63 x columns 0..127 hold W, rows 64..127 x columns 128..255 hold Ut
 // (the two cross blocks are not used).
 namespace wy {
-constexpr uint32_t kA1 = 0, kKT = 32768, kVT = 49152, kT = 65536, kMisc = 98304;
+constexpr uint32_t kA1 = 0, kVN = 32768, kT = 65536, kMisc = 98304;
 constexpr uint32_t kAbHi = kT, kAbLo = kT + 16384;
-constexpr uint32_t kStP1 = kA1, kStP2 = kA1 + 16384;  // 8 KB each
-constexpr uint32_t kStW1 = kKT, kStW2 = kVT;          // 16 KB each
-constexpr uint32_t kStUt = kT;                        // 32 KB
+// Staging (8 KB pieces): P parts in the unused row halves of the VN atoms;
+// the two 64-column atoms of W1 in the K rows of the A1 atoms and those of W2
+// in the V rows of the VN atoms (both consumed by the second product); Ut in AB.
+constexpr uint32_t kStP1 = kVN + 8192, kStP2 = kVN + 16384 + 8192;
+__device__ __forceinline__ uint32_t st_w1(int atom) { return kA1 + 16384u * uint32_t(atom); }
+__device__ __forceinline__ uint32_t st_w2(int atom) { return kVN + 16384u * uint32_t(atom); }
+constexpr uint32_t kStUt = kT;  // 32 KB
 constexpr size_t kSmem = kMisc + 2048 + 1024;  // + alignment slack
 constexpr uint32_t kTmemCols = 256;
 }  // namespace wy
@@ -172,10 +179,8 @@ __global__ void __launch_bounds__(kThreads) gdn_chunk_wy_kernel(const PrefArgs a
     if (warp == 0) tc::tmem_alloc(tbase, wy::kTmemCols);
     if (tid == 0) gdn::mbar_init(bar, 1);
 
-    // Stage K, Q (rows of A1), K^T and V^T as bf16 operand tiles; rows past n
-    // are zero.  Every load is issued before the first store.  A warp covers
-    // 32 consecutive tokens of one 8-column group, so the transposed stores of
-    // a warp land in one row of K^T / V^T (no bank conflicts).
+    // Stage K, Q (rows of A1) and V (rows of VN); rows past n are zero.
+    // Every load is issued before the first store.
     {
         uint4 kv[4], qv[4], vv[4];
 #pragma unroll
@@ -200,15 +205,7 @@ __global__ void __launch_bounds__(kThreads) gdn_chunk_wy_kernel(const PrefArgs a
             const int t = e % kC, c8 = (e / kC) * 8;
             *reinterpret_cast<uint4 *>(sm + wy::kA1 + tc::swz_off(128, t, c8)) = kv[it];
             *reinterpret_cast<uint4 *>(sm + wy::kA1 + tc::swz_off(128, kC + t, c8)) = qv[it];
-            const uint32_t kw[4] = {kv[it].x, kv[it].y, kv[it].z, kv[it].w};
-            const uint32_t vw[4] = {vv[it].x, vv[it].y, vv[it].z, vv[it].w};
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const uint16_t ke = uint16_t(i & 1 ? kw[i >> 1] >> 16 : kw[i >> 1] & 0xffffu);
-                const uint16_t ve = uint16_t(i & 1 ? vw[i >> 1] >> 16 : vw[i >> 1] & 0xffffu);
-                *reinterpret_cast<uint16_t *>(sm + wy::kKT + tc::swz_off(128, c8 + i, t)) = ke;
-                *reinterpret_cast<uint16_t *>(sm + wy::kVT + tc::swz_off(128, c8 + i, t)) = ve;
-            }
+            *reinterpret_cast<uint4 *>(sm + wy::kVN + tc::swz_off(128, t, c8)) = vv[it];
         }
         if (tid < kC) {
             Bs[tid] = bt;
@@ -285,17 +282,19 @@ __global__ void __launch_bounds__(kThreads) gdn_chunk_wy_kernel(const PrefArgs a
     }
     __syncthreads();
     if (ok) {
-        // (dec o K)^T parts for the scan's state update: the K^T tile already
-        // has the scan's layout, so 16-byte piece e of the tile (row j = e/8)
-        // is scaled by dec over its 8 tokens and stored at the same offset.
+        // dec o K parts for the scan's state update, an MN-major operand with
+        // the K rows' layout (64-column atoms 8 KB apart): 16-byte piece e of
+        // the output (atom e/512, token row i) is the same piece of A1's K row
+        // i, scaled by dec_i.
         for (int e = tid; e < kD * kC / 8; e += kThreads) {
-            const int j = e >> 3, i8 = ((e & 7) ^ (j & 7)) * 8;
-            const uint4 kr = *reinterpret_cast<const uint4 *>(sm + wy::kKT + e * 16);
+            const int atom = e >> 9, i = (e >> 3) & (kC - 1);
+            const uint4 kr = *reinterpret_cast<const uint4 *>(sm + wy::kA1 + atom * 16384 + (e & 511) * 16);
             const uint32_t kw[4] = {kr.x, kr.y, kr.z, kr.w};
+            const float di = dec[i];
             float kv[8];
 #pragma unroll
             for (int y = 0; y < 8; ++y)
-                kv[y] = gdn::bf16_to_f32(uint16_t(y & 1 ? kw[y >> 1] >> 16 : kw[y >> 1] & 0xffffu)) * dec[i8 + y];
+                kv[y] = gdn::bf16_to_f32(uint16_t(y & 1 ? kw[y >> 1] >> 16 : kw[y >> 1] & 0xffffu)) * di;
             uint4 hi, lo;
             split8(kv, hi, lo);
             *reinterpret_cast<uint4 *>(out + blob::kK1 + e * 16) = hi;
@@ -355,11 +354,13 @@ __global__ void __launch_bounds__(kThreads) gdn_chunk_wy_kernel(const PrefArgs a
     __syncthreads();
     if (ok && tid == 0) {
         tc::fence_after();
-        // D2 = AB [K^T; V^T]^T (M = 128, N = 256); hi and lo parts accumulate.
-        constexpr uint32_t idesc = tc::idesc_bf16(128, 256);
+        // D2 = AB [K | V] (M = 128, N = 256, B MN-major: four 64-column
+        // blocks 16 KB apart from A1's K rows to VN); hi and lo parts accumulate.
+        constexpr uint32_t idesc = tc::idesc_bf16(128, 256) | tc::kBMnMajor;
+        const uint64_t bkv = tc::smem_desc_mn(sb + wy::kA1, 16384);
 #pragma unroll
         for (int s = 0; s < 4; ++s) {
-            const uint64_t b = tc::smem_desc(sb + wy::kKT + s * 32);
+            const uint64_t b = tc::desc_at(bkv, s * 2048);
             tc::mma_bf16(tm, tc::smem_desc(sb + wy::kAbHi + s * 32), b, idesc, s ? 1u : 0u);
             tc::mma_bf16(tm, tc::smem_desc(sb + wy::kAbLo + s * 32), b, idesc, 1u);
         }
@@ -375,19 +376,19 @@ __global__ void __launch_bounds__(kThreads) gdn_chunk_wy_kernel(const PrefArgs a
         const int t = 32 * (q4 & 1) + lane;  // token row = accumulator lane (mod 64)
         const uint32_t lane_base = uint32_t(32 * q4) << 16;
         if (q4 < 2) {
-            // W row t -> its two bf16 parts, staged where [K^T; V^T] was
+            // W row t -> its two bf16 parts (columns 64hc.. in atom hc)
 #pragma unroll
             for (int part = 0; part < 4; ++part) {
-                const int col = 64 * hc + 16 * part;
+                const int col = 16 * part;
                 float w16[16];
-                tc::ld16(tm + lane_base + uint32_t(col), w16);
+                tc::ld16(tm + lane_base + uint32_t(64 * hc + col), w16);
 #pragma unroll
                 for (int x = 0; x < 16; x += 8) {
                     uint4 hi, lo;
                     split8(w16 + x, hi, lo);
                     const uint32_t off = tc::swz_off(64, t, col + x);
-                    *reinterpret_cast<uint4 *>(sm + wy::kStW1 + off) = hi;
-                    *reinterpret_cast<uint4 *>(sm + wy::kStW2 + off) = lo;
+                    *reinterpret_cast<uint4 *>(sm + wy::st_w1(hc) + off) = hi;
+                    *reinterpret_cast<uint4 *>(sm + wy::st_w2(hc) + off) = lo;
                 }
             }
         } else {
@@ -417,8 +418,10 @@ __global__ void __launch_bounds__(kThreads) gdn_chunk_wy_kernel(const PrefArgs a
             gdn::bulk_s2g(out + blob::kQ + 8192, sm + wy::kA1 + 16384 + 8192, 8192u);
             gdn::bulk_s2g(out + blob::kP1, sm + wy::kStP1, 8192u);
             gdn::bulk_s2g(out + blob::kP2, sm + wy::kStP2, 8192u);
-            gdn::bulk_s2g(out + blob::kW1, sm + wy::kStW1, 16384u);
-            gdn::bulk_s2g(out + blob::kW2, sm + wy::kStW2, 16384u);
+            for (int at = 0; at < 2; ++at) {
+                gdn::bulk_s2g(out + blob::kW1 + at * 8192, sm + wy::st_w1(at), 8192u);
+                gdn::bulk_s2g(out + blob::kW2 + at * 8192, sm + wy::st_w2(at), 8192u);
+            }
             gdn::bulk_s2g(out + blob::kUt, sm + wy::kStUt, 16384u);
             gdn::bulk_s2g(out + blob::kUt + 16384, sm + wy::kStUt + 16384, 16384u);
             gdn::bulk_commit();
@@ -555,6 +558,8 @@ __global__ void __launch_bounds__(kScanThreads, 1) gdn_chunk_scan_kernel(const P
     // in buffer c % 2 (the outputs of chunk c are read while chunk c + 1's
     // first products run).
     const uint64_t dsc = tc::smem_desc(sb);  // descriptors of the fixed tiles: tc::desc_at(dsc, offset)
+    const uint64_t dsc_k = tc::smem_desc_mn(sb + sc::kK1, 8192);  // dec o K parts, MN-major B (K2 at +16 KB)
+    constexpr uint32_t id128k = id128 | tc::kBMnMajor;
     auto oi_col = [](int b) { return uint32_t(64 + 128 * b); };
     auto oa_col = [](int b) { return uint32_t(128 + 256 * b); };
     // Phase A of chunk c (thread 0): Uacc = S W^T, committed to bar_u, then
@@ -656,13 +661,13 @@ __global__ void __launch_bounds__(kScanThreads, 1) gdn_chunk_scan_kernel(const P
                 for (int s = 0; s < 4; ++s) {
                     const uint64_t u1 = tc::desc_at(dsc, sc::kU1 + s * 32), u2 = tc::desc_at(dsc, sc::kU2 + s * 32);
                     const uint64_t p1 = tc::desc_at(dsc, sc::kP1 + s * 32), p2 = tc::desc_at(dsc, sc::kP2 + s * 32);
-                    const uint64_t k1 = tc::desc_at(dsc, sc::kK1 + s * 32), k2 = tc::desc_at(dsc, sc::kK2 + s * 32);
+                    const uint64_t k1 = tc::desc_at(dsc_k, s * 2048), k2 = tc::desc_at(dsc_k, (sc::kK2 - sc::kK1) + s * 2048);
                     tc::mma_bf16(oa, u1, p1, id64, s ? 1u : 0u);
                     tc::mma_bf16(oa, u1, p2, id64, 1u);
                     tc::mma_bf16(oa, u2, p1, id64, 1u);
-                    tc::mma_bf16(tm + 256, u1, k1, id128, s ? 1u : 0u);
-                    tc::mma_bf16(tm + 256, u1, k2, id128, 1u);
-                    tc::mma_bf16(tm + 256, u2, k1, id128, 1u);
+                    tc::mma_bf16(tm + 256, u1, k1, id128k, s ? 1u : 0u);
+                    tc::mma_bf16(tm + 256, u1, k2, id128k, 1u);
+                    tc::mma_bf16(tm + 256, u2, k1, id128k, 1u);
                 }
                 tc::commit(bar_b);
             }

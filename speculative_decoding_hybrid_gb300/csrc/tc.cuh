@@ -60,6 +60,23 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr) {
 // field changes.
 __device__ __forceinline__ uint64_t desc_at(uint64_t base, uint32_t off) { return base + (off >> 4); }
 
+// Descriptor of an MN-major 128-byte-swizzled tile (used for B): K rows of
+// 64 MN elements (128 B) swizzled like a K-major tile, 8-row K groups 1024 B
+// apart, and consecutive 64-element MN blocks `lbo` bytes apart.  One MMA's
+// 16 K rows span two K groups, so K steps advance the start by 2048 bytes.
+__device__ __forceinline__ uint64_t smem_desc_mn(uint32_t saddr, uint32_t lbo) {
+    uint64_t d = 0;
+    d |= uint64_t((saddr >> 4) & 0x3fffu);
+    d |= uint64_t((lbo >> 4) & 0x3fffu) << 16;
+    d |= uint64_t(1024u >> 4) << 32;
+    d |= uint64_t(1u) << 46;
+    d |= uint64_t(2u) << 61;
+    return d;
+}
+
+// Instruction-descriptor bit that marks B as MN-major.
+constexpr uint32_t kBMnMajor = 1u << 16;
+
 // Instruction descriptor for kind::f16 with bf16 A/B, fp32 D, both K-major.
 __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
     return (1u << 4)                       // D format: f32
