@@ -59,8 +59,8 @@ WORKLOAD_TEXT = {
 # DRAM traffic of one gdn_verify launch from an ncu capture (dram__bytes_read.sum + dram__bytes_write.sum)
 # on the full paged256 workload (profiles/dram_verify_paged256.md); reported only while the kernel source
 # is the one that was captured (its digest), otherwise null.
-TRAFFIC = {"gdn_verify": {"src_sha": "ab37bc2427cc02e5", "workload": "paged256",
-                          "bytes_per_launch": 554067968 + 2093959424, "alg_bytes_per_launch": 2709782528}}
+TRAFFIC = {"gdn_verify": {"src_sha": "95d7bcb94e1e7be8", "workload": "paged256",
+                          "bytes_per_launch": 554057472 + 2093630464, "alg_bytes_per_launch": 2709782528}}
 
 
 def src_digest(path):
@@ -397,6 +397,11 @@ class Bench:
         """One transaction.  ``ev`` (optional) collects, per kernel class, CUDA
         event pairs around its launches and the number of launches between
         them: the verify pair spans every layer's launch of one step."""
+        p = self.launch(ev)
+        return self.finish(p)
+
+    def launch(self, ev=None):
+        """Plans the step and queues its kernels (no host synchronisation)."""
         s = self.step_no
         ring, p = self.prepare(s)
         vs, loop = self.vs, self.loop
@@ -428,8 +433,13 @@ class Bench:
                 vs.accept(B, loop.cu_rows, self.logits[ring], self.tok_d)
             with timed(ev, "commit", 1):
                 vs.commit(B, loop.cu_rows, loop.dst_slot)
+        return p
+
+    def finish(self, p):
+        """The step's one readback, then the host bookkeeping."""
+        loop = self.loop
         acc, bon, out = loop.readback()
-        n_ver = int(acc.sum().item()) + B
+        n_ver = int(acc.sum().item()) + loop.B
         loop.finish(acc)
         self.step_no += 1
         self.verified += n_ver
@@ -511,25 +521,58 @@ def run_zero_copy(spec, dev, args, replay=False, graph=False):
     return res
 
 
+def _packed_layout(b: Bench):
+    """Byte offsets of every layer's row inputs and the logits in one packed
+    buffer (each piece 256-byte aligned)."""
+    pieces, off = [], 0
+    for r in b.rows[0]:
+        for x in (r.q, r.k, r.v, r.g, r.beta):
+            pieces.append((off, x.dtype, tuple(x.shape)))
+            off += (x.numel() * x.element_size() + 255) // 256 * 256
+    lg = b.logits[0]
+    pieces.append((off, lg.dtype, tuple(lg.shape)))
+    off += (lg.numel() * lg.element_size() + 255) // 256 * 256
+    return pieces, off
+
+
+def _views(buf, pieces):
+    out = []
+    for off, dt, shape in pieces:
+        n = 1
+        for d in shape:
+            n *= d
+        nbytes = n * torch.empty((), dtype=dt).element_size()
+        out.append(buf[off:off + nbytes].view(dt).view(shape))
+    return out
+
+
 def stage_e2e(b: Bench):
-    """Pinned host copies of the ring inputs and two device staging sets."""
+    """Every ring set's inputs packed into one pinned host buffer, and two
+    device staging buffers of the same layout (one copy per step)."""
     from speculative_decoding_hybrid_gb300.step import LayerRows
+    pieces, total = _packed_layout(b)
     host = []
     for i in range(b.spec.ring):
-        hl = [[x.detach().to("cpu").pin_memory() for x in (r.q, r.k, r.v, r.g, r.beta)] for r in b.rows[i]]
-        host.append((hl, b.logits[i].detach().to("cpu").pin_memory()))
+        hb = torch.empty((total,), dtype=torch.uint8).pin_memory()
+        src = [x for r in b.rows[i] for x in (r.q, r.k, r.v, r.g, r.beta)] + [b.logits[i]]
+        for v, x in zip(_views(hb, pieces), src):
+            v.copy_(x.detach().to("cpu"))
+        host.append(hb)
     stages = []
     for _ in range(2):
-        rows = [LayerRows(*(torch.empty_like(x) for x in (r.q, r.k, r.v, r.g, r.beta))) for r in b.rows[0]]
-        stages.append((rows, torch.empty_like(b.logits[0])))
+        db = torch.empty((total,), dtype=torch.uint8, device=b.dev)
+        vs = _views(db, pieces)
+        rows = [LayerRows(*vs[5 * l:5 * l + 5]) for l in range(len(b.rows[0]))]
+        stages.append((db, rows, vs[-1]))
     return host, stages
 
 
 def run_e2e(b: Bench, host, stages, steps, warmup):
     """Same step through the public API, with every step's inputs copied from
     pinned host memory and the results read back inside the timed region.
-    Copies for step s+1 run on a copy stream while step s computes (two
-    device staging sets); a step waits for its own inputs' copy event."""
+    A step's kernels are queued first; then the next step's inputs (one
+    packed copy) go to the other device staging buffer on a copy stream while
+    this step computes; a step waits for its own inputs' copy event."""
     spec = b.spec
     saved_rows, saved_logits = b.rows, b.logits
     copy_stream = torch.cuda.Stream()
@@ -539,30 +582,23 @@ def run_e2e(b: Bench, host, stages, steps, warmup):
     moved_bytes = [0]
 
     def issue_copy(step_no, slot):
-        hl, hlog = host[step_no % spec.ring]
-        rows, logits = stages[slot]
+        hb = host[step_no % spec.ring]
+        db = stages[slot][0]
         with torch.cuda.stream(copy_stream):
             copy_stream.wait_event(free[slot])  # the staging set's previous reader is done
-            moved = 0
-            for l in range(spec.layers):
-                dst = rows[l]
-                for x, dt in zip(hl[l], (dst.q, dst.k, dst.v, dst.g, dst.beta)):
-                    dt.copy_(x, non_blocking=True)
-                    moved += x.numel() * x.element_size()
-            logits.copy_(hlog, non_blocking=True)
-            moved += hlog.numel() * hlog.element_size()
+            db.copy_(hb, non_blocking=True)
             done[slot].record(copy_stream)
-        moved_bytes[0] += moved
+        moved_bytes[0] += hb.numel()
 
     def one(slot):
         compute.wait_event(done[slot])
-        rows, logits = stages[slot]
+        _, rows, logits = stages[slot]
         b.rows = [rows] * spec.ring
         b.logits = [logits] * spec.ring
-        issue_copy(b.step_no + 1, slot ^ 1)       # next step's inputs, overlapped
-        n, p = b.step()                           # ends with the step's one readback
+        p = b.launch()
         free[slot].record(compute)
-        return n, p
+        issue_copy(b.step_no + 1, slot ^ 1)       # next step's inputs, overlapped
+        return b.finish(p)                        # the step's one readback
 
     try:
         for e in free:
@@ -584,9 +620,17 @@ def run_e2e(b: Bench, host, stages, steps, warmup):
         dt = time.perf_counter() - t0
     finally:
         b.rows, b.logits = saved_rows, saved_logits
+    # the packed input copy alone, for context (how much of a step it would cost unhidden)
+    ca, cb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(copy_stream):
+        ca.record(copy_stream)
+        stages[0][0].copy_(host[0], non_blocking=True)
+        cb.record(copy_stream)
+    torch.cuda.synchronize()
+    copy_ms = ca.elapsed_time(cb)
     h2d = moved_bytes[0] / steps + (b.loop.B + 1) * 3 * 4 + b.cap * 4   # inputs + tables + tokens
     d2h = (2 * spec.batch + b.cap) * 4
-    return tok / dt, h2d, d2h
+    return tok / dt, h2d, d2h, copy_ms
 
 
 # ---------------------------------------------------------------------------
@@ -678,7 +722,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="paged256", choices=sorted(WORKLOADS) + sorted(PREFILL_SETS))
-    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--e2e-steps", type=int, default=40)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-prefill", action="store_true")
@@ -769,14 +813,15 @@ def main():
     e2e = None
     if not args.no_e2e:
         host, stages = stage_e2e(b)
-        val, h2d, d2h = run_e2e(b, host, stages, args.e2e_steps, 3)
+        val, h2d, d2h, copy_ms = run_e2e(b, host, stages, args.e2e_steps, 3)
         del host, stages
         if world > 1:
             t = torch.tensor([val], device=dev, dtype=torch.float64)
             dist.all_reduce(t)
             val = float(t.item())
         e2e = {"value": val, "unit": "verified tokens/s", "h2d_bytes_per_step": int(h2d),
-               "d2h_bytes_per_step": int(d2h), "steps": args.e2e_steps}
+               "d2h_bytes_per_step": int(d2h), "steps": args.e2e_steps,
+               "input_copy_ms_alone": copy_ms, "input_copy_gbs": h2d / (copy_ms * 1e-3) / 1e9}
 
     if rank != 0:
         if world > 1:

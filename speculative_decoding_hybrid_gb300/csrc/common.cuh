@@ -98,6 +98,16 @@ __device__ __forceinline__ void cp_async_wait() {
     asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
+// Programmatic dependent launch (kernels launched by gdn_host::launch_pdl):
+// let the next kernel on the stream be scheduled while this grid drains, then
+// wait until the previous grid has finished and its writes are visible.  It
+// comes before a kernel's first global-memory access; in a launch without
+// the attribute the wait returns at once.
+__device__ __forceinline__ void pdl_enter() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 __device__ __forceinline__ void set_status(uint32_t *status, uint32_t bits) {
     if (status) atomicOr(status, bits);
 }
@@ -115,4 +125,23 @@ inline bool dims_ok(const gdn_dims *d) {
     return true;
 }
 inline int launch_status(cudaError_t e) { return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA; }
+
+// Launch with programmatic stream serialization: the kernel (which starts
+// with gdn::pdl_enter) may be scheduled while the previous kernel on the
+// stream drains, instead of after it has fully retired.
+template <typename... KArgs, typename... Args>
+inline int launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                      Args... args) {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr{};
+    attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr.val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    return launch_status(cudaLaunchKernelEx(&cfg, kernel, args...));
+}
 }  // namespace gdn_host

@@ -28,6 +28,7 @@ struct CommitArgs {
 };
 
 __global__ void __launch_bounds__(kThreads) gdn_commit_kernel(const CommitArgs a) {
+    gdn::pdl_enter();
     const long long idx = blockIdx.x;
     const int c = int(idx % a.chunks);
     const long long rl = idx / a.chunks;
@@ -82,6 +83,7 @@ struct LocArgs {
 };
 
 __global__ void __launch_bounds__(kThreads) gdn_commit_at_kernel(const LocArgs a) {
+    gdn::pdl_enter();
     const long long idx = (long long)blockIdx.x * kThreads + threadIdx.x;
     if (idx >= (long long)a.B * a.L) return;
     if (a.status && (*reinterpret_cast<volatile uint32_t *>(a.status) & GDN_DEV_TIMEOUT)) return;
@@ -117,6 +119,7 @@ struct MatArgs {
 };
 
 __global__ void __launch_bounds__(kThreads) gdn_materialize_kernel(const MatArgs a) {
+    gdn::pdl_enter();
     const long long idx = blockIdx.x;
     const int c = int(idx % a.chunks);
     const long long rl = idx / a.chunks;
@@ -166,9 +169,8 @@ extern "C" int gdn_commit_at(const gdn_dims *dims, int32_t B, int32_t num_layers
     a.loc = loc;
     a.status = dev_status;
     const long long n = (long long)B * num_layers;
-    gdn_commit_at_kernel<<<unsigned((n + kThreads - 1) / kThreads), kThreads, 0, static_cast<cudaStream_t>(stream)>>>(
-        a);
-    return gdn_host::launch_status(cudaGetLastError());
+    return gdn_host::launch_pdl(gdn_commit_at_kernel, dim3(unsigned((n + kThreads - 1) / kThreads)), dim3(kThreads), 0,
+                                static_cast<cudaStream_t>(stream), a);
 }
 
 extern "C" int gdn_materialize(const gdn_dims *dims, int32_t B, int32_t num_layers, const float *state_base,
@@ -200,7 +202,9 @@ extern "C" int gdn_materialize(const gdn_dims *dims, int32_t B, int32_t num_laye
     a.status = dev_status;
     const long long grid = (long long)B * num_layers * a.chunks;
     if (grid > 0x7fffffffLL) return GDN_ERR_ARG;
-    gdn_materialize_kernel<<<unsigned(grid), kThreads, 0, static_cast<cudaStream_t>(stream)>>>(a);
+    const int st_m = gdn_host::launch_pdl(gdn_materialize_kernel, dim3(unsigned(grid)), dim3(kThreads), 0,
+                                          static_cast<cudaStream_t>(stream), a);
+    if (st_m != GDN_OK) return st_m;
     return gdn_host::launch_status(cudaGetLastError());
 }
 
@@ -239,6 +243,6 @@ extern "C" int gdn_commit(const gdn_dims *dims, int32_t B, int32_t num_layers, i
     a.status = dev_status;
     const long long grid = (long long)B * num_layers * a.chunks;
     if (grid > 0x7fffffffLL) return GDN_ERR_ARG;
-    gdn_commit_kernel<<<unsigned(grid), kThreads, 0, static_cast<cudaStream_t>(stream)>>>(a);
-    return gdn_host::launch_status(cudaGetLastError());
+    return gdn_host::launch_pdl(gdn_commit_kernel, dim3(unsigned(grid)), dim3(kThreads), 0,
+                                static_cast<cudaStream_t>(stream), a);
 }

@@ -150,6 +150,7 @@ __global__ void __launch_bounds__(kThreads, 4) gdn_recurrent_kernel(const RecArg
     float *vsm = reinterpret_cast<float *>(smem + L::kVOff);
     float *gsm = reinterpret_cast<float *>(smem + L::kGOff);
     float *bsm = gsm + GDN_MAX_ROWS;
+    gdn::pdl_enter();
 
     const int tid = threadIdx.x;
     const int bid = blockIdx.x;
@@ -343,8 +344,7 @@ int launch(const RecArgs &a, cudaStream_t st) {
     const long long grid = (long long)a.B * a.h_v * b.bph;
     if (grid <= 0) return GDN_OK;
     if (grid > 0x7fffffffLL) return GDN_ERR_ARG;
-    kern<<<unsigned(grid), kThreads, smem, st>>>(b);
-    return gdn_host::launch_status(cudaGetLastError());
+    return gdn_host::launch_pdl(kern, dim3(unsigned(grid)), dim3(kThreads), smem, st, b);
 }
 
 template <int MODE>

@@ -56,6 +56,7 @@ struct ArgArgs {
 };
 
 __global__ void __launch_bounds__(kArgThreads) argmax_partial_kernel(const ArgArgs a) {
+    gdn::pdl_enter();
     const int split = blockIdx.x;
     const int row = blockIdx.y;
     int total = a.cu_rows[a.B];
@@ -128,6 +129,7 @@ struct AccArgs {
 constexpr int kAccWarps = 4;
 
 __global__ void __launch_bounds__(kAccWarps * 32) accept_finalize_kernel(const AccArgs a) {
+    gdn::pdl_enter();
     const int lane = threadIdx.x & 31;
     const int r = blockIdx.x * kAccWarps + (threadIdx.x >> 5);
     if (r >= a.B) return;
@@ -228,8 +230,9 @@ int gdn_accept_launch(int32_t B, int32_t row_capacity, const int32_t *cu_rows, c
         aa.vec = (gdn_host::aligned16(logits) && (row_stride % 8) == 0) ? 1 : 0;
         aa.partial = static_cast<unsigned long long *>(workspace);
         if (row_capacity > 65535) return GDN_ERR_ARG;
-        argmax_partial_kernel<<<dim3(splits, row_capacity), kArgThreads, 0, st>>>(aa);
-        if (cudaGetLastError() != cudaSuccess) return GDN_ERR_CUDA;
+        const int st_a = gdn_host::launch_pdl(argmax_partial_kernel, dim3(splits, row_capacity), dim3(kArgThreads), 0,
+                                              st, aa);
+        if (st_a != GDN_OK) return st_a;
     }
     AccArgs ac{};
     ac.cu_rows = cu_rows;
@@ -245,8 +248,8 @@ int gdn_accept_launch(int32_t B, int32_t row_capacity, const int32_t *cu_rows, c
     ac.out_tokens = out_tokens;
     ac.stats = stats;
     ac.status = dev_status;
-    accept_finalize_kernel<<<(B + kAccWarps - 1) / kAccWarps, kAccWarps * 32, 0, st>>>(ac);
-    return gdn_host::launch_status(cudaGetLastError());
+    return gdn_host::launch_pdl(accept_finalize_kernel, dim3((B + kAccWarps - 1) / kAccWarps), dim3(kAccWarps * 32), 0,
+                                st, ac);
 }
 
 extern "C" int mtp_greedy_accept(int32_t B, int32_t row_capacity, const int32_t *cu_rows, const gdn_bf16 *logits,
