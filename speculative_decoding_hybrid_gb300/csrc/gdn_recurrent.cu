@@ -43,9 +43,13 @@ struct Lay {
     static constexpr size_t kVOff = kKqOff + size_t(GDN_MAX_ROWS) * 2 * DK * 2;
     static constexpr size_t kGOff = kVOff + size_t(GDN_MAX_ROWS) * RB * 4;
     static constexpr size_t kSmem = kGOff + 2 * GDN_MAX_ROWS * 4;
-    // replay mode: the previous transaction's accepted rows (k, v, g, beta)
-    static constexpr size_t kRkOff = kSmem;
-    static constexpr size_t kRvOff = kRkOff + size_t(GDN_MAX_ROWS) * DK * 2;
+    // replay mode (limited by instruction issue, not HBM): k and q staged as
+    // fp32, converted once per CTA instead of once per lane group, and the
+    // previous transaction's accepted rows (k as fp32, v, g, beta)
+    static constexpr size_t kVOffR = kKqOff + size_t(GDN_MAX_ROWS) * 2 * DK * 4;
+    static constexpr size_t kGOffR = kVOffR + size_t(GDN_MAX_ROWS) * RB * 4;
+    static constexpr size_t kRkOff = kGOffR + 2 * GDN_MAX_ROWS * 4;
+    static constexpr size_t kRvOff = kRkOff + size_t(GDN_MAX_ROWS) * DK * 4;
     static constexpr size_t kRgOff = kRvOff + size_t(GDN_MAX_ROWS) * RB * 4;
     static constexpr size_t kSmemReplay = kRgOff + 2 * GDN_MAX_ROWS * 4;
 };
@@ -147,8 +151,9 @@ __global__ void __launch_bounds__(kThreads, 4) gdn_recurrent_kernel(const RecArg
     int *flag = reinterpret_cast<int *>(smem + 64);
     float *tile = reinterpret_cast<float *>(smem + L::kTileOff);
     uint16_t *kq = reinterpret_cast<uint16_t *>(smem + L::kKqOff);
-    float *vsm = reinterpret_cast<float *>(smem + L::kVOff);
-    float *gsm = reinterpret_cast<float *>(smem + L::kGOff);
+    float *kqf = reinterpret_cast<float *>(smem + L::kKqOff);  // replay: fp32 k/q
+    float *vsm = reinterpret_cast<float *>(smem + (REPLAY ? L::kVOffR : L::kVOff));
+    float *gsm = reinterpret_cast<float *>(smem + (REPLAY ? L::kGOffR : L::kGOff));
     float *bsm = gsm + GDN_MAX_ROWS;
     gdn::pdl_enter();
 
@@ -228,7 +233,14 @@ __global__ void __launch_bounds__(kThreads, 4) gdn_recurrent_kernel(const RecArg
         const int which = rem / VPR;
         const int c = rem - which * VPR;
         const uint16_t *sp = (which == 0 ? a.k : a.q) + (size_t(t0 + t) * a.h_qk + hq) * DK + c * 8;
-        *reinterpret_cast<uint4 *>(kq + (t * 2 + which) * DK + c * 8) = __ldg(reinterpret_cast<const uint4 *>(sp));
+        const uint4 w = __ldg(reinterpret_cast<const uint4 *>(sp));
+        if constexpr (REPLAY) {
+            float4 *dp = reinterpret_cast<float4 *>(kqf + (t * 2 + which) * DK + c * 8);
+            dp[0] = bf16x4_to_f32(make_uint2(w.x, w.y));
+            dp[1] = bf16x4_to_f32(make_uint2(w.z, w.w));
+        } else {
+            *reinterpret_cast<uint4 *>(kq + (t * 2 + which) * DK + c * 8) = w;
+        }
     }
     for (int i = tid; i < nrows * nr; i += kThreads) {
         const int t = i / nr;
@@ -239,15 +251,17 @@ __global__ void __launch_bounds__(kThreads, 4) gdn_recurrent_kernel(const RecArg
         gsm[tid] = a.g[size_t(t0 + tid) * a.h_v + h];
         bsm[tid] = a.beta[size_t(t0 + tid) * a.h_v + h];
     }
-    uint16_t *rk = reinterpret_cast<uint16_t *>(smem + L::kRkOff);
+    float *rk = reinterpret_cast<float *>(smem + L::kRkOff);
     float *rv = reinterpret_cast<float *>(smem + L::kRvOff);
     float *rg = reinterpret_cast<float *>(smem + L::kRgOff);
     float *rbeta = rg + GDN_MAX_ROWS;
     if (REPLAY) {
         for (int i = tid; i < nrep * VPR; i += kThreads) {
             const int t = i / VPR, c = i - t * VPR;
-            *reinterpret_cast<uint4 *>(rk + t * DK + c * 8) =
-                __ldg(reinterpret_cast<const uint4 *>(a.pk + (size_t(p0 + t) * a.h_qk + hq) * DK + c * 8));
+            const uint4 w = __ldg(reinterpret_cast<const uint4 *>(a.pk + (size_t(p0 + t) * a.h_qk + hq) * DK + c * 8));
+            float4 *dp = reinterpret_cast<float4 *>(rk + t * DK + c * 8);
+            dp[0] = bf16x4_to_f32(make_uint2(w.x, w.y));
+            dp[1] = bf16x4_to_f32(make_uint2(w.z, w.w));
         }
         for (int i = tid; i < nrep * nr; i += kThreads) {
             const int t = i / nr, row = i - t * nr;
@@ -287,7 +301,7 @@ __global__ void __launch_bounds__(kThreads, 4) gdn_recurrent_kernel(const RecArg
             float4 kf[L::NV];
 #pragma unroll
             for (int c = 0; c < L::NV; ++c)
-                kf[c] = bf16x4_to_f32(*reinterpret_cast<const uint2 *>(rk + t * DK + (c * L::LPR + li) * 4));
+                kf[c] = *reinterpret_cast<const float4 *>(rk + t * DK + (c * L::LPR + li) * 4);
             const float vv = act ? rv[t * L::RB + lr] : 0.f;
             row_advance<L::NV, L::LPR>(s, kf, alpha, b, vv);
         }
@@ -306,8 +320,13 @@ __global__ void __launch_bounds__(kThreads, 4) gdn_recurrent_kernel(const RecArg
         float4 kf[L::NV], qf[L::NV];
 #pragma unroll
         for (int c = 0; c < L::NV; ++c) {
-            kf[c] = bf16x4_to_f32(*reinterpret_cast<const uint2 *>(kq + (t * 2 + 0) * DK + (c * L::LPR + li) * 4));
-            qf[c] = bf16x4_to_f32(*reinterpret_cast<const uint2 *>(kq + (t * 2 + 1) * DK + (c * L::LPR + li) * 4));
+            if constexpr (REPLAY) {
+                kf[c] = *reinterpret_cast<const float4 *>(kqf + (t * 2 + 0) * DK + (c * L::LPR + li) * 4);
+                qf[c] = *reinterpret_cast<const float4 *>(kqf + (t * 2 + 1) * DK + (c * L::LPR + li) * 4);
+            } else {
+                kf[c] = bf16x4_to_f32(*reinterpret_cast<const uint2 *>(kq + (t * 2 + 0) * DK + (c * L::LPR + li) * 4));
+                qf[c] = bf16x4_to_f32(*reinterpret_cast<const uint2 *>(kq + (t * 2 + 1) * DK + (c * L::LPR + li) * 4));
+            }
         }
         const float vv = act ? vsm[t * L::RB + lr] : 0.f;
         const float e = row_update<L::NV, L::LPR>(s, kf, qf, alpha, b, vv);
