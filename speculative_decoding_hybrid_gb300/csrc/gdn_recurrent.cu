@@ -242,13 +242,12 @@ __global__ void __launch_bounds__(kThreads, 4) gdn_recurrent_kernel(const RecArg
             *reinterpret_cast<uint4 *>(kq + (t * 2 + which) * DK + c * 8) = w;
         }
     }
-    for (int i = tid; i < nrows * nr; i += kThreads) {
-        const int t = i / nr;
-        const int row = i - t * nr;
-        vsm[t * L::RB + row] = gdn::bf16_to_f32(a.v[(size_t(t0 + t) * a.h_v + h) * a.dv + row0 + row]);
+    for (int i = tid; i < nrows * L::RB; i += kThreads) {
+        const int t = i / L::RB, row = i % L::RB;
+        if (row < nr) vsm[t * L::RB + row] = gdn::bf16_to_f32(a.v[(size_t(t0 + t) * a.h_v + h) * a.dv + row0 + row]);
     }
     if (tid < nrows) {
-        gsm[tid] = a.g[size_t(t0 + tid) * a.h_v + h];
+        gsm[tid] = expf(a.g[size_t(t0 + tid) * a.h_v + h]);  // alpha_t, once per token
         bsm[tid] = a.beta[size_t(t0 + tid) * a.h_v + h];
     }
     float *rk = reinterpret_cast<float *>(smem + L::kRkOff);
@@ -263,12 +262,13 @@ __global__ void __launch_bounds__(kThreads, 4) gdn_recurrent_kernel(const RecArg
             dp[0] = bf16x4_to_f32(make_uint2(w.x, w.y));
             dp[1] = bf16x4_to_f32(make_uint2(w.z, w.w));
         }
-        for (int i = tid; i < nrep * nr; i += kThreads) {
-            const int t = i / nr, row = i - t * nr;
+        for (int i = tid; i < nrep * L::RB; i += kThreads) {
+            const int t = i / L::RB, row = i % L::RB;
+            if (row >= nr) continue;
             rv[t * L::RB + row] = gdn::bf16_to_f32(a.pv[(size_t(p0 + t) * a.h_v + h) * a.dv + row0 + row]);
         }
         if (tid < nrep) {
-            rg[tid] = a.pg[size_t(p0 + tid) * a.h_v + h];
+            rg[tid] = expf(a.pg[size_t(p0 + tid) * a.h_v + h]);
             rbeta[tid] = a.pbeta[size_t(p0 + tid) * a.h_v + h];
         }
     }
@@ -296,7 +296,7 @@ __global__ void __launch_bounds__(kThreads, 4) gdn_recurrent_kernel(const RecArg
     if (REPLAY) {
         // The previous transaction's accepted rows: the state half of each token.
         for (int t = 0; t < nrep; ++t) {
-            const float alpha = expf(rg[t]);
+            const float alpha = rg[t];
             const float b = rbeta[t];
             float4 kf[L::NV];
 #pragma unroll
@@ -315,7 +315,7 @@ __global__ void __launch_bounds__(kThreads, 4) gdn_recurrent_kernel(const RecArg
         }
     }
     for (int t = 0; t < nrows; ++t) {
-        const float alpha = expf(gsm[t]);
+        const float alpha = gsm[t];
         const float b = bsm[t];
         float4 kf[L::NV], qf[L::NV];
 #pragma unroll
