@@ -92,20 +92,43 @@ __device__ __forceinline__ float group_sum(float x) {
     return x;
 }
 
+// Packed pairs of fp32 (Blackwell's f32x2 arithmetic: two lanes of IEEE
+// round-to-nearest fp32 per instruction, each rounded exactly like the
+// scalar operation).
+__device__ __forceinline__ unsigned long long f2_pack(float a, float b) {
+    unsigned long long r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+    return r;
+}
+__device__ __forceinline__ void f2_unpack(unsigned long long r, float &a, float &b) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(r));
+}
+__device__ __forceinline__ unsigned long long f2_mul(unsigned long long a, unsigned long long b) {
+    unsigned long long d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ unsigned long long f2_fma(unsigned long long a, unsigned long long b,
+                                                     unsigned long long c) {
+    unsigned long long d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+
+// A lane's share of a row dot product: even and odd elements accumulate in
+// the two halves of a packed pair (in element order), then the halves add.
 template <int NV>
 __device__ __forceinline__ float lane_dot(const float4 (&s)[NV], const float4 (&x)[NV]) {
-    float acc = __fmul_rn(s[0].x, x[0].x);
-    acc = __fmaf_rn(s[0].y, x[0].y, acc);
-    acc = __fmaf_rn(s[0].z, x[0].z, acc);
-    acc = __fmaf_rn(s[0].w, x[0].w, acc);
+    unsigned long long acc = f2_mul(f2_pack(s[0].x, s[0].y), f2_pack(x[0].x, x[0].y));
+    acc = f2_fma(f2_pack(s[0].z, s[0].w), f2_pack(x[0].z, x[0].w), acc);
 #pragma unroll
     for (int c = 1; c < NV; ++c) {
-        acc = __fmaf_rn(s[c].x, x[c].x, acc);
-        acc = __fmaf_rn(s[c].y, x[c].y, acc);
-        acc = __fmaf_rn(s[c].z, x[c].z, acc);
-        acc = __fmaf_rn(s[c].w, x[c].w, acc);
+        acc = f2_fma(f2_pack(s[c].x, s[c].y), f2_pack(x[c].x, x[c].y), acc);
+        acc = f2_fma(f2_pack(s[c].z, s[c].w), f2_pack(x[c].z, x[c].w), acc);
     }
-    return acc;
+    float e, o;
+    f2_unpack(acc, e, o);
+    return __fadd_rn(e, o);
 }
 
 // The state half of a token: prediction S k, then S <- alpha S + u k^T.
@@ -116,12 +139,16 @@ __device__ __forceinline__ void row_advance(float4 (&s)[NV], const float4 (&kf)[
                                             float vv) {
     const float pred = group_sum<LPR>(lane_dot<NV>(s, kf));
     const float u = __fmul_rn(b, __fsub_rn(vv, __fmul_rn(alpha, pred)));
+    // s <- u k + alpha s, elementwise (round(alpha s) then one fused multiply-add)
+    const unsigned long long a2 = f2_pack(alpha, alpha), u2 = f2_pack(u, u);
 #pragma unroll
     for (int c = 0; c < NV; ++c) {
-        s[c].x = __fmaf_rn(u, kf[c].x, __fmul_rn(alpha, s[c].x));
-        s[c].y = __fmaf_rn(u, kf[c].y, __fmul_rn(alpha, s[c].y));
-        s[c].z = __fmaf_rn(u, kf[c].z, __fmul_rn(alpha, s[c].z));
-        s[c].w = __fmaf_rn(u, kf[c].w, __fmul_rn(alpha, s[c].w));
+        const unsigned long long xy =
+            f2_fma(u2, f2_pack(kf[c].x, kf[c].y), f2_mul(a2, f2_pack(s[c].x, s[c].y)));
+        const unsigned long long zw =
+            f2_fma(u2, f2_pack(kf[c].z, kf[c].w), f2_mul(a2, f2_pack(s[c].z, s[c].w)));
+        f2_unpack(xy, s[c].x, s[c].y);
+        f2_unpack(zw, s[c].z, s[c].w);
     }
 }
 
