@@ -191,47 +191,53 @@ __global__ void __launch_bounds__(kThreads, 4) gdn_recurrent_kernel(const RecArg
     const int r = bid / (a.bph * a.h_v);
     const bool lead = (h == 0 && rb == 0 && tid == 0);
 
-    int t0, nrows;
-    uint32_t bad = 0;
+    // Every table entry this request needs, loaded together (no load waits
+    // on another); then the checks.
+    int t0 = r, t1 = r + 1;
     if (VERIFY || REPLAY) {
         t0 = a.cu_rows[r];
-        const int t1 = a.cu_rows[r + 1];
-        nrows = t1 - t0;
+        t1 = a.cu_rows[r + 1];
+    }
+    int acc = -1, pc0 = 0, pc1 = 0;
+    if (REPLAY) {
+        acc = a.prev_acc[r];
+        pc0 = a.prev_cu[r];
+        pc1 = a.prev_cu[r + 1];
+    }
+    int64_t off = 0;
+    int src = 0;
+    if (AT)
+        off = a.src_off[r];
+    else
+        src = a.src_slot[r];
+    int dst = 0;
+    if (WRITES_SLOT) dst = a.dst_slot[r];
+
+    uint32_t bad = 0;
+    const int nrows = t1 - t0;
+    if (VERIFY || REPLAY) {
         const int min_rows = REPLAY ? 0 : 1;
         if (t0 < 0 || nrows < min_rows || nrows > GDN_MAX_ROWS || t1 > a.row_capacity) bad |= GDN_DEV_ROWS_BAD;
-    } else {
-        t0 = r;
-        nrows = 1;
     }
     int p0 = 0, nrep = 0;  // replay rows p0 .. p0 + nrep - 1 of the previous transaction
-    if (REPLAY) {
-        const int acc = a.prev_acc[r];
-        if (acc >= 0) {
-            p0 = a.prev_cu[r];
-            nrep = acc + 1;
-            const int p1 = a.prev_cu[r + 1];
-            if (p0 < 0 || p0 + nrep > p1 || nrep > GDN_MAX_ROWS || p1 > a.prev_capacity) bad |= GDN_DEV_ROWS_BAD;
-        }
+    if (REPLAY && acc >= 0) {
+        p0 = pc0;
+        nrep = acc + 1;
+        if (p0 < 0 || p0 + nrep > pc1 || nrep > GDN_MAX_ROWS || pc1 > a.prev_capacity) bad |= GDN_DEV_ROWS_BAD;
     }
     const float *src_base = a.pool_src;
     if (AT) {
-        const int64_t off = a.src_off[r];
         if (off < 0 || off > a.max_off || (off & 3) != 0)
             bad |= GDN_DEV_SLOT_OOR;
         else
             src_base = a.pool_src + off;
     } else {
-        const int src = a.src_slot[r];
         if (src < 0 || src >= a.num_slots)
             bad |= GDN_DEV_SLOT_OOR;
         else
             src_base = a.pool_src + size_t(src) * a.slot_stride;
     }
-    int dst = 0;
-    if (WRITES_SLOT) {
-        dst = a.dst_slot[r];
-        if (dst < 0 || dst >= a.num_slots) bad |= GDN_DEV_SLOT_OOR;
-    }
+    if (WRITES_SLOT && (dst < 0 || dst >= a.num_slots)) bad |= GDN_DEV_SLOT_OOR;
     if (bad) {
         if (lead) {
             gdn::set_status(a.status, bad);
@@ -334,7 +340,7 @@ __global__ void __launch_bounds__(kThreads, 4) gdn_recurrent_kernel(const RecArg
         }
         // The replayed state is the request's committed state (also copied
         // when nothing is pending but the request moves to a fresh slot).
-        const bool moved = a.src_slot[r] != dst;
+        const bool moved = src != dst;
         if (act && (nrep > 0 || moved)) {
             float *dp = a.pool_dst + size_t(dst) * a.slot_stride + tile_off;
 #pragma unroll
