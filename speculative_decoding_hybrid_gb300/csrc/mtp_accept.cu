@@ -36,6 +36,39 @@ __device__ __forceinline__ unsigned long long make_key(uint32_t bits, uint32_t i
     return (static_cast<unsigned long long>(order17(bits)) << 32) | (0xffffffffu - idx);
 }
 
+// Largest of two bf16 pairs, lane by lane, NaN if either is NaN.
+__device__ __forceinline__ uint32_t bmax2(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("max.NaN.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+
+// order17 of the largest of the 8 bf16 values of a 16-byte vector.
+__device__ __forceinline__ uint32_t vec_max_order(const uint4 &w) {
+    const uint32_t m = bmax2(bmax2(w.x, w.y), bmax2(w.z, w.w));
+    const uint32_t lo = order17(m & 0xffffu), hi = order17(m >> 16);
+    return lo > hi ? lo : hi;
+}
+
+// Running (order, index) of a thread's scan over increasing indices: a
+// vector whose largest value does not beat the best so far is skipped with
+// a few packed maxima; otherwise its first element of that order is found
+// (ties keep the earlier index, so the first occurrence wins).
+__device__ __forceinline__ void scan_vec(const uint4 &w, uint32_t base, uint32_t vo, uint32_t &best_o,
+                                         uint32_t &best_i) {
+    if (vo <= best_o) return;
+    const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+        const uint32_t bits = (e & 1) ? (ws[e >> 1] >> 16) : (ws[e >> 1] & 0xffffu);
+        if (order17(bits) == vo) {
+            best_o = vo;
+            best_i = base + uint32_t(e);
+            return;
+        }
+    }
+}
+
 __device__ __forceinline__ unsigned long long umax64(unsigned long long a, unsigned long long b) {
     return a > b ? a : b;
 }
@@ -73,31 +106,34 @@ __global__ void __launch_bounds__(kArgThreads) argmax_partial_kernel(const ArgAr
         const uint4 *vp = reinterpret_cast<const uint4 *>(rp + c0);
         const int64_t nvec = (c1 - c0) / 8;
         int64_t i = threadIdx.x;
+        uint32_t best_o = 0, best_i = 0;  // order 0 is below every value: nothing seen yet
+        uint32_t best2 = 0xff80ff80u;     // the prefilter's running maximum (bf16 pair; valid once seen)
+        bool seen = false;
         for (; i + 3 * kArgThreads < nvec; i += 4 * kArgThreads) {
             uint4 w[4];
 #pragma unroll
             for (int u = 0; u < 4; ++u) w[u] = __ldcs(vp + i + u * kArgThreads);
+            // Prefilter in the bf16 domain: the chunk can only matter if its
+            // packed maximum differs from the running one (ties of -0 and +0
+            // pass here and are settled by the exact order below).
+            uint32_t m = bmax2(bmax2(bmax2(w[0].x, w[0].y), bmax2(w[0].z, w[0].w)),
+                               bmax2(bmax2(w[1].x, w[1].y), bmax2(w[1].z, w[1].w)));
+            m = bmax2(m, bmax2(bmax2(bmax2(w[2].x, w[2].y), bmax2(w[2].z, w[2].w)),
+                               bmax2(bmax2(w[3].x, w[3].y), bmax2(w[3].z, w[3].w))));
+            m = bmax2(m, __byte_perm(m, 0u, 0x1032));  // both halves: the chunk's maximum
+            if (!seen || bmax2(m, best2) != best2) {
+                seen = true;
+                best2 = bmax2(m, best2);
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const uint32_t base = uint32_t(c0 + (i + u * kArgThreads) * 8);
-                const uint32_t ws[4] = {w[u].x, w[u].y, w[u].z, w[u].w};
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    best = umax64(best, make_key(ws[e] & 0xffffu, base + 2 * e));
-                    best = umax64(best, make_key(ws[e] >> 16, base + 2 * e + 1));
-                }
+                for (int u = 0; u < 4; ++u)
+                    scan_vec(w[u], uint32_t(c0 + (i + u * kArgThreads) * 8), vec_max_order(w[u]), best_o, best_i);
             }
         }
         for (; i < nvec; i += kArgThreads) {
             const uint4 w = __ldcs(vp + i);
-            const uint32_t base = uint32_t(c0 + i * 8);
-            const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                best = umax64(best, make_key(ws[e] & 0xffffu, base + 2 * e));
-                best = umax64(best, make_key(ws[e] >> 16, base + 2 * e + 1));
-            }
+            scan_vec(w, uint32_t(c0 + i * 8), vec_max_order(w), best_o, best_i);
         }
+        if (best_o) best = (static_cast<unsigned long long>(best_o) << 32) | (0xffffffffu - best_i);
         // tail (vocab not a multiple of 8)
         for (int64_t j = c0 + nvec * 8 + threadIdx.x; j < c1; j += kArgThreads)
             best = umax64(best, make_key(rp[j], uint32_t(j)));
@@ -182,6 +218,8 @@ __global__ void __launch_bounds__(kAccWarps * 32) accept_finalize_kernel(const A
     }
 }
 
+// Vocabulary splits per row: about 1024 CTAs in all, at most kMaxSplits and
+// at least kMinSplitElems entries each.
 int accept_splits(int32_t rows, int64_t vocab) {
     int64_t s = (1024 + int64_t(rows > 0 ? rows : 1) - 1) / int64_t(rows > 0 ? rows : 1);
     if (s > kMaxSplits) s = kMaxSplits;

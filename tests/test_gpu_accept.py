@@ -67,7 +67,7 @@ def test_full_vocab_bernoulli_drafts(gs, cuda_dev):
 
 def test_ties_nan_and_split_boundaries(gs, cuda_dev):
     V = 151936
-    R = 6
+    R = 7
     lg = torch.randn((R, V), generator=sy.generator(9)).to(torch.bfloat16)
     # row 0: ties at three places, spanning several CTA splits: the lowest index wins
     for i in (149000, 70001, 70000):
@@ -83,8 +83,9 @@ def test_ties_nan_and_split_boundaries(gs, cuda_dev):
     lg[4] = float("-inf")
     lg[4, V - 1] = -1e30
     lg[5, V - 1] = 50.0
-    toks = [0, 1, 2, 3, 4, 5]
-    cu = [0, 2, 4, 6]
+    lg[6] = float("-inf")     # row 6: nothing but -inf, so the first index wins
+    toks = [0, 1, 2, 3, 4, 5, 6]
+    cu = [0, 2, 4, 7]
     toks[1] = 70000           # draft equals row 0's greedy choice
     check_against_oracle(gs, cuda_dev, lg, V, toks, cu)
 
