@@ -257,52 +257,111 @@ __global__ void __launch_bounds__(kThreads, 4) gdn_recurrent_kernel(const RecArg
         gdn::bulk_g2s(tile, src_base + tile_off, uint32_t(nr) * DK * 4u, bar);
     }
 
-    // Stage k and q rows (bf16) of this request's qk-head, 16 B per load.
+    // Stage the rows: k and q (this request's qk-head, 16 B per load), the
+    // tile's v entries and the gates, and in replay mode the previous
+    // transaction's accepted k, v and gates.  Every thread issues all of its
+    // loads before its first shared-memory store, so the loads overlap
+    // instead of waiting on one another.
     const int hq = h / a.grp;
     constexpr int VPR = DK / 8;
-    for (int i = tid; i < nrows * 2 * VPR; i += kThreads) {
-        const int t = i / (2 * VPR);
-        const int rem = i - t * 2 * VPR;
-        const int which = rem / VPR;
-        const int c = rem - which * VPR;
-        const uint16_t *sp = (which == 0 ? a.k : a.q) + (size_t(t0 + t) * a.h_qk + hq) * DK + c * 8;
-        const uint4 w = __ldg(reinterpret_cast<const uint4 *>(sp));
-        if constexpr (REPLAY) {
-            float4 *dp = reinterpret_cast<float4 *>(kqf + (t * 2 + which) * DK + c * 8);
-            dp[0] = bf16x4_to_f32(make_uint2(w.x, w.y));
-            dp[1] = bf16x4_to_f32(make_uint2(w.z, w.w));
-        } else {
-            *reinterpret_cast<uint4 *>(kq + (t * 2 + which) * DK + c * 8) = w;
+    constexpr int KQ_IT = (GDN_MAX_ROWS * 2 * VPR + kThreads - 1) / kThreads;
+    constexpr int V_IT = (GDN_MAX_ROWS * L::RB + kThreads - 1) / kThreads;
+    constexpr int RK_IT = (GDN_MAX_ROWS * VPR + kThreads - 1) / kThreads;
+    uint4 kqw[KQ_IT];
+    float vw[V_IT];
+#pragma unroll
+    for (int j = 0; j < KQ_IT; ++j) {
+        const int i = tid + j * kThreads;
+        if (i < nrows * 2 * VPR) {
+            const int t = i / (2 * VPR), rem = i % (2 * VPR), which = rem / VPR, c = rem % VPR;
+            const uint16_t *sp = (which == 0 ? a.k : a.q) + (size_t(t0 + t) * a.h_qk + hq) * DK + c * 8;
+            kqw[j] = __ldg(reinterpret_cast<const uint4 *>(sp));
         }
     }
-    for (int i = tid; i < nrows * L::RB; i += kThreads) {
+#pragma unroll
+    for (int j = 0; j < V_IT; ++j) {
+        const int i = tid + j * kThreads;
         const int t = i / L::RB, row = i % L::RB;
-        if (row < nr) vsm[t * L::RB + row] = gdn::bf16_to_f32(a.v[(size_t(t0 + t) * a.h_v + h) * a.dv + row0 + row]);
+        if (t < nrows && row < nr) vw[j] = gdn::bf16_to_f32(a.v[(size_t(t0 + t) * a.h_v + h) * a.dv + row0 + row]);
     }
+    float gw = 0.f, bw = 0.f;
     if (tid < nrows) {
-        gsm[tid] = expf(a.g[size_t(t0 + tid) * a.h_v + h]);  // alpha_t, once per token
-        bsm[tid] = a.beta[size_t(t0 + tid) * a.h_v + h];
+        gw = a.g[size_t(t0 + tid) * a.h_v + h];
+        bw = a.beta[size_t(t0 + tid) * a.h_v + h];
     }
     float *rk = reinterpret_cast<float *>(smem + L::kRkOff);
     float *rv = reinterpret_cast<float *>(smem + L::kRvOff);
     float *rg = reinterpret_cast<float *>(smem + L::kRgOff);
     float *rbeta = rg + GDN_MAX_ROWS;
-    if (REPLAY) {
-        for (int i = tid; i < nrep * VPR; i += kThreads) {
-            const int t = i / VPR, c = i - t * VPR;
-            const uint4 w = __ldg(reinterpret_cast<const uint4 *>(a.pk + (size_t(p0 + t) * a.h_qk + hq) * DK + c * 8));
-            float4 *dp = reinterpret_cast<float4 *>(rk + t * DK + c * 8);
-            dp[0] = bf16x4_to_f32(make_uint2(w.x, w.y));
-            dp[1] = bf16x4_to_f32(make_uint2(w.z, w.w));
+    uint4 rkw[RK_IT];
+    float rvw[V_IT];
+    float rgw = 0.f, rbw = 0.f;
+    if constexpr (REPLAY) {
+#pragma unroll
+        for (int j = 0; j < RK_IT; ++j) {
+            const int i = tid + j * kThreads;
+            if (i < nrep * VPR) {
+                const int t = i / VPR, c = i % VPR;
+                rkw[j] = __ldg(reinterpret_cast<const uint4 *>(a.pk + (size_t(p0 + t) * a.h_qk + hq) * DK + c * 8));
+            }
         }
-        for (int i = tid; i < nrep * L::RB; i += kThreads) {
+#pragma unroll
+        for (int j = 0; j < V_IT; ++j) {
+            const int i = tid + j * kThreads;
             const int t = i / L::RB, row = i % L::RB;
-            if (row >= nr) continue;
-            rv[t * L::RB + row] = gdn::bf16_to_f32(a.pv[(size_t(p0 + t) * a.h_v + h) * a.dv + row0 + row]);
+            if (t < nrep && row < nr)
+                rvw[j] = gdn::bf16_to_f32(a.pv[(size_t(p0 + t) * a.h_v + h) * a.dv + row0 + row]);
         }
         if (tid < nrep) {
-            rg[tid] = expf(a.pg[size_t(p0 + tid) * a.h_v + h]);
-            rbeta[tid] = a.pbeta[size_t(p0 + tid) * a.h_v + h];
+            rgw = a.pg[size_t(p0 + tid) * a.h_v + h];
+            rbw = a.pbeta[size_t(p0 + tid) * a.h_v + h];
+        }
+    }
+    // ... then the stores.
+#pragma unroll
+    for (int j = 0; j < KQ_IT; ++j) {
+        const int i = tid + j * kThreads;
+        if (i < nrows * 2 * VPR) {
+            const int t = i / (2 * VPR), rem = i % (2 * VPR), which = rem / VPR, c = rem % VPR;
+            if constexpr (REPLAY) {
+                float4 *dp = reinterpret_cast<float4 *>(kqf + (t * 2 + which) * DK + c * 8);
+                dp[0] = bf16x4_to_f32(make_uint2(kqw[j].x, kqw[j].y));
+                dp[1] = bf16x4_to_f32(make_uint2(kqw[j].z, kqw[j].w));
+            } else {
+                *reinterpret_cast<uint4 *>(kq + (t * 2 + which) * DK + c * 8) = kqw[j];
+            }
+        }
+    }
+#pragma unroll
+    for (int j = 0; j < V_IT; ++j) {
+        const int i = tid + j * kThreads;
+        const int t = i / L::RB, row = i % L::RB;
+        if (t < nrows && row < nr) vsm[t * L::RB + row] = vw[j];
+    }
+    if (tid < nrows) {
+        gsm[tid] = expf(gw);  // alpha_t, once per token
+        bsm[tid] = bw;
+    }
+    if constexpr (REPLAY) {
+#pragma unroll
+        for (int j = 0; j < RK_IT; ++j) {
+            const int i = tid + j * kThreads;
+            if (i < nrep * VPR) {
+                const int t = i / VPR, c = i % VPR;
+                float4 *dp = reinterpret_cast<float4 *>(rk + t * DK + c * 8);
+                dp[0] = bf16x4_to_f32(make_uint2(rkw[j].x, rkw[j].y));
+                dp[1] = bf16x4_to_f32(make_uint2(rkw[j].z, rkw[j].w));
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < V_IT; ++j) {
+            const int i = tid + j * kThreads;
+            const int t = i / L::RB, row = i % L::RB;
+            if (t < nrep && row < nr) rv[t * L::RB + row] = rvw[j];
+        }
+        if (tid < nrep) {
+            rg[tid] = expf(rgw);
+            rbeta[tid] = rbw;
         }
     }
     if (tid == 0) *flag = gdn::mbar_wait_bounded(bar, 0) ? 1 : 0;
