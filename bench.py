@@ -59,8 +59,8 @@ WORKLOAD_TEXT = {
 # DRAM traffic of one gdn_verify launch from an ncu capture (dram__bytes_read.sum + dram__bytes_write.sum)
 # on the full paged256 workload (profiles/dram_verify_paged256.md); reported only while the kernel source
 # is the one that was captured (its digest), otherwise null.
-TRAFFIC = {"gdn_verify": {"src_sha": "70b69e1630cde371", "workload": "paged256",
-                          "bytes_per_launch": 554117376 + 2093926144, "alg_bytes_per_launch": 2709782528}}
+TRAFFIC = {"gdn_verify": {"src_sha": "c5ea7b1d1d40deb8", "workload": "paged256",
+                          "bytes_per_launch": 554074112 + 2094449920, "alg_bytes_per_launch": 2709782528}}
 
 
 def src_digest(path):
