@@ -507,6 +507,7 @@ __global__ void __launch_bounds__(kScanThreads, 1) gdn_chunk_scan_kernel(const P
     uint64_t *bar_ib = reinterpret_cast<uint64_t *>(sm + sc::kMisc + 808);  // P, dec o K, e^G arrived
     uint32_t *tbase = reinterpret_cast<uint32_t *>(sm + sc::kMisc + 776);
     int *flag = reinterpret_cast<int *>(sm + sc::kMisc + 780);
+    int *oflag = reinterpret_cast<int *>(sm + sc::kMisc + 816);  // the Oi wait of the fetching thread
 
     if (warp == 0) tc::tmem_alloc(tbase, sc::kTmemCols);
     if (tid == 0) {
@@ -629,6 +630,15 @@ __global__ void __launch_bounds__(kScanThreads, 1) gdn_chunk_scan_kernel(const P
             break;
         }
         tc::fence_after();
+        // The next chunk's W and Q can land as soon as this chunk's Oi product
+        // is done with W and Q: a second thread waits for it and starts the
+        // fetch while the U split and phase B run.
+        if (tid == 32) {
+            const bool got = gdn::mbar_wait_bounded(bar_o, par_o);
+            *oflag = got ? 1 : 0;
+            if (got && more) scan_fetch_a(a, sm, bar_ia, s0, seq, h, c + 1);
+        }
+        par_o ^= 1u;
         // U^T[arow][t] = Ut[t][arow] - Uacc[arow][t], split into two bf16 parts.
         {
             float v16[16];
@@ -671,13 +681,10 @@ __global__ void __launch_bounds__(kScanThreads, 1) gdn_chunk_scan_kernel(const P
                 }
                 tc::commit(bar_b);
             }
-            good = good && gdn::mbar_wait_bounded(bar_o, par_o);
-            if (good && more) scan_fetch_a(a, sm, bar_ia, s0, seq, h, c + 1);
             good = good && gdn::mbar_wait_bounded(bar_b, par_b);
-            *flag = good ? 1 : 0;
+            *flag = (good && *oflag) ? 1 : 0;
         }
         par_ib ^= 1u;
-        par_o ^= 1u;
         par_b ^= 1u;
         __syncthreads();
         if (*flag == 0) {
