@@ -94,6 +94,9 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float x0, float x1) {
     return d;
 }
 
+// e^x for the gates inside a chunk (x <= 0): 2^(x log2 e).
+__device__ __forceinline__ float gate_exp(float x) { return exp2f(x * 1.4426950408889634f); }
+
 // Two-term bf16 split of 8 consecutive values, packed as two 16-byte chunks.
 __device__ __forceinline__ void split8(const float *x, uint4 &hi, uint4 &lo) {
     uint32_t h[4], l[4];
@@ -259,14 +262,14 @@ __global__ void __launch_bounds__(kThreads) gdn_chunk_wy_kernel(const PrefArgs a
 #pragma unroll
                 for (int x = 0; x < 16; ++x) {
                     const int i = col0 + x;
-                    Af[t * (kC + 1) + i] = (i < t && t < n) ? Bs[t] * expf(Gs[t] - Gs[i]) * v16[x] : 0.f;
+                    Af[t * (kC + 1) + i] = (i < t && t < n) ? Bs[t] * gate_exp(Gs[t] - Gs[i]) * v16[x] : 0.f;
                 }
             } else {
                 float pe[16];
 #pragma unroll
                 for (int x = 0; x < 16; ++x) {
                     const int i = col0 + x;
-                    pe[x] = (i <= t && t < n) ? expf(Gs[t] - Gs[i]) * v16[x] : 0.f;
+                    pe[x] = (i <= t && t < n) ? gate_exp(Gs[t] - Gs[i]) * v16[x] : 0.f;
                 }
 #pragma unroll
                 for (int x = 0; x < 16; x += 8) {
