@@ -328,18 +328,19 @@ class ReplayGraphs:
     A replay transaction has no per-step scalar arguments: everything it
     reads lives in fixed device buffers (the loop's row/slot tables, the
     tokens, the two accept-length buffers that alternate by transaction
-    parity).  With an even number of input sets cycled in order, the input
-    set index i fixes the whole launch sequence of a transaction -- 30 x
-    gdn_verify_replay (this set's rows, the previous set's accepted rows),
-    the greedy accept, and the copy of the row table for the next replay --
-    so each set gets one graph, replayed with a single launch.  The caller
-    uploads the tables and tokens before ``launch`` and reads back after."""
+    parity).  With the input sets cycled in order, transaction s is fixed by
+    s modulo n = lcm(number of sets, 2) -- its input set, the previous
+    transaction's set and the accept-buffer parity -- and so is its whole
+    launch sequence (every layer's gdn_verify_replay, the greedy accept and
+    the copy of the row table for the next replay): each residue gets one
+    graph, replayed with a single launch.  The caller uploads the tables and
+    tokens before ``launch`` and reads back after."""
 
     def __init__(self, rs: ReplayStep, loop: "DecodeLoop", ring_rows: Sequence[Sequence[LayerRows]],
                  ring_logits: Sequence[torch.Tensor], tokens: torch.Tensor):
-        assert len(ring_rows) % 2 == 0, "the accept buffers alternate: use an even number of input sets"
         self.rs, self.loop = rs, loop
-        self.n = len(ring_rows)
+        self.sets = len(ring_rows)
+        self.n = self.sets if self.sets % 2 == 0 else 2 * self.sets
         self.graphs = []
         B = loop.B
         stream = torch.cuda.Stream()
@@ -348,11 +349,11 @@ class ReplayGraphs:
         try:
             for i in range(self.n):
                 rs.prev_acc, rs.accept_len = rs.acc_bufs[(i + 1) % 2], rs.acc_bufs[i % 2]
-                rs.prev_rows = ring_rows[(i - 1) % self.n]
+                rs.prev_rows = ring_rows[(i - 1) % self.sets]
                 g = torch.cuda.CUDAGraph()
                 with torch.cuda.graph(g, stream=stream):
-                    rs._verify_all(B, loop.cu_rows, loop.src_slot, loop.dst_slot, ring_rows[i])
-                    rs.accept(B, loop.cu_rows, ring_logits[i], tokens)
+                    rs._verify_all(B, loop.cu_rows, loop.src_slot, loop.dst_slot, ring_rows[i % self.sets])
+                    rs.accept(B, loop.cu_rows, ring_logits[i % self.sets], tokens)
                     rs.prev_cu.copy_(loop.cu_rows[:B + 1], non_blocking=True)
                 self.graphs.append(g)
         finally:
@@ -360,12 +361,12 @@ class ReplayGraphs:
         torch.cuda.current_stream().wait_stream(stream)
 
     def launch(self, step_no: int, ring_rows: Sequence[Sequence[LayerRows]]):
-        """Transaction number ``step_no`` (its input set is step_no % n)."""
+        """Transaction number ``step_no`` (its input set is step_no modulo the number of sets)."""
         i = step_no % self.n
         rs = self.rs
         rs.prev_acc, rs.accept_len = rs.acc_bufs[(i + 1) % 2], rs.acc_bufs[i % 2]
         self.graphs[i].replay()
-        rs.prev_rows = ring_rows[i]
+        rs.prev_rows = ring_rows[i % self.sets]
         rs.pending = True
 
 

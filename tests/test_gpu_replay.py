@@ -95,13 +95,16 @@ def test_replay_refuses_more_accepted_rows_than_existed(gs, cuda_dev):
     assert not torch.equal(pool[1], before[1])        # request 1 replayed its 2 rows
 
 
-def test_replay_graphs_match_eager_transactions(gs, cuda_dev):
-    """One CUDA graph per input set replays a whole transaction (30 verify
-    launches in the paged workload, 2 here) with identical results."""
+@pytest.mark.parametrize("ring", [4, 3])
+def test_replay_graphs_match_eager_transactions(gs, cuda_dev, ring):
+    """One CUDA graph per transaction residue (input set and accept-buffer
+    parity) replays a whole transaction (30 verify launches in the paged
+    workload, 2 here) with identical results; an odd number of input sets
+    takes twice as many graphs."""
     from speculative_decoding_hybrid_gb300.step import DecodeLoop, LayerRows, ReplayGraphs, ReplayStep
     dims = sy.Dims(4, 8, 128, 128)
     d = gs.dims(dims.h_qk, dims.h_v, dims.d_k, dims.d_v)
-    L, B, num_slots, vocab, ring, steps = 2, 5, 8, 2048, 4, 9
+    L, B, num_slots, vocab, steps = 2, 5, 8, 2048, 9
     cap = B * 4
     init = sy.state(sy.generator(8), (num_slots, L, dims.h_v, dims.d_v, dims.d_k)).to(cuda_dev)
     slots = [0, 1, 2, 3, 4]
@@ -123,6 +126,7 @@ def test_replay_graphs_match_eager_transactions(gs, cuda_dev):
     lg_.plan_step([3] * B)          # the tables the graphs read exist before capture
     lg_.upload_tables()
     graphs = ReplayGraphs(graph, lg_, rows, [x[0] for x in logits], tok_g)
+    assert len(graphs.graphs) == (ring if ring % 2 == 0 else 2 * ring)
     # restart the graph loop's planner state (the capture executed nothing)
     lg_.pool = pools[1] = mk()
     for _ in range(5):
