@@ -103,9 +103,13 @@ __device__ __forceinline__ void cp_async_wait() {
 // wait until the previous grid has finished and its writes are visible.  It
 // comes before a kernel's first global-memory access; in a launch without
 // the attribute the wait returns at once.
-__device__ __forceinline__ void pdl_enter() {
+__device__ __forceinline__ void pdl_launch_dependents() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_enter() {
+    pdl_launch_dependents();
+    pdl_wait();
 }
 
 __device__ __forceinline__ void set_status(uint32_t *status, uint32_t bits) {

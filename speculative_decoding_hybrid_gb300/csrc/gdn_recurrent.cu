@@ -83,6 +83,10 @@ struct RecArgs {
     uint32_t *status;
     int32_t B, h_qk, h_v, dv, row_capacity, grp, bph;
     float q_scale;
+    // The previous launch on the stream writes none of the tables or slots
+    // this one reads (a later layer of a multi-layer call): the tables and
+    // the state tile are read before waiting for that launch to finish.
+    int32_t early;
 };
 
 template <int LPR>
@@ -182,7 +186,8 @@ __global__ void __launch_bounds__(kThreads, 4) gdn_recurrent_kernel(const RecArg
     float *vsm = reinterpret_cast<float *>(smem + (REPLAY ? L::kVOffR : L::kVOff));
     float *gsm = reinterpret_cast<float *>(smem + (REPLAY ? L::kGOffR : L::kGOff));
     float *bsm = gsm + GDN_MAX_ROWS;
-    gdn::pdl_enter();
+    gdn::pdl_launch_dependents();
+    if (!a.early) gdn::pdl_wait();  // otherwise after the tile's copy has started
 
     const int tid = threadIdx.x;
     const int bid = blockIdx.x;
@@ -239,6 +244,7 @@ __global__ void __launch_bounds__(kThreads, 4) gdn_recurrent_kernel(const RecArg
     }
     if (WRITES_SLOT && (dst < 0 || dst >= a.num_slots)) bad |= GDN_DEV_SLOT_OOR;
     if (bad) {
+        if (a.early) gdn::pdl_wait();
         if (lead) {
             gdn::set_status(a.status, bad);
             if (VERIFY) a.ckpt_tag[r] = uint64_t(a.txn) << 32;
@@ -256,6 +262,7 @@ __global__ void __launch_bounds__(kThreads, 4) gdn_recurrent_kernel(const RecArg
         gdn::mbar_arrive_expect_tx(bar, uint32_t(nr) * DK * 4u);
         gdn::bulk_g2s(tile, src_base + tile_off, uint32_t(nr) * DK * 4u, bar);
     }
+    if (a.early) gdn::pdl_wait();  // the rows may come from the previous launch's outputs
 
     // Stage the rows: k and q (this request's qk-head, 16 B per load), the
     // tile's v entries and the gates, and in replay mode the previous
@@ -517,7 +524,7 @@ extern "C" int gdn_decode_step(const gdn_dims *dims, int32_t B, const gdn_bf16 *
     return dispatch<kDecode>(dims->d_k, a, static_cast<cudaStream_t>(stream));
 }
 
-extern "C" int gdn_verify(const gdn_dims *dims, int32_t B, int32_t row_capacity, const int32_t *cu_rows,
+static int gdn_verify_impl(int early, const gdn_dims *dims, int32_t B, int32_t row_capacity, const int32_t *cu_rows,
                           const gdn_bf16 *q, const gdn_bf16 *k, const gdn_bf16 *v, const float *g,
                           const float *beta, const float *pool_layer, int64_t slot_stride, int32_t num_slots,
                           const int32_t *src_slot, float *ckpt_layer, uint64_t *ckpt_tag, uint32_t txn,
@@ -529,6 +536,7 @@ extern "C" int gdn_verify(const gdn_dims *dims, int32_t B, int32_t row_capacity,
     if (!gdn_host::aligned16(ckpt_layer)) return GDN_ERR_ARG;
     if (B == 0) return GDN_OK;
     RecArgs a{};
+    a.early = early;
     a.cu_rows = cu_rows;
     a.q = q;
     a.k = k;
@@ -555,7 +563,7 @@ extern "C" int gdn_verify(const gdn_dims *dims, int32_t B, int32_t row_capacity,
     return dispatch<kVerify>(dims->d_k, a, static_cast<cudaStream_t>(stream));
 }
 
-extern "C" int gdn_verify_at(const gdn_dims *dims, int32_t B, int32_t row_capacity, const int32_t *cu_rows,
+static int gdn_verify_at_impl(int early, const gdn_dims *dims, int32_t B, int32_t row_capacity, const int32_t *cu_rows,
                              const gdn_bf16 *q, const gdn_bf16 *k, const gdn_bf16 *v, const float *g,
                              const float *beta, const float *state_base, int64_t state_elems_total,
                              const int64_t *src_off, float *ckpt_layer, uint64_t *ckpt_tag, uint32_t txn, gdn_bf16 *o,
@@ -572,6 +580,7 @@ extern "C" int gdn_verify_at(const gdn_dims *dims, int32_t B, int32_t row_capaci
         return GDN_ERR_ARG;
     if (B == 0) return GDN_OK;
     RecArgs a{};
+    a.early = early;
     a.cu_rows = cu_rows;
     a.q = q;
     a.k = k;
@@ -597,7 +606,7 @@ extern "C" int gdn_verify_at(const gdn_dims *dims, int32_t B, int32_t row_capaci
     return dispatch<kVerifyAt>(dims->d_k, a, static_cast<cudaStream_t>(stream));
 }
 
-extern "C" int gdn_verify_replay(const gdn_dims *dims, int32_t B, int32_t row_capacity, const int32_t *cu_rows,
+static int gdn_verify_replay_impl(int early, const gdn_dims *dims, int32_t B, int32_t row_capacity, const int32_t *cu_rows,
                                  const gdn_bf16 *q, const gdn_bf16 *k, const gdn_bf16 *v, const float *g,
                                  const float *beta, int32_t prev_capacity, const int32_t *prev_cu_rows,
                                  const int32_t *prev_accept_len, const gdn_bf16 *prev_k, const gdn_bf16 *prev_v,
@@ -612,6 +621,7 @@ extern "C" int gdn_verify_replay(const gdn_dims *dims, int32_t B, int32_t row_ca
     if (!gdn_host::aligned16(prev_k)) return GDN_ERR_ARG;
     if (B == 0) return GDN_OK;
     RecArgs a{};
+    a.early = early;
     a.cu_rows = cu_rows;
     a.q = q;
     a.k = k;
@@ -641,4 +651,94 @@ extern "C" int gdn_verify_replay(const gdn_dims *dims, int32_t B, int32_t row_ca
     a.grp = dims->h_v / dims->h_qk;
     a.q_scale = dims->q_scale;
     return dispatch<kReplay>(dims->d_k, a, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" int gdn_verify(const gdn_dims *dims, int32_t B, int32_t row_capacity, const int32_t *cu_rows,
+                          const gdn_bf16 *q, const gdn_bf16 *k, const gdn_bf16 *v, const float *g,
+                          const float *beta, const float *pool_layer, int64_t slot_stride, int32_t num_slots,
+                          const int32_t *src_slot, float *ckpt_layer, uint64_t *ckpt_tag, uint32_t txn,
+                          gdn_bf16 *o, uint32_t *dev_status, void *stream) {
+    return gdn_verify_impl(0, dims, B, row_capacity, cu_rows, q, k, v, g, beta, pool_layer, slot_stride, num_slots, src_slot, ckpt_layer, ckpt_tag, txn, o, dev_status, stream);
+}
+
+extern "C" int gdn_verify_at(const gdn_dims *dims, int32_t B, int32_t row_capacity, const int32_t *cu_rows,
+                             const gdn_bf16 *q, const gdn_bf16 *k, const gdn_bf16 *v, const float *g,
+                             const float *beta, const float *state_base, int64_t state_elems_total,
+                             const int64_t *src_off, float *ckpt_layer, uint64_t *ckpt_tag, uint32_t txn, gdn_bf16 *o,
+                             uint32_t *dev_status, void *stream) {
+    return gdn_verify_at_impl(0, dims, B, row_capacity, cu_rows, q, k, v, g, beta, state_base, state_elems_total, src_off, ckpt_layer, ckpt_tag, txn, o, dev_status, stream);
+}
+
+extern "C" int gdn_verify_replay(const gdn_dims *dims, int32_t B, int32_t row_capacity, const int32_t *cu_rows,
+                                 const gdn_bf16 *q, const gdn_bf16 *k, const gdn_bf16 *v, const float *g,
+                                 const float *beta, int32_t prev_capacity, const int32_t *prev_cu_rows,
+                                 const int32_t *prev_accept_len, const gdn_bf16 *prev_k, const gdn_bf16 *prev_v,
+                                 const float *prev_g, const float *prev_beta, float *pool_layer, int64_t slot_stride,
+                                 int32_t num_slots, const int32_t *src_slot, const int32_t *dst_slot, gdn_bf16 *o,
+                                 uint32_t *dev_status, void *stream) {
+    return gdn_verify_replay_impl(0, dims, B, row_capacity, cu_rows, q, k, v, g, beta, prev_capacity, prev_cu_rows, prev_accept_len, prev_k, prev_v, prev_g, prev_beta, pool_layer, slot_stride, num_slots, src_slot, dst_slot, o, dev_status, stream);
+}
+
+// Multi-layer issue of the per-layer verify calls: one host call walks the
+// layers in order and makes the same calls a caller would make layer by
+// layer (same kernels, arguments and stream).  A layer after the first
+// follows the previous layer's launch, which writes none of the tables or
+// slots it reads, so it may read those and start its state tile's copy
+// before that launch has finished (the rows still wait for it).
+extern "C" int gdn_verify_layers(const gdn_dims *dims, int32_t num_layers, int32_t B, int32_t row_capacity,
+                                 const int32_t *cu_rows, const gdn_layer_rows *rows, const float *pool,
+                                 int64_t slot_stride, int64_t layer_stride, int32_t num_slots,
+                                 const int32_t *src_slot, float *ckpt, int64_t ckpt_layer_stride,
+                                 uint64_t *ckpt_tag, uint32_t txn, gdn_bf16 *o, int64_t o_layer_stride,
+                                 uint32_t *dev_status, void *stream) {
+    if (num_layers < 0) return GDN_ERR_ARG;
+    if (num_layers > 0 && (!rows || !pool || !ckpt || !ckpt_tag || !o)) return GDN_ERR_NULL;
+    for (int32_t l = 0; l < num_layers; ++l) {
+        const gdn_layer_rows &x = rows[l];
+        const int st = gdn_verify_impl(l > 0, dims, B, row_capacity, cu_rows, x.q, x.k, x.v, x.g, x.beta,
+                                  pool + int64_t(l) * layer_stride, slot_stride, num_slots, src_slot,
+                                  ckpt + int64_t(l) * ckpt_layer_stride, ckpt_tag + int64_t(l) * B, txn,
+                                  o + int64_t(l) * o_layer_stride, dev_status, stream);
+        if (st != GDN_OK) return st;
+    }
+    return GDN_OK;
+}
+
+extern "C" int gdn_verify_replay_layers(const gdn_dims *dims, int32_t num_layers, int32_t B, int32_t row_capacity,
+                                        const int32_t *cu_rows, const gdn_layer_rows *rows, int32_t prev_capacity,
+                                        const int32_t *prev_cu_rows, const int32_t *prev_accept_len,
+                                        const gdn_layer_rows *prev_rows, float *pool, int64_t slot_stride,
+                                        int64_t layer_stride, int32_t num_slots, const int32_t *src_slot,
+                                        const int32_t *dst_slot, gdn_bf16 *o, int64_t o_layer_stride,
+                                        uint32_t *dev_status, void *stream) {
+    if (num_layers < 0) return GDN_ERR_ARG;
+    if (num_layers > 0 && (!rows || !prev_rows || !pool || !o)) return GDN_ERR_NULL;
+    for (int32_t l = 0; l < num_layers; ++l) {
+        const gdn_layer_rows &x = rows[l];
+        const gdn_layer_rows &p = prev_rows[l];
+        const int st = gdn_verify_replay_impl(l > 0, dims, B, row_capacity, cu_rows, x.q, x.k, x.v, x.g, x.beta, prev_capacity,
+                                         prev_cu_rows, prev_accept_len, p.k, p.v, p.g, p.beta,
+                                         pool + int64_t(l) * layer_stride, slot_stride, num_slots, src_slot, dst_slot,
+                                         o + int64_t(l) * o_layer_stride, dev_status, stream);
+        if (st != GDN_OK) return st;
+    }
+    return GDN_OK;
+}
+
+extern "C" int gdn_verify_at_layers(const gdn_dims *dims, int32_t num_layers, int32_t B, int32_t row_capacity,
+                                    const int32_t *cu_rows, const gdn_layer_rows *rows, const float *state_base,
+                                    int64_t state_elems_total, const int64_t *src_off, float *ckpt,
+                                    int64_t ckpt_layer_stride, uint64_t *ckpt_tag, uint32_t txn, gdn_bf16 *o,
+                                    int64_t o_layer_stride, uint32_t *dev_status, void *stream) {
+    if (num_layers < 0) return GDN_ERR_ARG;
+    if (num_layers > 0 && (!rows || !src_off || !ckpt || !ckpt_tag || !o)) return GDN_ERR_NULL;
+    for (int32_t l = 0; l < num_layers; ++l) {
+        const gdn_layer_rows &x = rows[l];
+        const int st = gdn_verify_at_impl(l > 0, dims, B, row_capacity, cu_rows, x.q, x.k, x.v, x.g, x.beta, state_base,
+                                     state_elems_total, src_off + int64_t(l) * B,
+                                     ckpt + int64_t(l) * ckpt_layer_stride, ckpt_tag + int64_t(l) * B, txn,
+                                     o + int64_t(l) * o_layer_stride, dev_status, stream);
+        if (st != GDN_OK) return st;
+    }
+    return GDN_OK;
 }
