@@ -54,8 +54,11 @@ struct PrefArgs {
 // Operand tiles are 128-byte-swizzled K-major bf16 tiles (tc.cuh); "parts"
 // are the two-term bf16 split x = x1 + x2, x1 = bf16(x), x2 = bf16(x - x1).
 namespace blob {
-constexpr uint32_t kW1 = 0, kW2 = 16384;     // W = T diag(beta e^G) K parts: 64 rows (t) x 128 (d_k)
-constexpr uint32_t kQ = 32768;               // Q (exact bf16):               64 rows (t) x 128 (d_k)
+// [W1; Q]: W's high part (rows 0..63) stacked on Q (exact bf16, rows 64..127),
+// one 128-row tile (atoms 16 KB apart) so that one N = 128 product gives
+// S W1^T and S Q^T together; W's low part W2 is a 64-row tile.
+constexpr uint32_t kW1Q = 0;                 // 128 rows (t, then t) x 128 (d_k)
+constexpr uint32_t kW2 = 32768;              // 64 rows (t) x 128 (d_k)
 constexpr uint32_t kP1 = 49152, kP2 = 57344; // P = M o Q K^T parts:         64 rows (t) x  64 (i)
 constexpr uint32_t kK1 = 65536, kK2 = 81920; // dec o K parts, MN-major B:  64 rows (i) x 128 (d_k)
 constexpr uint32_t kTiles = 98304;           // bytes of operand tiles (one contiguous block)
@@ -417,12 +420,12 @@ __global__ void __launch_bounds__(kThreads) gdn_chunk_wy_kernel(const PrefArgs a
     if (tid == 0) {
         if (ok) {
             // Q tile (rows 64..127 of both A1 atoms), P, W and Ut parts.
-            gdn::bulk_s2g(out + blob::kQ, sm + wy::kA1 + 8192, 8192u);
-            gdn::bulk_s2g(out + blob::kQ + 8192, sm + wy::kA1 + 16384 + 8192, 8192u);
+            gdn::bulk_s2g(out + blob::kW1Q + 8192, sm + wy::kA1 + 8192, 8192u);           // Q, atom 0
+            gdn::bulk_s2g(out + blob::kW1Q + 16384 + 8192, sm + wy::kA1 + 16384 + 8192, 8192u);  // Q, atom 1
             gdn::bulk_s2g(out + blob::kP1, sm + wy::kStP1, 8192u);
             gdn::bulk_s2g(out + blob::kP2, sm + wy::kStP2, 8192u);
             for (int at = 0; at < 2; ++at) {
-                gdn::bulk_s2g(out + blob::kW1 + at * 8192, sm + wy::st_w1(at), 8192u);
+                gdn::bulk_s2g(out + blob::kW1Q + at * 16384, sm + wy::st_w1(at), 8192u);
                 gdn::bulk_s2g(out + blob::kW2 + at * 8192, sm + wy::st_w2(at), 8192u);
             }
             gdn::bulk_s2g(out + blob::kUt, sm + wy::kStUt, 16384u);
@@ -453,7 +456,7 @@ __global__ void __launch_bounds__(kThreads) gdn_chunk_wy_kernel(const PrefArgs a
 namespace sc {
 constexpr uint32_t kS1 = 0, kS2 = 32768;  // S parts       128 rows (d_v) x 128 (d_k)
 constexpr uint32_t kTiles = 65536;        // the chunk's W, Q, P and dec o K tiles, in the workspace layout
-constexpr uint32_t kW1 = kTiles + blob::kW1, kW2 = kTiles + blob::kW2, kQ = kTiles + blob::kQ;
+constexpr uint32_t kW1Q = kTiles + blob::kW1Q, kW2 = kTiles + blob::kW2;
 constexpr uint32_t kP1 = kTiles + blob::kP1, kP2 = kTiles + blob::kP2;
 constexpr uint32_t kK1 = kTiles + blob::kK1, kK2 = kTiles + blob::kK2;
 constexpr uint32_t kU1 = kTiles + blob::kTiles, kU2 = kU1 + 16384;  // U^T parts 128 rows (d_v) x 64 (i)
@@ -558,41 +561,35 @@ __global__ void __launch_bounds__(kScanThreads, 1) gdn_chunk_scan_kernel(const P
     const uint32_t tm = *tbase;
     constexpr uint32_t id64 = tc::idesc_bf16(128, 64);
     constexpr uint32_t id128 = tc::idesc_bf16(128, 128);
-    // Tensor-memory columns: Uacc 0..63, dS 256..383, and Oi / Oa of chunk c
-    // in buffer c % 2 (the outputs of chunk c are read while chunk c + 1's
-    // first products run).
+    // Tensor-memory columns: dS 256..383, and for chunk c in buffer c % 2
+    // [Uacc | Oi] (128 columns) and Oa (the outputs of chunk c are read while
+    // chunk c + 1's first products run): buffer 0 at 0..127 and 128..191,
+    // buffer 1 at 384..511 and 192..255.
     const uint64_t dsc = tc::smem_desc(sb);  // descriptors of the fixed tiles: tc::desc_at(dsc, offset)
     const uint64_t dsc_k = tc::smem_desc_mn(sb + sc::kK1, 8192);  // dec o K parts, MN-major B (K2 at +16 KB)
     constexpr uint32_t id128k = id128 | tc::kBMnMajor;
-    auto oi_col = [](int b) { return uint32_t(64 + 128 * b); };
-    auto oa_col = [](int b) { return uint32_t(128 + 256 * b); };
-    // Phase A of chunk c (thread 0): Uacc = S W^T, committed to bar_u, then
-    // Oi = S Q^T (finished before phase B's commit fires).
+    auto uo_col = [](int b) { return uint32_t(384 * b); };  // Uacc at +0, Oi at +64
+    auto oi_col = [](int b) { return uint32_t(384 * b + 64); };
+    auto oa_col = [](int b) { return uint32_t(128 + 64 * b); };
+    // Phase A of chunk c (thread 0): [Uacc | Oi] = S [W1; Q]^T (N = 128) for
+    // both parts of S, plus S1 W2^T into Uacc (N = 64); committed to bar_u and
+    // bar_o (W and Q are then free for the next chunk's fetch).
     auto issue_phase_a = [&](int c) {
         tc::fence_after();
+        const uint32_t d = tm + uo_col(c & 1);
 #pragma unroll
         for (int at = 0; at < 2; ++at)
 #pragma unroll
             for (int s = 0; s < 4; ++s) {
-                const uint32_t ka = at * 16384 + s * 32, kb = at * 8192 + s * 32;
+                const uint32_t ka = at * 16384 + s * 32;
                 const uint64_t a1 = tc::desc_at(dsc, sc::kS1 + ka), a2 = tc::desc_at(dsc, sc::kS2 + ka);
-                const uint64_t w1 = tc::desc_at(dsc, sc::kW1 + kb), w2 = tc::desc_at(dsc, sc::kW2 + kb);
-                tc::mma_bf16(tm, a1, w1, id64, (at | s) ? 1u : 0u);
-                tc::mma_bf16(tm, a1, w2, id64, 1u);
-                tc::mma_bf16(tm, a2, w1, id64, 1u);
+                const uint64_t wq = tc::desc_at(dsc, sc::kW1Q + ka);
+                const uint64_t w2 = tc::desc_at(dsc, sc::kW2 + at * 8192 + s * 32);
+                tc::mma_bf16(d, a1, wq, id128, (at | s) ? 1u : 0u);
+                tc::mma_bf16(d, a1, w2, id64, 1u);
+                tc::mma_bf16(d, a2, wq, id128, 1u);
             }
         tc::commit(bar_u);
-        const uint32_t oi = tm + oi_col(c & 1);
-#pragma unroll
-        for (int at = 0; at < 2; ++at)
-#pragma unroll
-            for (int s = 0; s < 4; ++s) {
-                const uint32_t ka = at * 16384 + s * 32, kb = at * 8192 + s * 32;
-                const uint64_t a1 = tc::desc_at(dsc, sc::kS1 + ka), a2 = tc::desc_at(dsc, sc::kS2 + ka);
-                const uint64_t qd = tc::desc_at(dsc, sc::kQ + kb);
-                tc::mma_bf16(oi, a1, qd, id64, (at | s) ? 1u : 0u);
-                tc::mma_bf16(oi, a2, qd, id64, 1u);
-            }
         tc::commit(bar_o);
     };
     // Per-thread Ut values of chunk c: Ut[t][arow] for t in [16cq, 16cq+16).
@@ -646,7 +643,7 @@ __global__ void __launch_bounds__(kScanThreads, 1) gdn_chunk_scan_kernel(const P
         {
             float v16[16];
             const int col0 = 16 * cq;
-            tc::ld16(tm + lane_base + uint32_t(col0), v16);
+            tc::ld16(tm + lane_base + uo_col(c & 1) + uint32_t(col0), v16);
 #pragma unroll
             for (int x = 0; x < 16; x += 8) {
                 float u[8];
