@@ -59,8 +59,8 @@ WORKLOAD_TEXT = {
 # DRAM traffic of one gdn_verify launch from an ncu capture (dram__bytes_read.sum + dram__bytes_write.sum)
 # on the full paged256 workload (profiles/dram_verify_paged256.md); reported only while the kernel source
 # is the one that was captured (its digest), otherwise null.
-TRAFFIC = {"gdn_verify": {"src_sha": "c5ea7b1d1d40deb8", "workload": "paged256",
-                          "bytes_per_launch": 554074112 + 2094449920, "alg_bytes_per_launch": 2709782528}}
+TRAFFIC = {"gdn_verify": {"src_sha": "3fdbecb81ca3fcf0", "workload": "paged256",
+                          "bytes_per_launch": 554256384 + 2094016512, "alg_bytes_per_launch": 2709782528}}
 
 
 def src_digest(path):
@@ -590,13 +590,20 @@ def run_e2e(b: Bench, host, stages, steps, warmup):
             done[slot].record(copy_stream)
         moved_bytes[0] += hb.numel()
 
-    def one(slot):
+    marks = []   # (start, end) events of the timed steps on the compute stream
+
+    def one(slot, mark=False):
         compute.wait_event(done[slot])
         _, rows, logits = stages[slot]
         b.rows = [rows] * spec.ring
         b.logits = [logits] * spec.ring
+        if mark:
+            marks.append((torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)))
+            marks[-1][0].record(compute)
         p = b.launch()
         free[slot].record(compute)
+        if mark:
+            marks[-1][1].record(compute)
         issue_copy(b.step_no + 1, slot ^ 1)       # next step's inputs, overlapped
         return b.finish(p)                        # the step's one readback
 
@@ -613,7 +620,7 @@ def run_e2e(b: Bench, host, stages, steps, warmup):
         t0 = time.perf_counter()
         tok = 0
         for _ in range(steps):
-            n, p = one(slot)
+            n, p = one(slot, mark=True)
             slot ^= 1
             tok += n
         torch.cuda.synchronize()
@@ -628,9 +635,13 @@ def run_e2e(b: Bench, host, stages, steps, warmup):
         cb.record(copy_stream)
     torch.cuda.synchronize()
     copy_ms = ca.elapsed_time(cb)
+    # device idle time between a step's last kernel and the next step's first
+    # (the host's readback, planning and launch of the next step)
+    gaps = [marks[i][1].elapsed_time(marks[i + 1][0]) for i in range(len(marks) - 1)]
+    gap_ms = sum(gaps) / len(gaps) if gaps else 0.0
     h2d = moved_bytes[0] / steps + (b.loop.B + 1) * 3 * 4 + b.cap * 4   # inputs + tables + tokens
     d2h = (2 * spec.batch + b.cap) * 4
-    return tok / dt, h2d, d2h, copy_ms
+    return tok / dt, h2d, d2h, copy_ms, gap_ms
 
 
 # ---------------------------------------------------------------------------
@@ -813,7 +824,7 @@ def main():
     e2e = None
     if not args.no_e2e:
         host, stages = stage_e2e(b)
-        val, h2d, d2h, copy_ms = run_e2e(b, host, stages, args.e2e_steps, 3)
+        val, h2d, d2h, copy_ms, gap_ms = run_e2e(b, host, stages, args.e2e_steps, 3)
         del host, stages
         if world > 1:
             t = torch.tensor([val], device=dev, dtype=torch.float64)
@@ -821,7 +832,8 @@ def main():
             val = float(t.item())
         e2e = {"value": val, "unit": "verified tokens/s", "h2d_bytes_per_step": int(h2d),
                "d2h_bytes_per_step": int(d2h), "steps": args.e2e_steps,
-               "input_copy_ms_alone": copy_ms, "input_copy_gbs": h2d / (copy_ms * 1e-3) / 1e9}
+               "input_copy_ms_alone": copy_ms, "input_copy_gbs": h2d / (copy_ms * 1e-3) / 1e9,
+               "device_idle_ms_between_steps": gap_ms}
 
     if rank != 0:
         if world > 1:
