@@ -352,7 +352,10 @@ int gdn_verify_replay_layers(const gdn_dims *dims, int32_t num_layers, int32_t B
  * token and publishes only its final state to dst_slot[i].  chunk = 64.
  * Work is ordered on `stream`, so a decode/verify queued after it on the
  * same stream reads the published state ([NATIVE] What changed).
- * max_seqlen (host) bounds every sequence's length.
+ * max_seqlen (host, >= 0) is accepted for callers that track it; every
+ * length is read from cu_seqlens on the device.
+ * Workspace (gdn_prefill_workspace_bytes): 128.25 KB per (chunk slot, v-head)
+ * for ceil(row_capacity / 64) + nseq chunk slots, plus small tables.
  */
 size_t gdn_prefill_workspace_bytes(const gdn_dims *dims, int32_t nseq, int32_t row_capacity);
 int gdn_chunked_prefill(const gdn_dims *dims, int32_t nseq, int32_t row_capacity,

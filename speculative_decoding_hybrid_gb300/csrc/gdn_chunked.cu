@@ -35,7 +35,7 @@ __device__ __forceinline__ int chunk_slot(int seq_start, int c, int seq) { retur
 
 struct PrefArgs {
     const int32_t *cu;
-    int32_t nseq, h_qk, h_v, grp, max_chunks, row_capacity, num_slots;
+    int32_t nseq, h_qk, h_v, grp, row_capacity, num_slots;
     const uint16_t *q, *k, *v;
     const float *g, *beta;
     float *pool;
@@ -43,7 +43,8 @@ struct PrefArgs {
     const int32_t *src_slot, *dst_slot;
     uint16_t *o;
     float *ws;             // per (chunk slot, v-head) blobs, see namespace blob
-    const int32_t *order;  // sequences by decreasing length (written by gdn_seq_order_kernel)
+    const int32_t *order;      // sequences by decreasing length (written by gdn_prefill_tables_kernel)
+    const int32_t *chunk_seq;  // per chunk slot: its sequence, or -1 (same kernel)
     float q_scale;
     uint32_t *status;
 };
@@ -123,7 +124,7 @@ __device__ __forceinline__ void split8(const float *x, uint4 &hi, uint4 &lo) {
 //                 blocks 16 KB apart), so no transposed copy is needed
 //   AB   [T diag(beta e^G); T diag(beta)], hi and lo parts,
 //                 128 rows (t, twice) x 64 (i), K-major                2 x 16 KB
-//   (the fp32 matrix A -> T, [64][65], lives in the AB area before those
+//   (the fp32 matrix A -> T, [64][68], lives in the AB area before those
 //    tiles are written)
 //   misc G, beta, e^G, mbarrier, tensor-memory base, flag, dec
 // Outputs are staged and leave by bulk copies issued at the very end (stores
@@ -144,6 +145,7 @@ constexpr uint32_t kStP1 = kVN + 8192, kStP2 = kVN + 16384 + 8192;
 __device__ __forceinline__ uint32_t st_w1(int atom) { return kA1 + 16384u * uint32_t(atom); }
 __device__ __forceinline__ uint32_t st_w2(int atom) { return kVN + 16384u * uint32_t(atom); }
 constexpr uint32_t kStUt = kT;  // 32 KB
+constexpr int kAs = 68;         // row stride (floats) of the fp32 matrix A -> T: 16-byte rows, no bank conflicts
 constexpr size_t kSmem = kMisc + 2048 + 1024;  // + alignment slack
 constexpr uint32_t kTmemCols = 256;
 }  // namespace wy
@@ -155,14 +157,16 @@ constexpr uint32_t kTmemCols = 256;
 __host__ __device__ constexpr int ut_index(int t, int j) { return t * kD + ((((j >> 2) ^ (t & 7))) << 2) + (j & 3); }
 
 __global__ void __launch_bounds__(kThreads) gdn_chunk_wy_kernel(const PrefArgs a) {
-    const int seq = blockIdx.x / a.max_chunks;
-    const int c = blockIdx.x % a.max_chunks;
+    // One CTA per chunk slot and v-head; slots that hold no chunk exit.
+    const int seq = a.chunk_seq[blockIdx.x];
+    if (seq < 0) return;
     const int h = blockIdx.y;
     const int s0 = a.cu[seq];
     const int s1 = a.cu[seq + 1];
     const int len = s1 - s0;
     if (s0 < 0 || len < 0 || s1 > a.row_capacity) return;  // reported by the scan kernel
-    if (c * kC >= len) return;
+    const int c = int(blockIdx.x) - seq - s0 / kC;         // inverse of chunk_slot
+    if (c < 0 || c * kC >= len) return;
     const int t0 = s0 + c * kC;
     const int n = min(kC, len - c * kC);
     const int hq = h / a.grp;
@@ -263,9 +267,14 @@ __global__ void __launch_bounds__(kThreads) gdn_chunk_wy_kernel(const PrefArgs a
             tc::ld16(tm + (uint32_t(32 * q4) << 16) + uint32_t(col0), v16);
             if (q4 < 2) {
 #pragma unroll
-                for (int x = 0; x < 16; ++x) {
-                    const int i = col0 + x;
-                    Af[t * (kC + 1) + i] = (i < t && t < n) ? Bs[t] * gate_exp(Gs[t] - Gs[i]) * v16[x] : 0.f;
+                for (int x = 0; x < 16; x += 4) {
+                    float av[4];
+#pragma unroll
+                    for (int y = 0; y < 4; ++y) {
+                        const int i = col0 + x + y;
+                        av[y] = (i < t && t < n) ? Bs[t] * gate_exp(Gs[t] - Gs[i]) * v16[x + y] : 0.f;
+                    }
+                    *reinterpret_cast<float4 *>(Af + t * wy::kAs + col0 + x) = make_float4(av[0], av[1], av[2], av[3]);
                 }
             } else {
                 float pe[16];
@@ -306,35 +315,66 @@ __global__ void __launch_bounds__(kThreads) gdn_chunk_wy_kernel(const PrefArgs a
             *reinterpret_cast<uint4 *>(out + blob::kK1 + e * 16) = hi;
             *reinterpret_cast<uint4 *>(out + blob::kK2 + e * 16) = lo;
         }
-        // T = (I + A)^{-1} by forward substitution, column by column: T[t][j]
-        // = delta_tj - sum_{i<t} A[t][i] T[i][j].  Four threads own a column j
-        // (rows 4m + q, m = 0..15); when row t is final its owner broadcasts
-        // T[t][j] to the other three, and every thread adds A[r][t] T[t][j] to
-        // the running sums of its later rows r (A is 0 on and above the diagonal).
+        // T = (I + A)^{-1} by forward substitution, column by column, four
+        // pivot rows at a time: T[t][j] = delta_tj - sum_{i<t} A[t][i] T[i][j].
+        // Four threads own a column j (rows 4m + q, m = 0..15) and keep the
+        // running sums p of their rows.  For pivot rows 4 tau .. 4 tau + 3 the
+        // owners' right-hand sides b = delta - p go to all four threads, which
+        // solve the unit lower-triangular 4 x 4 diagonal block of (I + A) in
+        // closed form (D = its inverse) and add A[r][4 tau .. 4 tau + 3] v to
+        // the sums of their later rows r.  Pivots above a warp's first column
+        // give zeros and are skipped; column blocks are assigned so that the
+        // two warps sharing a scheduler (w, w + 4) have the same number of steps.
         {
-            const int j = tid >> 2, q = tid & 3;
+            const int cb = warp < 4 ? warp : 11 - warp;
+            const int j = 8 * cb + (lane >> 2), q = lane & 3;
+            const int base = lane & ~3;
             float p[16];
 #pragma unroll
             for (int m = 0; m < 16; ++m) p[m] = 0.f;
 #pragma unroll
-            for (int t = 0; t < kC; ++t) {
-                const int mt = t >> 2;
-                float v = t == j ? 1.f : (t > j ? -p[mt] : 0.f);  // meaningful in the owner's lane
-                v = __shfl_sync(0xffffffffu, v, (lane & ~3) | (t & 3));
-                if (q == (t & 3)) p[mt] = v;
+            for (int tau = 0; tau < 16; ++tau) {
+                if (tau >= 2 * cb) {
+                    const float4 a1 = *reinterpret_cast<const float4 *>(Af + (4 * tau + 1) * wy::kAs + 4 * tau);
+                    const float4 a2 = *reinterpret_cast<const float4 *>(Af + (4 * tau + 2) * wy::kAs + 4 * tau);
+                    const float4 a3 = *reinterpret_cast<const float4 *>(Af + (4 * tau + 3) * wy::kAs + 4 * tau);
+                    const float d10 = -a1.x, d21 = -a2.y, d32 = -a3.z;
+                    const float d20 = -fmaf(a2.y, d10, a2.x);
+                    const float d31 = -fmaf(a3.z, d21, a3.y);
+                    const float d30 = -fmaf(a3.z, d20, fmaf(a3.y, d10, a3.x));
+                    const float bq = (4 * tau + q == j ? 1.f : 0.f) - p[tau];
+                    const float b0 = __shfl_sync(0xffffffffu, bq, base);
+                    const float b1 = __shfl_sync(0xffffffffu, bq, base | 1);
+                    const float b2 = __shfl_sync(0xffffffffu, bq, base | 2);
+                    const float b3 = __shfl_sync(0xffffffffu, bq, base | 3);
+                    const float v0 = b0;
+                    const float v1 = fmaf(d10, b0, b1);
+                    const float v2 = fmaf(d21, b1, fmaf(d20, b0, b2));
+                    const float v3 = fmaf(d32, b2, fmaf(d31, b1, fmaf(d30, b0, b3)));
+                    p[tau] = q == 0 ? v0 : (q == 1 ? v1 : (q == 2 ? v2 : v3));
 #pragma unroll
-                for (int m = mt; m < 16; ++m) p[m] = fmaf(Af[(4 * m + q) * (kC + 1) + t], v, p[m]);
+                    for (int m = tau + 1; m < 16; ++m) {
+                        const float4 am = *reinterpret_cast<const float4 *>(Af + (4 * m + q) * wy::kAs + 4 * tau);
+                        p[m] = fmaf(am.w, v3, fmaf(am.z, v2, fmaf(am.y, v1, fmaf(am.x, v0, p[m]))));
+                    }
+                }
             }
             __syncthreads();  // every A entry is read before T overwrites it
 #pragma unroll
-            for (int m = 0; m < 16; ++m) Af[(4 * m + q) * (kC + 1) + j] = p[m];
+            for (int m = 0; m < 16; ++m) Af[(4 * m + q) * wy::kAs + j] = p[m];
         }
         __syncthreads();
         // AB rows t: T diag(beta e^G); rows 64 + t: T diag(beta); hi and lo parts.
         const int t = tid >> 2, i0 = (tid & 3) * 16;
         float tv[16];
 #pragma unroll
-        for (int x = 0; x < 16; ++x) tv[x] = Af[t * (kC + 1) + i0 + x];
+        for (int x = 0; x < 16; x += 4) {
+            const float4 tr = *reinterpret_cast<const float4 *>(Af + t * wy::kAs + i0 + x);
+            tv[x] = tr.x;
+            tv[x + 1] = tr.y;
+            tv[x + 2] = tr.z;
+            tv[x + 3] = tr.w;
+        }
         __syncthreads();  // every T entry is read before the tiles overwrite it
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
@@ -744,8 +784,13 @@ __global__ void __launch_bounds__(kScanThreads, 1) gdn_chunk_scan_kernel(const P
 }
 
 // order[r] = the sequence with the r-th largest length (ties by index), so
-// that the scan's longest dependency chains are scheduled in its first wave.
-__global__ void gdn_seq_order_kernel(const int32_t *cu, int nseq, int32_t *order) {
+// that the scan's longest dependency chains are scheduled in its first wave;
+// chunk_seq[x] = the sequence whose chunk sits in workspace slot x (-1 for
+// none), so that the per-chunk kernel's grid covers only the slot range.
+// One block: sequences that fail the scan's row checks get no chunks.
+__global__ void gdn_prefill_tables_kernel(const int32_t *cu, int nseq, int row_capacity, int nslots,
+                                          int32_t *order, int32_t *chunk_seq) {
+    for (int x = threadIdx.x; x < nslots; x += blockDim.x) chunk_seq[x] = -1;
     for (int i = threadIdx.x; i < nseq; i += blockDim.x) {
         const int li = cu[i + 1] - cu[i];
         int r = 0;
@@ -755,6 +800,14 @@ __global__ void gdn_seq_order_kernel(const int32_t *cu, int nseq, int32_t *order
         }
         order[r] = i;
     }
+    __syncthreads();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
+    for (int i = warp; i < nseq; i += nwarps) {
+        const int s0 = cu[i], s1 = cu[i + 1];
+        if (s0 < 0 || s1 < s0 || s1 > row_capacity) continue;
+        const int nch = (s1 - s0 + kC - 1) / kC;
+        for (int c = lane; c < nch; c += 32) chunk_seq[chunk_slot(s0, c, i)] = i;
+    }
 }
 
 constexpr size_t kWySmem = wy::kSmem;
@@ -762,14 +815,23 @@ constexpr size_t kScanSmem = sc::kSmem;
 
 }  // namespace
 
-static size_t blobs_bytes(const gdn_dims *dims, int32_t nseq, int32_t row_capacity) {
-    const size_t slots = size_t((row_capacity + kC - 1) / kC) + size_t(nseq);
-    return slots * size_t(dims->h_v) * kWsFloats * sizeof(float);
+// Chunk slots: sequence i's chunk c uses slot chunk_slot(cu[i], c, i), which
+// is below ceil(row_capacity / 64) + nseq for every valid sequence.
+static size_t chunk_slots(int32_t nseq, int32_t row_capacity) {
+    return size_t((int64_t(row_capacity) + kC - 1) / kC) + size_t(nseq);
 }
 
+static size_t blobs_bytes(const gdn_dims *dims, int32_t nseq, int32_t row_capacity) {
+    return chunk_slots(nseq, row_capacity) * size_t(dims->h_v) * kWsFloats * sizeof(float);
+}
+
+static size_t align16(size_t x) { return (x + 15) / 16 * 16; }
+
+// Workspace: the blobs, then order[nseq], then chunk_seq[slots].
 extern "C" size_t gdn_prefill_workspace_bytes(const gdn_dims *dims, int32_t nseq, int32_t row_capacity) {
     if (!dims || nseq < 0 || row_capacity < 0) return 0;
-    return blobs_bytes(dims, nseq, row_capacity) + (size_t(nseq) * 4 + 15) / 16 * 16;
+    return blobs_bytes(dims, nseq, row_capacity) + align16(size_t(nseq) * 4) +
+           align16(chunk_slots(nseq, row_capacity) * 4);
 }
 
 extern "C" int gdn_chunked_prefill(const gdn_dims *dims, int32_t nseq, int32_t row_capacity,
@@ -801,7 +863,6 @@ extern "C" int gdn_chunked_prefill(const gdn_dims *dims, int32_t nseq, int32_t r
     a.h_qk = dims->h_qk;
     a.h_v = dims->h_v;
     a.grp = dims->h_v / dims->h_qk;
-    a.max_chunks = (max_seqlen + kC - 1) / kC;
     a.row_capacity = row_capacity;
     a.num_slots = num_slots;
     a.q = q;
@@ -815,9 +876,11 @@ extern "C" int gdn_chunked_prefill(const gdn_dims *dims, int32_t nseq, int32_t r
     a.dst_slot = dst_slot;
     a.o = o;
     a.ws = static_cast<float *>(workspace);
-    int32_t *order = reinterpret_cast<int32_t *>(static_cast<unsigned char *>(workspace) +
-                                                 blobs_bytes(dims, nseq, row_capacity));
+    unsigned char *tables = static_cast<unsigned char *>(workspace) + blobs_bytes(dims, nseq, row_capacity);
+    int32_t *order = reinterpret_cast<int32_t *>(tables);
+    int32_t *chunk_seq = reinterpret_cast<int32_t *>(tables + align16(size_t(nseq) * 4));
     a.order = order;
+    a.chunk_seq = chunk_seq;
     a.q_scale = dims->q_scale;
     a.status = dev_status;
     if (cudaFuncSetAttribute(gdn_chunk_wy_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kWySmem)) !=
@@ -825,14 +888,12 @@ extern "C" int gdn_chunked_prefill(const gdn_dims *dims, int32_t nseq, int32_t r
         cudaFuncSetAttribute(gdn_chunk_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kScanSmem)) !=
             cudaSuccess)
         return GDN_ERR_CUDA;
-    gdn_seq_order_kernel<<<1, nseq < 1024 ? (nseq + 31) / 32 * 32 : 1024, 0, st>>>(cu_seqlens, nseq, order);
+    const size_t slots = chunk_slots(nseq, row_capacity);
+    if (slots > 0x7fffffffULL || dims->h_v > 65535) return GDN_ERR_ARG;
+    gdn_prefill_tables_kernel<<<1, 1024, 0, st>>>(cu_seqlens, nseq, row_capacity, int(slots), order, chunk_seq);
     if (cudaGetLastError() != cudaSuccess) return GDN_ERR_CUDA;
-    if (a.max_chunks > 0) {
-        const long long gx = (long long)nseq * a.max_chunks;
-        if (gx > 0x7fffffffLL || dims->h_v > 65535) return GDN_ERR_ARG;
-        gdn_chunk_wy_kernel<<<dim3(unsigned(gx), dims->h_v), kThreads, kWySmem, st>>>(a);
-        if (cudaGetLastError() != cudaSuccess) return GDN_ERR_CUDA;
-    }
+    gdn_chunk_wy_kernel<<<dim3(unsigned(slots), dims->h_v), kThreads, kWySmem, st>>>(a);
+    if (cudaGetLastError() != cudaSuccess) return GDN_ERR_CUDA;
     const long long gs = (long long)nseq * dims->h_v;
     gdn_chunk_scan_kernel<<<unsigned(gs), kScanThreads, kScanSmem, st>>>(a);
     return gdn_host::launch_status(cudaGetLastError());
