@@ -21,6 +21,8 @@
 // Sequence i's chunks start at cu_seqlens[i]; chunk c of sequence i uses
 // workspace slot (cu_seqlens[i] + 64c)/64 + i, unique and below
 // ceil(row_capacity/64) + nseq.
+#include <cuda.h>
+
 #include "common.cuh"
 #include "tc.cuh"
 
@@ -47,6 +49,10 @@ struct PrefArgs {
     const int32_t *chunk_seq;  // per chunk slot: its sequence, or -1 (same kernel)
     float q_scale;
     uint32_t *status;
+    // q, k (rows x h_qk x 128) and v (rows x h_v x 128) as 3-D bf16 tensors
+    // for the copy engine: boxes of 64 columns x 1 head x 64 rows, 128-byte
+    // swizzle, zero fill past row_capacity
+    CUtensorMap tm_q, tm_k, tm_v;
 };
 
 // Workspace per (chunk slot, v-head): everything the scan needs for one chunk,
@@ -156,7 +162,7 @@ constexpr uint32_t kTmemCols = 256;
 // still reads 32 consecutive values of one row from one segment.
 __host__ __device__ constexpr int ut_index(int t, int j) { return t * kD + ((((j >> 2) ^ (t & 7))) << 2) + (j & 3); }
 
-__global__ void __launch_bounds__(kThreads) gdn_chunk_wy_kernel(const PrefArgs a) {
+__global__ void __launch_bounds__(kThreads) gdn_chunk_wy_kernel(const __grid_constant__ PrefArgs a) {
     // One CTA per chunk slot and v-head; slots that hold no chunk exit.
     const int seq = a.chunk_seq[blockIdx.x];
     if (seq < 0) return;
@@ -186,40 +192,41 @@ __global__ void __launch_bounds__(kThreads) gdn_chunk_wy_kernel(const PrefArgs a
     int *flag = reinterpret_cast<int *>(sm + wy::kMisc + 780);
     float *dec = reinterpret_cast<float *>(sm + wy::kMisc + 1024);
 
-    if (warp == 0) tc::tmem_alloc(tbase, wy::kTmemCols);
-    if (tid == 0) gdn::mbar_init(bar, 1);
+    uint64_t *bar_ld = reinterpret_cast<uint64_t *>(sm + wy::kMisc + 784);
+    int *staged_flag = reinterpret_cast<int *>(sm + wy::kMisc + 792);
 
-    // Stage K, Q (rows of A1) and V (rows of VN); rows past n are zero.
-    // Every load is issued before the first store.
-    {
-        uint4 kv[4], qv[4], vv[4];
+    // Stage K, Q (rows of A1) and V (rows of VN) by six tensor copies of
+    // 64 rows x 64 columns each, 128-byte swizzled by the copy engine (the
+    // layout of the operand tiles); the gates by the threads meanwhile.
+    if (tid == 0) {
+        gdn::mbar_init(bar, 1);
+        gdn::mbar_init(bar_ld, 1);
+        gdn::mbar_arrive_expect_tx(bar_ld, 6u * 8192u);
 #pragma unroll
-        for (int it = 0; it < 4; ++it) {
-            const int e = tid + it * kThreads;
-            const int t = e % kC, c8 = (e / kC) * 8;
-            kv[it] = qv[it] = vv[it] = make_uint4(0, 0, 0, 0);
-            if (t < n) {
-                kv[it] = __ldg(reinterpret_cast<const uint4 *>(a.k + (size_t(t0 + t) * a.h_qk + hq) * kD + c8));
-                qv[it] = __ldg(reinterpret_cast<const uint4 *>(a.q + (size_t(t0 + t) * a.h_qk + hq) * kD + c8));
-                vv[it] = __ldg(reinterpret_cast<const uint4 *>(a.v + (size_t(t0 + t) * a.h_v + h) * kD + c8));
-            }
+        for (int at = 0; at < 2; ++at) {
+            gdn::tma_load_3d(sm + wy::kA1 + at * 16384, &a.tm_k, 64 * at, hq, t0, bar_ld);
+            gdn::tma_load_3d(sm + wy::kA1 + at * 16384 + 8192, &a.tm_q, 64 * at, hq, t0, bar_ld);
+            gdn::tma_load_3d(sm + wy::kVN + at * 16384, &a.tm_v, 64 * at, h, t0, bar_ld);
         }
-        float bt = 0.f, gt = 0.f;
-        if (tid < n) {
-            bt = a.beta[size_t(t0 + tid) * a.h_v + h];
-            gt = a.g[size_t(t0 + tid) * a.h_v + h];
-        }
-#pragma unroll
-        for (int it = 0; it < 4; ++it) {
-            const int e = tid + it * kThreads;
-            const int t = e % kC, c8 = (e / kC) * 8;
-            *reinterpret_cast<uint4 *>(sm + wy::kA1 + tc::swz_off(128, t, c8)) = kv[it];
-            *reinterpret_cast<uint4 *>(sm + wy::kA1 + tc::swz_off(128, kC + t, c8)) = qv[it];
-            *reinterpret_cast<uint4 *>(sm + wy::kVN + tc::swz_off(128, t, c8)) = vv[it];
-        }
-        if (tid < kC) {
-            Bs[tid] = bt;
-            Gs[tid] = gt;
+    }
+    __syncwarp();
+    if (warp == 0) tc::tmem_alloc(tbase, wy::kTmemCols);
+    if (tid < kC) {
+        Bs[tid] = tid < n ? a.beta[size_t(t0 + tid) * a.h_v + h] : 0.f;
+        Gs[tid] = tid < n ? a.g[size_t(t0 + tid) * a.h_v + h] : 0.f;
+    }
+    if (tid == 0) *staged_flag = gdn::mbar_wait_bounded(bar_ld, 0) ? 1 : 0;
+    __syncthreads();
+    const bool staged = *staged_flag != 0;
+    if (staged && n < kC) {
+        // Rows n..63 (the next sequence's rows or padding) become zero: K,
+        // Q and V rows, 128 bytes per row and atom.
+        for (int e = tid; e < (kC - n) * 48; e += kThreads) {
+            const int piece = e & 7, rest = e >> 3;
+            const int which = rest % 6, row = n + rest / 6;
+            const uint32_t off = which < 4 ? wy::kA1 + (which >> 1) * 16384 + (which & 1) * 8192
+                                           : wy::kVN + (which - 4) * 16384;
+            *reinterpret_cast<uint4 *>(sm + off + row * 128 + piece * 16) = make_uint4(0, 0, 0, 0);
         }
     }
     gdn::fence_proxy_async_smem();
@@ -229,7 +236,7 @@ __global__ void __launch_bounds__(kThreads) gdn_chunk_wy_kernel(const PrefArgs a
     const uint32_t tm = *tbase;
 
     // D1 = A1 K^T: rows 0..63 are K K^T, rows 64..127 are Q K^T.
-    if (tid == 0) {
+    if (tid == 0 && staged) {
         constexpr uint32_t idesc = tc::idesc_bf16(128, 64);
 #pragma unroll
         for (int at = 0; at < 2; ++at)
@@ -241,25 +248,35 @@ __global__ void __launch_bounds__(kThreads) gdn_chunk_wy_kernel(const PrefArgs a
         tc::commit(bar);
     }
     if (warp == 0) {
-        chunk_cumsum(Gs, n, Gs);  // G = cumsum(g) while the MMA runs (in place: each lane owns two entries)
-        if (lane == 0) *flag = gdn::mbar_wait_bounded(bar, 0) ? 1 : 0;
+        // While the product runs: G = cumsum(g) (in place: each lane owns two
+        // entries), e^G and dec_i = e^{G_last - G_i} (0 past the n tokens).
+        chunk_cumsum(Gs, n, Gs);
+        __syncwarp();
+        const float gl = Gs[n - 1];
+#pragma unroll
+        for (int e = lane; e < kC; e += 32) {
+            const float ge = Gs[e];
+            const float x = expf(ge);
+            eG[e] = x;
+            dec[e] = e < n ? expf(gl - ge) : 0.f;
+            reinterpret_cast<float *>(out + blob::kEG)[e] = x;
+        }
+        if (lane == 0) *flag = staged && gdn::mbar_wait_bounded(bar, 0) ? 1 : 0;
     }
     __syncthreads();
     bool ok = *flag != 0;
     if (ok) {
         (void)gdn::mbar_try_wait(bar, 0);
         tc::fence_after();
-        if (tid < kC) {
-            eG[tid] = expf(Gs[tid]);
-            dec[tid] = tid < n ? expf(Gs[n - 1] - Gs[tid]) : 0.f;
-            reinterpret_cast<float *>(out + blob::kEG)[tid] = eG[tid];
-        }
         // Rows 0..63: A[t][i] = beta_t e^{G_t-G_i} (k_t.k_i), i < t (0 elsewhere).
         // Rows 64..127: P[t][i] = e^{G_t-G_i} (q_t.k_i), i <= t, split into its
         // two parts in the staging area (rows 0..63 of the A1 atoms: the K rows,
         // consumed by the product above).
+        // Masked entries take e^{-inf} = 0 (K and Q rows past n are zero, so
+        // every product is finite): no divergent branch per element.
         const int q4 = warp & 3, hc = warp >> 2;
         const int t = 32 * (q4 & 1) + lane;
+        const float gt = Gs[t], bt = Bs[t];
 #pragma unroll
         for (int part = 0; part < 2; ++part) {
             float v16[16];
@@ -272,7 +289,7 @@ __global__ void __launch_bounds__(kThreads) gdn_chunk_wy_kernel(const PrefArgs a
 #pragma unroll
                     for (int y = 0; y < 4; ++y) {
                         const int i = col0 + x + y;
-                        av[y] = (i < t && t < n) ? Bs[t] * gate_exp(Gs[t] - Gs[i]) * v16[x + y] : 0.f;
+                        av[y] = bt * gate_exp(i < t && t < n ? gt - Gs[i] : -INFINITY) * v16[x + y];
                     }
                     *reinterpret_cast<float4 *>(Af + t * wy::kAs + col0 + x) = make_float4(av[0], av[1], av[2], av[3]);
                 }
@@ -281,7 +298,7 @@ __global__ void __launch_bounds__(kThreads) gdn_chunk_wy_kernel(const PrefArgs a
 #pragma unroll
                 for (int x = 0; x < 16; ++x) {
                     const int i = col0 + x;
-                    pe[x] = (i <= t && t < n) ? gate_exp(Gs[t] - Gs[i]) * v16[x] : 0.f;
+                    pe[x] = gate_exp(i <= t && t < n ? gt - Gs[i] : -INFINITY) * v16[x];
                 }
 #pragma unroll
                 for (int x = 0; x < 16; x += 8) {
@@ -472,7 +489,9 @@ __global__ void __launch_bounds__(kThreads) gdn_chunk_wy_kernel(const PrefArgs a
             gdn::bulk_s2g(out + blob::kUt + 16384, sm + wy::kStUt + 16384, 16384u);
             gdn::bulk_commit();
         }
-        gdn::bulk_wait_all();  // this CTA's stores are complete before its shared memory is released
+        // The stores have read their shared-memory sources before it is
+        // released; their writes are complete when the grid is.
+        gdn::bulk_wait_read_all();
     }
     if (warp == 0) tc::tmem_dealloc(tm, wy::kTmemCols);
 }
@@ -827,6 +846,38 @@ static size_t blobs_bytes(const gdn_dims *dims, int32_t nseq, int32_t row_capaci
 
 static size_t align16(size_t x) { return (x + 15) / 16 * 16; }
 
+// cuTensorMapEncodeTiled, reached through the runtime's driver entry points.
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_tiled() {
+    static EncodeTiledFn fn = [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            return static_cast<EncodeTiledFn>(nullptr);
+        return reinterpret_cast<EncodeTiledFn>(p);
+    }();
+    return fn;
+}
+
+// Rows of `heads` x 128 bf16 values (rows x heads x 128, innermost last) as a
+// 3-D tensor with boxes of 64 values x 1 head x 64 rows, 128-byte swizzled.
+static bool encode_rows(CUtensorMap *m, const void *base, int heads, int rows) {
+    const EncodeTiledFn fn = encode_tiled();
+    if (!fn) return false;
+    const cuuint64_t dims[3] = {cuuint64_t(kD), cuuint64_t(heads), cuuint64_t(rows > 0 ? rows : 1)};
+    const cuuint64_t strides[2] = {cuuint64_t(kD) * 2, cuuint64_t(heads) * kD * 2};
+    const cuuint32_t box[3] = {64, 1, kC};
+    const cuuint32_t elem[3] = {1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, elem,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // Workspace: the blobs, then order[nseq], then chunk_seq[slots].
 extern "C" size_t gdn_prefill_workspace_bytes(const gdn_dims *dims, int32_t nseq, int32_t row_capacity) {
     if (!dims || nseq < 0 || row_capacity < 0) return 0;
@@ -883,6 +934,9 @@ extern "C" int gdn_chunked_prefill(const gdn_dims *dims, int32_t nseq, int32_t r
     a.chunk_seq = chunk_seq;
     a.q_scale = dims->q_scale;
     a.status = dev_status;
+    if (!encode_rows(&a.tm_q, q, dims->h_qk, row_capacity) || !encode_rows(&a.tm_k, k, dims->h_qk, row_capacity) ||
+        !encode_rows(&a.tm_v, v, dims->h_v, row_capacity))
+        return GDN_ERR_CUDA;
     if (cudaFuncSetAttribute(gdn_chunk_wy_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kWySmem)) !=
             cudaSuccess ||
         cudaFuncSetAttribute(gdn_chunk_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kScanSmem)) !=

@@ -27,7 +27,9 @@ def run_prefill(gs, dev, dims, lengths, src, dst, pool, seed=3, cap=None):
     d = gs.dims(dims.h_qk, dims.h_v, dims.d_k, dims.d_v)
     ws_bytes = gs.gdn_prefill_workspace_bytes(d, len(lengths), cap)
     ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
-    r = rows.to(dev)
+    # rows R .. cap-1 (capacity no sequence uses) hold NaN
+    pad = lambda x: torch.cat([x, torch.full((cap - R,) + tuple(x.shape[1:]), float("nan"), dtype=x.dtype)])
+    r = sy.Rows(pad(rows.q), pad(rows.k), pad(rows.v), pad(rows.g), pad(rows.beta)).to(dev)
     o = torch.full((max(cap, 1), dims.h_v, dims.d_v), float("nan"), dtype=torch.bfloat16, device=dev)
     st = torch.zeros(1, dtype=torch.int32, device=dev)
     cu_d = cu.to(dev)
@@ -79,6 +81,24 @@ def test_prefill_small_ragged(gs, cuda_dev, lengths):
     for s in range(2 * n + 1):
         if s not in dst:
             assert torch.equal(pool[s], init[s]), "only destination slots are written"
+
+
+def test_prefill_unused_rows_do_not_leak(gs, cuda_dev):
+    """Capacity past the last sequence holds NaN in q, k, v, g and beta; the
+    last chunk's 64-row window reaches into it, and nothing of it may reach
+    the outputs or the published states."""
+    dims = sy.Dims(2, 4, 128, 128)
+    lengths = [70, 5]
+    n = len(lengths)
+    pool = torch.zeros((2 * n, dims.h_v, dims.d_v, dims.d_k), dtype=torch.float32, device=cuda_dev)
+    rows, cu, o, st = run_prefill(gs, cuda_dev, dims, lengths, [-1] * n, [n + i for i in range(n)], pool,
+                                  cap=sum(lengths) + 100)
+    assert st == 0
+    finals = [pool[n + i].cpu().numpy() for i in range(n)]
+    assert all(np.isfinite(f).all() for f in finals)
+    ws, wo = check_sequences(rows, cu, o, [np.zeros((dims.h_v, 128, 128))] * n, finals, lengths)
+    assert ws <= CHUNK_STATE_RTOL, ws
+    assert wo <= 1.0, wo
 
 
 def test_prefill_workload_full_size(gs, cuda_dev):
