@@ -133,10 +133,12 @@ __device__ __forceinline__ void split8(const float *x, uint4 &hi, uint4 &lo) {
 //   (the fp32 matrix A -> T, [64][68], lives in the AB area before those
 //    tiles are written)
 //   misc G, beta, e^G, mbarrier, tensor-memory base, flag, dec
-// Outputs are staged and leave by bulk copies issued at the very end (stores
-// in flight hold back the tensor cores): the Q tile is rows 64..127 of both A1
-// atoms as they stand; the P parts go to the unused halves of the VN atoms;
-// after the second product the W parts replace VN and Ut replaces AB.
+// Outputs: the Q tile (rows 64..127 of both A1 atoms as the copy engine left
+// them) leaves by bulk copies once the first product is done, and the P and
+// dec o K parts go from registers straight to the workspace; the W and Ut
+// parts are staged (the W parts in the K rows of A1 and the V rows of VN,
+// both consumed by the second product, Ut where AB was) and leave by bulk
+// copies at the very end: written from registers, their rows would scatter.
 // Tensor memory (256 columns): first D1 = [K;Q] K^T at columns 0..63 (rows
 // 0..63: K K^T, rows 64..127: Q K^T), then D2 = AB [K | V] at 0..255:
 // rows 0..63 x columns 0..127 hold W, rows 64..127 x columns 128..255 hold Ut
@@ -144,10 +146,8 @@ __device__ __forceinline__ void split8(const float *x, uint4 &hi, uint4 &lo) {
 namespace wy {
 constexpr uint32_t kA1 = 0, kVN = 32768, kT = 65536, kMisc = 98304;
 constexpr uint32_t kAbHi = kT, kAbLo = kT + 16384;
-// Staging (8 KB pieces): P parts in the unused row halves of the VN atoms;
-// the two 64-column atoms of W1 in the K rows of the A1 atoms and those of W2
-// in the V rows of the VN atoms (both consumed by the second product); Ut in AB.
-constexpr uint32_t kStP1 = kVN + 8192, kStP2 = kVN + 16384 + 8192;
+// Staging (8 KB pieces): the two 64-column atoms of W1 in the K rows of the
+// A1 atoms and those of W2 in the V rows of the VN atoms; Ut in AB.
 __device__ __forceinline__ uint32_t st_w1(int atom) { return kA1 + 16384u * uint32_t(atom); }
 __device__ __forceinline__ uint32_t st_w2(int atom) { return kVN + 16384u * uint32_t(atom); }
 constexpr uint32_t kStUt = kT;  // 32 KB
@@ -268,6 +268,13 @@ __global__ void __launch_bounds__(kThreads) gdn_chunk_wy_kernel(const __grid_con
     if (ok) {
         (void)gdn::mbar_try_wait(bar, 0);
         tc::fence_after();
+        if (tid == 0) {
+            // The Q tile as it stands; the copy is done long before the
+            // second product is issued.
+            gdn::bulk_s2g(out + blob::kW1Q + 8192, sm + wy::kA1 + 8192, 8192u);
+            gdn::bulk_s2g(out + blob::kW1Q + 16384 + 8192, sm + wy::kA1 + 16384 + 8192, 8192u);
+            gdn::bulk_commit();
+        }
         // Rows 0..63: A[t][i] = beta_t e^{G_t-G_i} (k_t.k_i), i < t (0 elsewhere).
         // Rows 64..127: P[t][i] = e^{G_t-G_i} (q_t.k_i), i <= t, split into its
         // two parts in the staging area (rows 0..63 of the A1 atoms: the K rows,
@@ -305,8 +312,8 @@ __global__ void __launch_bounds__(kThreads) gdn_chunk_wy_kernel(const __grid_con
                     uint4 hi, lo;
                     split8(pe + x, hi, lo);
                     const uint32_t off = tc::swz_off(64, t, col0 + x);
-                    *reinterpret_cast<uint4 *>(sm + wy::kStP1 + off) = hi;
-                    *reinterpret_cast<uint4 *>(sm + wy::kStP2 + off) = lo;
+                    *reinterpret_cast<uint4 *>(out + blob::kP1 + off) = hi;
+                    *reinterpret_cast<uint4 *>(out + blob::kP2 + off) = lo;
                 }
             }
         }
@@ -314,24 +321,6 @@ __global__ void __launch_bounds__(kThreads) gdn_chunk_wy_kernel(const __grid_con
     }
     __syncthreads();
     if (ok) {
-        // dec o K parts for the scan's state update, an MN-major operand with
-        // the K rows' layout (64-column atoms 8 KB apart): 16-byte piece e of
-        // the output (atom e/512, token row i) is the same piece of A1's K row
-        // i, scaled by dec_i.
-        for (int e = tid; e < kD * kC / 8; e += kThreads) {
-            const int atom = e >> 9, i = (e >> 3) & (kC - 1);
-            const uint4 kr = *reinterpret_cast<const uint4 *>(sm + wy::kA1 + atom * 16384 + (e & 511) * 16);
-            const uint32_t kw[4] = {kr.x, kr.y, kr.z, kr.w};
-            const float di = dec[i];
-            float kv[8];
-#pragma unroll
-            for (int y = 0; y < 8; ++y)
-                kv[y] = gdn::bf16_to_f32(uint16_t(y & 1 ? kw[y >> 1] >> 16 : kw[y >> 1] & 0xffffu)) * di;
-            uint4 hi, lo;
-            split8(kv, hi, lo);
-            *reinterpret_cast<uint4 *>(out + blob::kK1 + e * 16) = hi;
-            *reinterpret_cast<uint4 *>(out + blob::kK2 + e * 16) = lo;
-        }
         // T = (I + A)^{-1} by forward substitution, column by column, four
         // pivot rows at a time: T[t][j] = delta_tj - sum_{i<t} A[t][i] T[i][j].
         // Four threads own a column j (rows 4m + q, m = 0..15) and keep the
@@ -374,6 +363,27 @@ __global__ void __launch_bounds__(kThreads) gdn_chunk_wy_kernel(const __grid_con
                         const float4 am = *reinterpret_cast<const float4 *>(Af + (4 * m + q) * wy::kAs + 4 * tau);
                         p[m] = fmaf(am.w, v3, fmaf(am.z, v2, fmaf(am.y, v1, fmaf(am.x, v0, p[m]))));
                     }
+                }
+            }
+            if (warp >= 4) {
+                // The warps with few pivot steps (column blocks 4..7) then
+                // write the dec o K parts for the scan's state update, an
+                // MN-major operand with the K rows' layout (64-column atoms
+                // 8 KB apart): 16-byte piece e of the output (atom e/512,
+                // token row i) is the same piece of A1's K row i, scaled by dec_i.
+                for (int e = tid - 128; e < kD * kC / 8; e += kThreads - 128) {
+                    const int atom = e >> 9, i = (e >> 3) & (kC - 1);
+                    const uint4 kr = *reinterpret_cast<const uint4 *>(sm + wy::kA1 + atom * 16384 + (e & 511) * 16);
+                    const uint32_t kw[4] = {kr.x, kr.y, kr.z, kr.w};
+                    const float di = dec[i];
+                    float kv[8];
+#pragma unroll
+                    for (int y = 0; y < 8; ++y)
+                        kv[y] = gdn::bf16_to_f32(uint16_t(y & 1 ? kw[y >> 1] >> 16 : kw[y >> 1] & 0xffffu)) * di;
+                    uint4 hi, lo;
+                    split8(kv, hi, lo);
+                    *reinterpret_cast<uint4 *>(out + blob::kK1 + e * 16) = hi;
+                    *reinterpret_cast<uint4 *>(out + blob::kK2 + e * 16) = lo;
                 }
             }
             __syncthreads();  // every A entry is read before T overwrites it
@@ -476,11 +486,7 @@ __global__ void __launch_bounds__(kThreads) gdn_chunk_wy_kernel(const __grid_con
     __syncthreads();
     if (tid == 0) {
         if (ok) {
-            // Q tile (rows 64..127 of both A1 atoms), P, W and Ut parts.
-            gdn::bulk_s2g(out + blob::kW1Q + 8192, sm + wy::kA1 + 8192, 8192u);           // Q, atom 0
-            gdn::bulk_s2g(out + blob::kW1Q + 16384 + 8192, sm + wy::kA1 + 16384 + 8192, 8192u);  // Q, atom 1
-            gdn::bulk_s2g(out + blob::kP1, sm + wy::kStP1, 8192u);
-            gdn::bulk_s2g(out + blob::kP2, sm + wy::kStP2, 8192u);
+            // W and Ut parts.
             for (int at = 0; at < 2; ++at) {
                 gdn::bulk_s2g(out + blob::kW1Q + at * 16384, sm + wy::st_w1(at), 8192u);
                 gdn::bulk_s2g(out + blob::kW2 + at * 8192, sm + wy::st_w2(at), 8192u);
