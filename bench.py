@@ -18,6 +18,7 @@ the max of the timed region.
 from __future__ import annotations
 
 import argparse
+import ctypes
 import hashlib
 import json
 import os
@@ -303,18 +304,22 @@ class timed:
 def per_launch_ms(ev, name):
     """Average device time per launch of a kernel class: the event-timed
     spans over the launches they enclose (back-to-back launches on one
-    stream, so the few-microsecond gaps between them count against it)."""
+    stream, so the few-microsecond gaps between them count against it).
+    A span is an event pair, or (milliseconds, None) from the library's
+    host driver, which times the same launches with events of its own."""
     spans = ev.get(name, [])
     n = sum(x[2] for x in spans)
-    return sum(a.elapsed_time(b) for a, b, _ in spans) / max(n, 1), n
+    return sum(a if b is None else a.elapsed_time(b) for a, b, _ in spans) / max(n, 1), n
 
 
 class Bench:
-    def __init__(self, spec: sy.Spec, dev, rank=0, arena=False, replay=False):
+    def __init__(self, spec: sy.Spec, dev, rank=0, arena=False, replay=False, python_driver=False):
         from speculative_decoding_hybrid_gb300 import binding as gs
         from speculative_decoding_hybrid_gb300.step import ArenaStep, DecodeLoop, LayerRows, ReplayStep, VerifyStep
         self.arena = arena
         self.replay = replay
+        self.native = not (arena or replay or python_driver)
+        self._kms = (ctypes.c_float * 3)()
         self.gs, self.spec, self.dev = gs, spec, dev
         d = spec.dims
         self.d = d
@@ -396,9 +401,43 @@ class Bench:
     def step(self, ev=None):
         """One transaction.  ``ev`` (optional) collects, per kernel class, CUDA
         event pairs around its launches and the number of launches between
-        them: the verify pair spans every layer's launch of one step."""
+        them: the verify pair spans every layer's launch of one step.  The
+        copy-commit path goes through the library's host driver
+        (``gdn_decode_transaction``) unless ``python_driver`` is set."""
+        if self.native:
+            return self.native_step(ev)
         p = self.launch(ev)
         return self.finish(p)
+
+    def native_step(self, ev=None):
+        """One transaction by ``gdn_decode_transaction``: the step's draft ids
+        (precomputed synthetic inputs for the requested draft counts) go to
+        the device, then one library call plans, verifies, accepts, commits
+        and reads back."""
+        s = self.step_no
+        loop = self.loop
+        B = loop.B
+        ks = self.ks[s % self.ks.shape[0]].tolist()
+        loop.req_np[:B, 1] = np.asarray(ks, dtype=np.int32)
+        pre = self.pre.get(s)
+        if pre is None or pre[0] != ks:
+            raise RuntimeError("draft ids of step %d were not precomputed" % s)
+        self.tok_d.copy_(pre[1], non_blocking=True)
+        ring = s % self.spec.ring
+        acc = loop.transaction(self.rows[ring], self.logits[ring], self.tok_d,
+                               kernel_ms=self._kms if ev is not None else None)
+        p = loop.plan
+        if p.k != ks:
+            raise RuntimeError("the planner changed the draft counts of step %d" % s)
+        if ev is not None:
+            for name, ms, n in (("verify", self._kms[0], self.spec.layers), ("accept", self._kms[1], 1),
+                                ("commit", self._kms[2], 1)):
+                ev.setdefault(name, []).append((float(ms), None, n))
+        self.last_plan = p
+        n_ver = int(acc.sum()) + B
+        self.step_no += 1
+        self.verified += n_ver
+        return n_ver, p
 
     def launch(self, ev=None):
         """Plans the step and queues its kernels (no host synchronisation)."""
@@ -600,6 +639,16 @@ def run_e2e(b: Bench, host, stages, steps, warmup):
         if mark:
             marks.append((torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)))
             marks[-1][0].record(compute)
+        if b.native:
+            # the library's host driver blocks until the step is done: the
+            # next step's inputs are queued first (their staging set was
+            # released by the step before)
+            issue_copy(b.step_no + 1, slot ^ 1)
+            r = b.native_step()
+            free[slot].record(compute)
+            if mark:
+                marks[-1][1].record(compute)
+            return r
         p = b.launch()
         free[slot].record(compute)
         if mark:
@@ -743,6 +792,9 @@ def main():
     ap.add_argument("--replay", dest="replay", action="store_true", default=True,
                     help="also time compact fixed-state replay (no checkpoints) on the same workload")
     ap.add_argument("--no-replay", dest="replay", action="store_false")
+    ap.add_argument("--python-driver", action="store_true",
+                    help="drive the copy-commit steps from Python (one library call per stage) instead of "
+                         "gdn_decode_transaction")
     args = ap.parse_args()
     if args.workload in PREFILL_SETS:
         if args.impl == "reference":
@@ -777,7 +829,7 @@ def main():
 
     from speculative_decoding_hybrid_gb300 import build
     build.build()
-    b = Bench(rank_spec(spec, rank), dev, rank)
+    b = Bench(rank_spec(spec, rank), dev, rank, python_driver=args.python_driver)
     b.precompute_drafts(args.warmup + args.steps + (0 if args.no_e2e else 3 + args.e2e_steps))
     for _ in range(args.warmup):
         b.step()

@@ -440,6 +440,58 @@ int gdn_pool_apply(gdn_pool *pool, const gdn_plan *plan, int32_t n);
 /* Abort ([NATIVE] recovery after abort): fresh slots of the plan return to the pool. */
 int gdn_pool_abort(gdn_pool *pool, const gdn_plan *plan, int32_t n);
 
+/*
+ * gdn_decode_transaction -- one decode transaction in one host call
+ * ([ENGINE] Summary: the engine plans, verifies every layer, accepts on the
+ * device and reads the results back once; Correctness fix: each layer rolls
+ * back to its accepted checkpoint; [NATIVE] Results: recovery after abort).
+ * It runs, in order: plan_transaction over reqs; the decode group's tables
+ * (cu_rows, src_slot, dst_slot) from io->host_tables (page-locked host,
+ * [3][n_reqs+1]) to io->tables (device, same shape) on `stream`;
+ * gdn_verify_layers with txn + 1; mtp_greedy_accept; gdn_commit; one
+ * device-to-host read into io->host_out (page-locked host, 2*n_reqs +
+ * row_capacity int32: accept_len[0..B), bonus at n_reqs.., emitted tokens at
+ * 2*n_reqs..); a wait for `stream`; gdn_pool_apply; then for every decoded
+ * request i: reqs[i].slot = its destination slot and reqs[i].cur_len +=
+ * accept_len + 1.  *txn is the transaction counter (incremented).
+ * ckpt_tag holds num_layers x B tags (B = decode requests of the plan).
+ * kernel_ms (host, 3 floats, or NULL): device time of the verify launches of
+ * all layers, of the accept and of the commit, from events on `stream`.
+ * Decode requests only: a request list holding a prefill returns
+ * GDN_ERR_ARG before anything is planned.  A plan that selects no request,
+ * or a call that fails after planning, is undone with gdn_pool_abort (its
+ * fresh slots return to the pool) and GDN_ERR_ARG or that call's status is
+ * returned.  Blocks the host until the transaction is done.
+ * Device-detected errors accumulate in *io->dev_status as usual.
+ */
+typedef struct gdn_decode_io {
+    int32_t *tables;                  /* device [3][n_reqs+1] */
+    const gdn_layer_rows *rows;       /* host array [num_layers] */
+    float *pool;
+    int64_t slot_stride, layer_stride;
+    int32_t num_slots;
+    float *ckpt;
+    int64_t ckpt_layer_stride;
+    uint64_t *ckpt_tag;
+    gdn_bf16 *o;
+    int64_t o_layer_stride;
+    const gdn_bf16 *logits;
+    int64_t vocab, logit_row_stride;
+    const int32_t *tokens;            /* packed draft ids (device) */
+    int32_t *argmax, *accept_len, *bonus, *out_tokens;
+    mtp_stats *stats;
+    void *workspace;
+    size_t workspace_bytes;
+    uint32_t *dev_status;
+    int32_t *host_tables;             /* page-locked host [3][n_reqs+1] */
+    int32_t *host_out;                /* page-locked host [2*n_reqs + row_capacity] */
+} gdn_decode_io;
+
+int gdn_decode_transaction(const gdn_dims *dims, int32_t num_layers, int32_t row_capacity,
+                           gdn_req *reqs, int32_t n_reqs, const gdn_plan_limits *lim,
+                           gdn_pool *pool, gdn_plan *plan, uint32_t *txn,
+                           const gdn_decode_io *io, float *kernel_ms, void *stream);
+
 const char *gdn_status_string(int status);
 
 /* Failure-detection self-test: a kernel waits on an mbarrier that is never

@@ -34,7 +34,7 @@ EXPORTS = ["gdn_decode_step", "gdn_verify", "mtp_accept_workspace_bytes", "mtp_g
            "gdn_verify_replay_layers",
            "gdn_prefill_workspace_bytes", "gdn_chunked_prefill", "gdn_pool_init", "gdn_pool_alloc",
            "gdn_pool_share", "gdn_pool_release", "plan_transaction", "gdn_pool_apply", "gdn_pool_abort",
-           "gdn_status_string"]
+           "gdn_decode_transaction", "gdn_status_string"]
 
 
 class GdnError(RuntimeError):
@@ -87,6 +87,18 @@ class gdn_plan(ctypes.Structure):
                                       "pre_req", "pre_cu", "pre_src", "pre_dst")])
 
 
+class gdn_decode_io(ctypes.Structure):
+    _fields_ = [("tables", ctypes.c_void_p), ("rows", ctypes.c_void_p), ("pool", ctypes.c_void_p),
+                ("slot_stride", ctypes.c_int64), ("layer_stride", ctypes.c_int64), ("num_slots", ctypes.c_int32),
+                ("ckpt", ctypes.c_void_p), ("ckpt_layer_stride", ctypes.c_int64), ("ckpt_tag", ctypes.c_void_p),
+                ("o", ctypes.c_void_p), ("o_layer_stride", ctypes.c_int64), ("logits", ctypes.c_void_p),
+                ("vocab", ctypes.c_int64), ("logit_row_stride", ctypes.c_int64), ("tokens", ctypes.c_void_p),
+                ("argmax", ctypes.c_void_p), ("accept_len", ctypes.c_void_p), ("bonus", ctypes.c_void_p),
+                ("out_tokens", ctypes.c_void_p), ("stats", ctypes.c_void_p), ("workspace", ctypes.c_void_p),
+                ("workspace_bytes", ctypes.c_size_t), ("dev_status", ctypes.c_void_p),
+                ("host_tables", ctypes.c_void_p), ("host_out", ctypes.c_void_p)]
+
+
 def _load():
     if not os.path.exists(LIB_PATH):
         raise ImportError("libgdnspec.so is not built (expected at %s); run "
@@ -120,6 +132,9 @@ def _load():
         "gdn_verify_at_layers": [DP, I32, I32, I32, P, P, P, I64, P, P, I64, P, U32, P, I64, P, P],
         "gdn_verify_replay_layers": [DP, I32, I32, I32, P, P, I32, P, P, P, P, I64, I64, I32, P, P, P, I64, P, P],
         "gdn_selftest_wait_timeout": [P, ctypes.c_uint64, P],
+        "gdn_decode_transaction": [DP, I32, I32, ctypes.POINTER(gdn_req), I32, ctypes.POINTER(gdn_plan_limits),
+                                   ctypes.POINTER(gdn_pool), ctypes.POINTER(gdn_plan), ctypes.POINTER(ctypes.c_uint32),
+                                   ctypes.POINTER(gdn_decode_io), P, P],
     }
     for name, args in sig.items():
         f = getattr(L, name)
@@ -270,6 +285,17 @@ def gdn_verify_layers(d: gdn_dims, num_layers, B, row_capacity, cu_rows, rows, p
         ctypes.byref(d), num_layers, B, row_capacity, _ptr(cu_rows), ctypes.cast(rows, ctypes.c_void_p), _ptr(pool),
         slot_stride, layer_stride, num_slots, _ptr(src_slot), _ptr(ckpt), ckpt_layer_stride, _ptr(ckpt_tag), txn,
         _ptr(o), o_layer_stride, _ptr(dev_status), _stream(stream)))
+
+
+def gdn_decode_transaction(d: gdn_dims, num_layers, row_capacity, reqs, n_reqs, lim, pool, plan, txn, io,
+                           kernel_ms=None, stream=None):
+    """``reqs``: a gdn_req array; ``lim``: gdn_plan_limits; ``pool``, ``plan``:
+    Pool and Plan objects; ``txn``: a ctypes.c_uint32 (updated);
+    ``io``: a gdn_decode_io; ``kernel_ms``: None or a ctypes float array of 3."""
+    return _check("gdn_decode_transaction", lib.gdn_decode_transaction(
+        ctypes.byref(d), num_layers, row_capacity, reqs, n_reqs, ctypes.byref(lim), ctypes.byref(pool.c),
+        ctypes.byref(plan.c), ctypes.byref(txn), ctypes.byref(io),
+        None if kernel_ms is None else ctypes.cast(kernel_ms, ctypes.c_void_p), _stream(stream)))
 
 
 def gdn_verify_at_layers(d: gdn_dims, num_layers, B, row_capacity, cu_rows, rows, state_base, state_elems_total,

@@ -1,0 +1,128 @@
+// Host driver of one decode transaction: the plan, the device work of every
+// layer and the one device-to-host read, issued by the library in one call.
+//
+// "Run chained MTP drafting in the batch Engine", Summary: the engine plans
+// each transaction (per-request draft lengths), verifies every layer, accepts
+// on the device and reads the accepted ids back once at the end; Correctness
+// fix: a rejected draft rolls each layer back to its accepted checkpoint.
+// "Native three-step MTP", Results: a failed step leaves the slot pool as it
+// was (recovery after abort).
+//
+// The calls made here are the library's own entry points, in the order a
+// caller would make them; this file only removes the host glue between them.
+#include <cuda_runtime.h>
+#include <string.h>
+
+#include "gdnspec.h"
+
+namespace {
+
+// Six timing events per host thread and device, created on first use.
+struct StepEvents {
+    int device = -1;
+    cudaEvent_t ev[6] = {};
+};
+
+bool step_events(StepEvents &se) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return false;
+    if (se.device == dev) return true;
+    for (auto &e : se.ev)
+        if (e) {
+            cudaEventDestroy(e);
+            e = nullptr;
+        }
+    se.device = -1;
+    for (auto &e : se.ev)
+        if (cudaEventCreate(&e) != cudaSuccess) return false;
+    se.device = dev;
+    return true;
+}
+
+thread_local StepEvents t_events;
+
+}  // namespace
+
+extern "C" int gdn_decode_transaction(const gdn_dims *dims, int32_t num_layers, int32_t row_capacity,
+                                      gdn_req *reqs, int32_t n_reqs, const gdn_plan_limits *lim, gdn_pool *pool,
+                                      gdn_plan *plan, uint32_t *txn, const gdn_decode_io *io, float *kernel_ms,
+                                      void *stream) {
+    if (!dims || !reqs || !lim || !pool || !plan || !txn || !io) return GDN_ERR_NULL;
+    if (!io->tables || !io->rows || !io->host_tables || !io->host_out || !io->accept_len || !io->bonus ||
+        !io->out_tokens)
+        return GDN_ERR_NULL;
+    if (n_reqs <= 0 || num_layers <= 0 || row_capacity <= 0) return GDN_ERR_ARG;
+    for (int32_t i = 0; i < n_reqs; ++i)
+        if (reqs[i].kind != GDN_REQ_DECODE) return GDN_ERR_ARG;  // decode transactions only; nothing planned
+    int st = plan_transaction(reqs, n_reqs, lim, pool, plan);
+    if (st != GDN_OK) return st;
+    const int32_t B = plan->n_decode;
+    const int32_t rows = plan->decode_rows;
+    if (plan->n_prefill > 0 || B <= 0 || rows > row_capacity) {
+        gdn_pool_abort(pool, plan, n_reqs);
+        return GDN_ERR_ARG;
+    }
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int32_t W = n_reqs + 1;
+    int32_t *h = io->host_tables;
+    memcpy(h, plan->dec_cu, size_t(B + 1) * 4);
+    memcpy(h + W, plan->dec_src, size_t(B) * 4);
+    memcpy(h + 2 * W, plan->dec_dst, size_t(B) * 4);
+    const int32_t *cu = io->tables;
+    const int32_t *src = io->tables + W;
+    const int32_t *dst = io->tables + 2 * W;
+    bool timing = kernel_ms != nullptr && step_events(t_events);
+    cudaEvent_t *ev = t_events.ev;
+    const uint32_t t = *txn + 1u;
+    auto fail = [&](int code) {
+        gdn_pool_abort(pool, plan, n_reqs);
+        return code;
+    };
+    if (cudaMemcpyAsync(io->tables, h, size_t(3) * W * 4, cudaMemcpyHostToDevice, s) != cudaSuccess)
+        return fail(GDN_ERR_CUDA);
+    if (timing) cudaEventRecord(ev[0], s);
+    st = gdn_verify_layers(dims, num_layers, B, row_capacity, cu, io->rows, io->pool, io->slot_stride,
+                           io->layer_stride, io->num_slots, src, io->ckpt, io->ckpt_layer_stride, io->ckpt_tag, t,
+                           io->o, io->o_layer_stride, io->dev_status, stream);
+    if (st != GDN_OK) return fail(st);
+    if (timing) {
+        cudaEventRecord(ev[1], s);
+        cudaEventRecord(ev[2], s);
+    }
+    st = mtp_greedy_accept(B, row_capacity, cu, io->logits, io->vocab, io->logit_row_stride, io->tokens, io->argmax,
+                           io->accept_len, io->bonus, io->out_tokens, io->stats, io->workspace, io->workspace_bytes,
+                           io->dev_status, stream);
+    if (st != GDN_OK) return fail(st);
+    if (timing) {
+        cudaEventRecord(ev[3], s);
+        cudaEventRecord(ev[4], s);
+    }
+    st = gdn_commit(dims, B, num_layers, row_capacity, cu, io->accept_len, io->ckpt, io->ckpt_layer_stride,
+                    io->ckpt_tag, t, io->pool, io->slot_stride, io->layer_stride, io->num_slots, dst, io->dev_status,
+                    stream);
+    if (st != GDN_OK) return fail(st);
+    if (timing) cudaEventRecord(ev[5], s);
+    *txn = t;
+    int32_t *ho = io->host_out;
+    if (cudaMemcpyAsync(ho, io->accept_len, size_t(B) * 4, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+        cudaMemcpyAsync(ho + n_reqs, io->bonus, size_t(B) * 4, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+        cudaMemcpyAsync(ho + 2 * n_reqs, io->out_tokens, size_t(rows) * 4, cudaMemcpyDeviceToHost, s) !=
+            cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess)
+        return fail(GDN_ERR_CUDA);
+    if (timing) {
+        for (int i = 0; i < 3; ++i)
+            if (cudaEventElapsedTime(&kernel_ms[i], ev[2 * i], ev[2 * i + 1]) != cudaSuccess) kernel_ms[i] = -1.f;
+    }
+    // The commit is done: requests that moved release their old slot, and
+    // every decode request advances by its accepted drafts plus the bonus.
+    st = gdn_pool_apply(pool, plan, n_reqs);
+    if (st != GDN_OK) return st;
+    for (int32_t j = 0; j < B; ++j) {
+        const int32_t i = plan->dec_req[j];
+        const int32_t acc = ho[j];
+        reqs[i].slot = plan->dst[i];
+        if (acc >= 0) reqs[i].cur_len += acc + 1;
+    }
+    return GDN_OK;
+}

@@ -150,6 +150,8 @@ class DecodeLoop:
         self.h_tab_np = self.h_tab.numpy()
         self.d_tab = torch.zeros((3, B + 1), dtype=torch.int32, device=dev)
         self.h_out = torch.zeros((2 * B + vs.cap,), dtype=torch.int32).pin_memory()
+        self._io = None
+        self._txn = ctypes.c_uint32(vs.txn)
 
     @property
     def slot(self):
@@ -200,6 +202,40 @@ class DecodeLoop:
         self.h_out[2 * B:].copy_(self.vs.out_tokens, non_blocking=True)
         torch.cuda.current_stream().synchronize()
         return self.h_out[:B], self.h_out[B:2 * B], self.h_out[2 * B:]
+
+    def transaction(self, layer_rows: Sequence[LayerRows], logits: torch.Tensor, tokens: torch.Tensor,
+                    kernel_ms=None, stream=None):
+        """One whole decode transaction by the library's host driver
+        (``gdn_decode_transaction``): plan, tables, every layer's verify,
+        accept, commit, the one readback and the request bookkeeping in one
+        call.  Returns the accepted draft counts of the decoded requests (a
+        numpy view, valid until the next transaction).  ``kernel_ms``: None or
+        a ctypes float array of 3 (verify, accept, commit device times)."""
+        vs, B = self.vs, self.B
+        io = self._io
+        if io is None:
+            io = self._io = gs.gdn_decode_io()
+            io.tables = self.d_tab.data_ptr()
+            io.pool = vs.pool.data_ptr()
+            io.slot_stride, io.layer_stride, io.num_slots = vs.slot_stride, vs.layer_stride, vs.num_slots
+            io.ckpt, io.ckpt_layer_stride = vs.ckpt.data_ptr(), vs.ckpt_layer_stride
+            io.ckpt_tag = vs._tags.data_ptr()
+            io.o, io.o_layer_stride = vs.o.data_ptr(), vs.o.stride(0)
+            io.vocab = vs.vocab
+            io.argmax, io.accept_len = vs.argmax.data_ptr(), vs.accept_len.data_ptr()
+            io.bonus, io.out_tokens = vs.bonus.data_ptr(), vs.out_tokens.data_ptr()
+            io.stats = vs.stats.data_ptr()
+            io.workspace, io.workspace_bytes = vs.workspace.data_ptr(), vs.ws_bytes
+            io.dev_status = vs.status.data_ptr()
+            io.host_tables, io.host_out = self.h_tab.data_ptr(), self.h_out.data_ptr()
+        self._txn.value = vs.txn
+        io.rows = ctypes.cast(vs.rows_array(layer_rows), ctypes.c_void_p).value
+        io.logits, io.logit_row_stride = logits.data_ptr(), logits.stride(0)
+        io.tokens = tokens.data_ptr()
+        gs.gdn_decode_transaction(vs.d, vs.L, vs.cap, self.reqs, B, self.lim, self.pool, self.plan, self._txn, io,
+                                  kernel_ms, stream)
+        vs.txn = self._txn.value
+        return self.h_out.numpy()[:self.plan.c.n_decode]
 
     def finish(self, accept_len):
         st = gs.gdn_pool_apply(self.pool, self.plan, self.B)
