@@ -665,6 +665,32 @@ __global__ void __launch_bounds__(kScanThreads, 1) gdn_chunk_scan_kernel(const P
         for (int x = 0; x < 16; ++x) ut[x] = Ut[ut_index(16 * cq + x, arow)];
     };
 
+    // Outputs of chunk c: o_t = q_scale (e^{G_t} Oi[:,t] + Oa[:,t]) for the
+    // 16 tokens of this thread's column quarter.  They are written one chunk
+    // late, while the next chunk's phase B runs (the other warps wait for it
+    // anyway); thread 0 is then issuing that phase, so the columns of warp 0
+    // (tokens 0..15 of lane quadrant 0) go to warps 4 and 8, eight each.
+    auto outputs_part = [&](int c, int col0, int x0, int x1) {
+        const int t0 = s0 + c * kC;
+        const int n = min(kC, len - c * kC);
+        const float *eG = reinterpret_cast<const float *>(sm + sc::kMisc + (c & 1) * 256);
+        float oi[16], oa[16];
+        tc::ld16(tm + lane_base + oi_col(c & 1) + uint32_t(col0), oi);
+        tc::ld16(tm + lane_base + oa_col(c & 1) + uint32_t(col0), oa);
+#pragma unroll
+        for (int x = 0; x < 16; ++x) {
+            const int t = col0 + x;
+            if (x >= x0 && x < x1 && t < n)
+                a.o[(size_t(t0 + t) * a.h_v + h) * kD + arow] =
+                    gdn::f32_to_bf16(a.q_scale * fmaf(eG[t], oi[x], oa[x]));
+        }
+    };
+    auto write_outputs = [&](int c) {
+        if (warp != 0) outputs_part(c, 16 * cq, 0, 16);
+        if (warp == 4) outputs_part(c, 0, 0, 8);
+        if (warp == 8) outputs_part(c, 0, 8, 16);
+    };
+
     uint32_t par_u = 0, par_b = 0, par_o = 0, par_ia = 0, par_ib = 0;
     bool ok = true;
     const int nchunks = (len + kC - 1) / kC;
@@ -727,6 +753,7 @@ __global__ void __launch_bounds__(kScanThreads, 1) gdn_chunk_scan_kernel(const P
         // Phase B: Oa = U^T P^T, dS = U^T (dec o K), once this chunk's P and
         // dec o K have arrived; meanwhile the next chunk's W and Q are fetched
         // as soon as this chunk's Oi is done with W and Q.
+        bool good_b = true;
         if (tid == 0) {
             bool good = gdn::mbar_wait_bounded(bar_ib, par_ib);
             if (good) {
@@ -746,7 +773,11 @@ __global__ void __launch_bounds__(kScanThreads, 1) gdn_chunk_scan_kernel(const P
                 }
                 tc::commit(bar_b);
             }
-            good = good && gdn::mbar_wait_bounded(bar_b, par_b);
+            good_b = good;
+        }
+        if (c > 0) write_outputs(c - 1);  // while phase B runs
+        if (tid == 0) {
+            const bool good = good_b && gdn::mbar_wait_bounded(bar_b, par_b);
             *flag = (good && *oflag) ? 1 : 0;
         }
         par_ib ^= 1u;
@@ -780,21 +811,11 @@ __global__ void __launch_bounds__(kScanThreads, 1) gdn_chunk_scan_kernel(const P
             }
             if (tid == 0) issue_phase_a(c + 1);
         }
-        // Outputs of this chunk's tokens, while the next chunk's first products run.
-        {
-            float oi[16], oa[16];
-            const int col0 = 16 * cq;
-            tc::ld16(tm + lane_base + oi_col(c & 1) + uint32_t(col0), oi);
-            tc::ld16(tm + lane_base + oa_col(c & 1) + uint32_t(col0), oa);
-#pragma unroll
-            for (int x = 0; x < 16; ++x) {
-                const int t = col0 + x;
-                if (t < n)
-                    a.o[(size_t(t0 + t) * a.h_v + h) * kD + arow] =
-                        gdn::f32_to_bf16(a.q_scale * fmaf(eG[t], oi[x], oa[x]));
-            }
-        }
         tc::fence_before();
+    }
+    if (ok && nchunks > 0) {
+        tc::fence_after();
+        write_outputs(nchunks - 1);
     }
     if (ok) {
         float4 *dp = reinterpret_cast<float4 *>(a.pool + size_t(dst) * a.slot_stride + row_off);
