@@ -72,3 +72,34 @@ def test_multi_layer_calls_check_arguments_before_launching(lib):
     rp = gs.lib.gdn_verify_replay_layers(ctypes.byref(d), -2, 1, 4, None, None, 4, None, None, None, None, 0, 0, 1,
                                          None, None, None, 0, None, None)
     assert rp == gs.GDN_ERR_ARG
+
+
+def test_decode_transaction_checks_arguments_before_planning(lib):
+    """gdn_decode_transaction refuses missing buffers and request lists that
+    hold a prefill before it plans anything (the pool stays as it was)."""
+    from speculative_decoding_hybrid_gb300 import binding as gs
+    d = gs.dims(2, 4, 16, 16)
+    pool = gs.Pool(4)
+    held = pool.alloc()
+    plan = gs.Plan(2)
+    reqs = (gs.gdn_req * 2)()
+    reqs[0] = gs.gdn_req(gs.REQ_DECODE, 3, 0, 1, 1 << 20, held)
+    reqs[1] = gs.gdn_req(gs.REQ_PREFILL, 0, 5, 0, 1 << 20, -1)
+    lim = gs.gdn_plan_limits(64, 2, 3)
+    txn = ctypes.c_uint32(7)
+    io = gs.gdn_decode_io()
+    before = (pool.refcount.copy(), pool.free_list())
+    # no device buffers in io
+    st = gs.lib.gdn_decode_transaction(ctypes.byref(d), 1, 8, reqs, 2, ctypes.byref(lim), ctypes.byref(pool.c),
+                                       ctypes.byref(plan.c), ctypes.byref(txn), ctypes.byref(io), None, None)
+    assert st == gs.GDN_ERR_NULL
+    # every pointer set (never dereferenced on this path): the prefill is refused before planning
+    for name, _ in gs.gdn_decode_io._fields_:
+        if name not in ("slot_stride", "layer_stride", "num_slots", "ckpt_layer_stride", "o_layer_stride", "vocab",
+                        "logit_row_stride", "workspace_bytes"):
+            setattr(io, name, 16)
+    st = gs.lib.gdn_decode_transaction(ctypes.byref(d), 1, 8, reqs, 2, ctypes.byref(lim), ctypes.byref(pool.c),
+                                       ctypes.byref(plan.c), ctypes.byref(txn), ctypes.byref(io), None, None)
+    assert st == gs.GDN_ERR_ARG
+    assert (pool.refcount == before[0]).all() and pool.free_list() == before[1] and txn.value == 7
+    assert reqs[0].slot == held and reqs[0].cur_len == 1
