@@ -934,6 +934,8 @@ def main():
         "data": "synthetic",
         "config": {"workload": args.workload, "desc": WORKLOAD_TEXT[args.workload],
                    "l2": l2desc,
+                   "driver": "gdn_decode_transaction (one library call per step)" if b.native
+                   else "Python (one library call per stage)",
                    "parallelism": "replicas (requests sharded, no collective)" if world > 1 else "single GPU"},
         "verify_commit_gbs": vc_gbs,
         "verify_commit_frac": vc_gbs / peak,
