@@ -830,6 +830,7 @@ def main():
     from speculative_decoding_hybrid_gb300 import build
     build.build()
     b = Bench(rank_spec(spec, rank), dev, rank, python_driver=args.python_driver)
+    native_driver = b.native
     b.precompute_drafts(args.warmup + args.steps + (0 if args.no_e2e else 3 + args.e2e_steps))
     for _ in range(args.warmup):
         b.step()
@@ -934,7 +935,7 @@ def main():
         "data": "synthetic",
         "config": {"workload": args.workload, "desc": WORKLOAD_TEXT[args.workload],
                    "l2": l2desc,
-                   "driver": "gdn_decode_transaction (one library call per step)" if b.native
+                   "driver": "gdn_decode_transaction (one library call per step)" if native_driver
                    else "Python (one library call per stage)",
                    "parallelism": "replicas (requests sharded, no collective)" if world > 1 else "single GPU"},
         "verify_commit_gbs": vc_gbs,
