@@ -318,7 +318,7 @@ class Bench:
         from speculative_decoding_hybrid_gb300.step import ArenaStep, DecodeLoop, LayerRows, ReplayStep, VerifyStep
         self.arena = arena
         self.replay = replay
-        self.native = not (arena or replay or python_driver)
+        self.native = not (replay or python_driver)
         self._kms = (ctypes.c_float * 3)()
         self.gs, self.spec, self.dev = gs, spec, dev
         d = spec.dims
@@ -554,7 +554,8 @@ def run_zero_copy(spec, dev, args, replay=False, graph=False):
         raise RuntimeError("zero-copy loop status %d" % int(b.vs.status.item()))
     res = {"value": tok / (ms * 1e-3), "unit": "verified tokens/s", "ms_per_step": ms / args.steps,
            "verify_ms": v_ms, "commit_at_ms": c_ms, "verify_commit_gbs": gbs, "verify_commit_frac": gbs / peak,
-           "state_gib": (b.vs.arena.numel() if not replay else b.vs.pool.numel()) * 4 / 2 ** 30}
+           "state_gib": (b.vs.arena.numel() if not replay else b.vs.pool.numel()) * 4 / 2 ** 30,
+           "driver": "gdn_decode_transaction_at" if b.native else "Python"}
     del b
     torch.cuda.empty_cache()
     return res

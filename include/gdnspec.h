@@ -461,7 +461,8 @@ int gdn_pool_abort(gdn_pool *pool, const gdn_plan *plan, int32_t n);
  * GDN_ERR_ARG before anything is planned.  A plan that selects no request,
  * or a call that fails after planning, is undone with gdn_pool_abort (its
  * fresh slots return to the pool) and GDN_ERR_ARG or that call's status is
- * returned.  Blocks the host until the transaction is done.
+ * returned.  Blocks the host until the transaction is done (it waits for
+ * `stream`, so it cannot be captured into a CUDA graph).
  * Device-detected errors accumulate in *io->dev_status as usual.
  */
 typedef struct gdn_decode_io {
@@ -491,6 +492,29 @@ int gdn_decode_transaction(const gdn_dims *dims, int32_t num_layers, int32_t row
                            gdn_req *reqs, int32_t n_reqs, const gdn_plan_limits *lim,
                            gdn_pool *pool, gdn_plan *plan, uint32_t *txn,
                            const gdn_decode_io *io, float *kernel_ms, void *stream);
+
+/*
+ * gdn_decode_transaction_at -- gdn_decode_transaction over a state arena
+ * (the zero-copy commit above): gdn_verify_at_layers reads every start state
+ * at arena->arena + loc[l*n_reqs + r] and writes the checkpoints at
+ * arena->arena + area_off[(txn + 1) & 1]; gdn_commit_at rewrites loc.
+ * io->pool, slot_stride, layer_stride, num_slots and ckpt are not used.
+ * Every request must be a decode request selected by the plan (the location
+ * table holds one entry per request and layer); otherwise the plan is
+ * undone and GDN_ERR_ARG returned.
+ */
+typedef struct gdn_arena_io {
+    float *arena;                     /* device */
+    int64_t elems_total;              /* fp32 elements of the arena */
+    int64_t *loc;                     /* device [num_layers][n_reqs] element offsets */
+    int64_t area_off[2];              /* element offsets of the two checkpoint areas */
+} gdn_arena_io;
+
+int gdn_decode_transaction_at(const gdn_dims *dims, int32_t num_layers, int32_t row_capacity,
+                              gdn_req *reqs, int32_t n_reqs, const gdn_plan_limits *lim,
+                              gdn_pool *pool, gdn_plan *plan, uint32_t *txn,
+                              const gdn_decode_io *io, const gdn_arena_io *arena,
+                              float *kernel_ms, void *stream);
 
 const char *gdn_status_string(int status);
 

@@ -34,7 +34,7 @@ EXPORTS = ["gdn_decode_step", "gdn_verify", "mtp_accept_workspace_bytes", "mtp_g
            "gdn_verify_replay_layers",
            "gdn_prefill_workspace_bytes", "gdn_chunked_prefill", "gdn_pool_init", "gdn_pool_alloc",
            "gdn_pool_share", "gdn_pool_release", "plan_transaction", "gdn_pool_apply", "gdn_pool_abort",
-           "gdn_decode_transaction", "gdn_status_string"]
+           "gdn_decode_transaction", "gdn_decode_transaction_at", "gdn_status_string"]
 
 
 class GdnError(RuntimeError):
@@ -99,6 +99,11 @@ class gdn_decode_io(ctypes.Structure):
                 ("host_tables", ctypes.c_void_p), ("host_out", ctypes.c_void_p)]
 
 
+class gdn_arena_io(ctypes.Structure):
+    _fields_ = [("arena", ctypes.c_void_p), ("elems_total", ctypes.c_int64), ("loc", ctypes.c_void_p),
+                ("area_off", ctypes.c_int64 * 2)]
+
+
 def _load():
     if not os.path.exists(LIB_PATH):
         raise ImportError("libgdnspec.so is not built (expected at %s); run "
@@ -135,6 +140,10 @@ def _load():
         "gdn_decode_transaction": [DP, I32, I32, ctypes.POINTER(gdn_req), I32, ctypes.POINTER(gdn_plan_limits),
                                    ctypes.POINTER(gdn_pool), ctypes.POINTER(gdn_plan), ctypes.POINTER(ctypes.c_uint32),
                                    ctypes.POINTER(gdn_decode_io), P, P],
+        "gdn_decode_transaction_at": [DP, I32, I32, ctypes.POINTER(gdn_req), I32, ctypes.POINTER(gdn_plan_limits),
+                                      ctypes.POINTER(gdn_pool), ctypes.POINTER(gdn_plan),
+                                      ctypes.POINTER(ctypes.c_uint32), ctypes.POINTER(gdn_decode_io),
+                                      ctypes.POINTER(gdn_arena_io), P, P],
     }
     for name, args in sig.items():
         f = getattr(L, name)
@@ -295,6 +304,15 @@ def gdn_decode_transaction(d: gdn_dims, num_layers, row_capacity, reqs, n_reqs, 
     return _check("gdn_decode_transaction", lib.gdn_decode_transaction(
         ctypes.byref(d), num_layers, row_capacity, reqs, n_reqs, ctypes.byref(lim), ctypes.byref(pool.c),
         ctypes.byref(plan.c), ctypes.byref(txn), ctypes.byref(io),
+        None if kernel_ms is None else ctypes.cast(kernel_ms, ctypes.c_void_p), _stream(stream)))
+
+
+def gdn_decode_transaction_at(d: gdn_dims, num_layers, row_capacity, reqs, n_reqs, lim, pool, plan, txn, io, arena,
+                              kernel_ms=None, stream=None):
+    """gdn_decode_transaction over a state arena; ``arena``: a gdn_arena_io."""
+    return _check("gdn_decode_transaction_at", lib.gdn_decode_transaction_at(
+        ctypes.byref(d), num_layers, row_capacity, reqs, n_reqs, ctypes.byref(lim), ctypes.byref(pool.c),
+        ctypes.byref(plan.c), ctypes.byref(txn), ctypes.byref(io), ctypes.byref(arena),
         None if kernel_ms is None else ctypes.cast(kernel_ms, ctypes.c_void_p), _stream(stream)))
 
 

@@ -41,16 +41,17 @@ bool step_events(StepEvents &se) {
 
 thread_local StepEvents t_events;
 
-}  // namespace
-
-extern "C" int gdn_decode_transaction(const gdn_dims *dims, int32_t num_layers, int32_t row_capacity,
-                                      gdn_req *reqs, int32_t n_reqs, const gdn_plan_limits *lim, gdn_pool *pool,
-                                      gdn_plan *plan, uint32_t *txn, const gdn_decode_io *io, float *kernel_ms,
-                                      void *stream) {
+// One decode transaction; `arena` selects the zero-copy form (start states
+// at arena locations, checkpoints in the area of the transaction's parity,
+// commit by rewriting locations) instead of the slot-pool form.
+int run_transaction(const gdn_dims *dims, int32_t num_layers, int32_t row_capacity, gdn_req *reqs, int32_t n_reqs,
+                    const gdn_plan_limits *lim, gdn_pool *pool, gdn_plan *plan, uint32_t *txn,
+                    const gdn_decode_io *io, const gdn_arena_io *arena, float *kernel_ms, void *stream) {
     if (!dims || !reqs || !lim || !pool || !plan || !txn || !io) return GDN_ERR_NULL;
     if (!io->tables || !io->rows || !io->host_tables || !io->host_out || !io->accept_len || !io->bonus ||
         !io->out_tokens)
         return GDN_ERR_NULL;
+    if (arena && (!arena->arena || !arena->loc)) return GDN_ERR_NULL;
     if (n_reqs <= 0 || num_layers <= 0 || row_capacity <= 0) return GDN_ERR_ARG;
     for (int32_t i = 0; i < n_reqs; ++i)
         if (reqs[i].kind != GDN_REQ_DECODE) return GDN_ERR_ARG;  // decode transactions only; nothing planned
@@ -58,7 +59,8 @@ extern "C" int gdn_decode_transaction(const gdn_dims *dims, int32_t num_layers, 
     if (st != GDN_OK) return st;
     const int32_t B = plan->n_decode;
     const int32_t rows = plan->decode_rows;
-    if (plan->n_prefill > 0 || B <= 0 || rows > row_capacity) {
+    // The location table is laid out per request: every request must be in the transaction.
+    if (plan->n_prefill > 0 || B <= 0 || rows > row_capacity || (arena && B != n_reqs)) {
         gdn_pool_abort(pool, plan, n_reqs);
         return GDN_ERR_ARG;
     }
@@ -74,6 +76,7 @@ extern "C" int gdn_decode_transaction(const gdn_dims *dims, int32_t num_layers, 
     bool timing = kernel_ms != nullptr && step_events(t_events);
     cudaEvent_t *ev = t_events.ev;
     const uint32_t t = *txn + 1u;
+    const int64_t area = arena ? arena->area_off[t & 1u] : 0;
     auto fail = [&](int code) {
         gdn_pool_abort(pool, plan, n_reqs);
         return code;
@@ -81,9 +84,14 @@ extern "C" int gdn_decode_transaction(const gdn_dims *dims, int32_t num_layers, 
     if (cudaMemcpyAsync(io->tables, h, size_t(3) * W * 4, cudaMemcpyHostToDevice, s) != cudaSuccess)
         return fail(GDN_ERR_CUDA);
     if (timing) cudaEventRecord(ev[0], s);
-    st = gdn_verify_layers(dims, num_layers, B, row_capacity, cu, io->rows, io->pool, io->slot_stride,
-                           io->layer_stride, io->num_slots, src, io->ckpt, io->ckpt_layer_stride, io->ckpt_tag, t,
-                           io->o, io->o_layer_stride, io->dev_status, stream);
+    if (arena)
+        st = gdn_verify_at_layers(dims, num_layers, B, row_capacity, cu, io->rows, arena->arena, arena->elems_total,
+                                  arena->loc, arena->arena + area, io->ckpt_layer_stride, io->ckpt_tag, t, io->o,
+                                  io->o_layer_stride, io->dev_status, stream);
+    else
+        st = gdn_verify_layers(dims, num_layers, B, row_capacity, cu, io->rows, io->pool, io->slot_stride,
+                               io->layer_stride, io->num_slots, src, io->ckpt, io->ckpt_layer_stride, io->ckpt_tag,
+                               t, io->o, io->o_layer_stride, io->dev_status, stream);
     if (st != GDN_OK) return fail(st);
     if (timing) {
         cudaEventRecord(ev[1], s);
@@ -97,9 +105,13 @@ extern "C" int gdn_decode_transaction(const gdn_dims *dims, int32_t num_layers, 
         cudaEventRecord(ev[3], s);
         cudaEventRecord(ev[4], s);
     }
-    st = gdn_commit(dims, B, num_layers, row_capacity, cu, io->accept_len, io->ckpt, io->ckpt_layer_stride,
-                    io->ckpt_tag, t, io->pool, io->slot_stride, io->layer_stride, io->num_slots, dst, io->dev_status,
-                    stream);
+    if (arena)
+        st = gdn_commit_at(dims, B, num_layers, row_capacity, cu, io->accept_len, area, io->ckpt_layer_stride,
+                           io->ckpt_tag, t, arena->loc, io->dev_status, stream);
+    else
+        st = gdn_commit(dims, B, num_layers, row_capacity, cu, io->accept_len, io->ckpt, io->ckpt_layer_stride,
+                        io->ckpt_tag, t, io->pool, io->slot_stride, io->layer_stride, io->num_slots, dst,
+                        io->dev_status, stream);
     if (st != GDN_OK) return fail(st);
     if (timing) cudaEventRecord(ev[5], s);
     *txn = t;
@@ -125,4 +137,23 @@ extern "C" int gdn_decode_transaction(const gdn_dims *dims, int32_t num_layers, 
         if (acc >= 0) reqs[i].cur_len += acc + 1;
     }
     return GDN_OK;
+}
+
+}  // namespace
+
+extern "C" int gdn_decode_transaction(const gdn_dims *dims, int32_t num_layers, int32_t row_capacity,
+                                      gdn_req *reqs, int32_t n_reqs, const gdn_plan_limits *lim, gdn_pool *pool,
+                                      gdn_plan *plan, uint32_t *txn, const gdn_decode_io *io, float *kernel_ms,
+                                      void *stream) {
+    return run_transaction(dims, num_layers, row_capacity, reqs, n_reqs, lim, pool, plan, txn, io, nullptr,
+                           kernel_ms, stream);
+}
+
+extern "C" int gdn_decode_transaction_at(const gdn_dims *dims, int32_t num_layers, int32_t row_capacity,
+                                         gdn_req *reqs, int32_t n_reqs, const gdn_plan_limits *lim, gdn_pool *pool,
+                                         gdn_plan *plan, uint32_t *txn, const gdn_decode_io *io,
+                                         const gdn_arena_io *arena, float *kernel_ms, void *stream) {
+    if (!arena) return GDN_ERR_NULL;
+    return run_transaction(dims, num_layers, row_capacity, reqs, n_reqs, lim, pool, plan, txn, io, arena, kernel_ms,
+                           stream);
 }

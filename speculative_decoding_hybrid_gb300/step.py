@@ -151,6 +151,7 @@ class DecodeLoop:
         self.d_tab = torch.zeros((3, B + 1), dtype=torch.int32, device=dev)
         self.h_out = torch.zeros((2 * B + vs.cap,), dtype=torch.int32).pin_memory()
         self._io = None
+        self._arena_io = None
         self._txn = ctypes.c_uint32(vs.txn)
 
     @property
@@ -206,7 +207,8 @@ class DecodeLoop:
     def transaction(self, layer_rows: Sequence[LayerRows], logits: torch.Tensor, tokens: torch.Tensor,
                     kernel_ms=None, stream=None):
         """One whole decode transaction by the library's host driver
-        (``gdn_decode_transaction``): plan, tables, every layer's verify,
+        (``gdn_decode_transaction``, or ``gdn_decode_transaction_at`` over an
+        ``ArenaStep``'s state arena): plan, tables, every layer's verify,
         accept, commit, the one readback and the request bookkeeping in one
         call.  Returns the accepted draft counts of the decoded requests (a
         numpy view, valid until the next transaction).  ``kernel_ms``: None or
@@ -218,7 +220,8 @@ class DecodeLoop:
             io.tables = self.d_tab.data_ptr()
             io.pool = vs.pool.data_ptr()
             io.slot_stride, io.layer_stride, io.num_slots = vs.slot_stride, vs.layer_stride, vs.num_slots
-            io.ckpt, io.ckpt_layer_stride = vs.ckpt.data_ptr(), vs.ckpt_layer_stride
+            ck = getattr(vs, "ckpt", None)
+            io.ckpt, io.ckpt_layer_stride = (ck.data_ptr() if ck is not None else None), vs.ckpt_layer_stride
             io.ckpt_tag = vs._tags.data_ptr()
             io.o, io.o_layer_stride = vs.o.data_ptr(), vs.o.stride(0)
             io.vocab = vs.vocab
@@ -232,8 +235,17 @@ class DecodeLoop:
         io.rows = ctypes.cast(vs.rows_array(layer_rows), ctypes.c_void_p).value
         io.logits, io.logit_row_stride = logits.data_ptr(), logits.stride(0)
         io.tokens = tokens.data_ptr()
-        gs.gdn_decode_transaction(vs.d, vs.L, vs.cap, self.reqs, B, self.lim, self.pool, self.plan, self._txn, io,
-                                  kernel_ms, stream)
+        if isinstance(vs, ArenaStep):
+            ar = self._arena_io
+            if ar is None:
+                ar = self._arena_io = gs.gdn_arena_io()
+                ar.arena, ar.elems_total, ar.loc = vs.arena.data_ptr(), vs.total, vs.loc.data_ptr()
+                ar.area_off[0], ar.area_off[1] = vs.area_off
+            gs.gdn_decode_transaction_at(vs.d, vs.L, vs.cap, self.reqs, B, self.lim, self.pool, self.plan,
+                                         self._txn, io, ar, kernel_ms, stream)
+        else:
+            gs.gdn_decode_transaction(vs.d, vs.L, vs.cap, self.reqs, B, self.lim, self.pool, self.plan, self._txn,
+                                      io, kernel_ms, stream)
         vs.txn = self._txn.value
         return self.h_out.numpy()[:self.plan.c.n_decode]
 

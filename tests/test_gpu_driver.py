@@ -23,12 +23,15 @@ def gs(cuda_dev):
     return binding
 
 
-def test_native_transaction_matches_python_driver(gs, cuda_dev):
+@pytest.mark.parametrize("arena", [False, True])
+def test_native_transaction_matches_python_driver(gs, cuda_dev, arena):
+    """Copy commit (gdn_decode_transaction) and zero-copy commit over a state
+    arena (gdn_decode_transaction_at)."""
     import bench
     steps = SPEC.steps
     runs = []
     for python_driver in (True, False):
-        b = bench.Bench(SPEC, cuda_dev, python_driver=python_driver)
+        b = bench.Bench(SPEC, cuda_dev, arena=arena, python_driver=python_driver)
         assert b.native == (not python_driver)
         b.precompute_drafts(steps)
         per_step = []
@@ -45,6 +48,8 @@ def test_native_transaction_matches_python_driver(gs, cuda_dev):
         assert torch.equal(x[3], y[3]) and torch.equal(x[4], y[4]) and torch.equal(x[5], y[5])
     assert int(a.vs.status.item()) == 0 and int(n.vs.status.item()) == 0
     assert torch.equal(a.vs.pool, n.vs.pool)
+    if arena:
+        assert torch.equal(a.vs.loc, n.vs.loc) and torch.equal(a.vs.arena, n.vs.arena)
     assert torch.equal(a.vs.stats, n.vs.stats)
     assert a.vs.txn == n.vs.txn == steps
     assert np.array_equal(a.loop.req_np, n.loop.req_np)
