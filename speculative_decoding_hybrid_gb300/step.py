@@ -214,6 +214,8 @@ class DecodeLoop:
         numpy view, valid until the next transaction).  ``kernel_ms``: None or
         a ctypes float array of 3 (verify, accept, commit device times)."""
         vs, B = self.vs, self.B
+        if isinstance(vs, ReplayStep):
+            raise TypeError("fixed-state replay has no one-call driver: use ReplayStep.run or ReplayGraphs")
         io = self._io
         if io is None:
             io = self._io = gs.gdn_decode_io()
