@@ -409,20 +409,27 @@ class Bench:
         p = self.launch(ev)
         return self.finish(p)
 
-    def native_step(self, ev=None):
-        """One transaction by ``gdn_decode_transaction``: the step's draft ids
-        (precomputed synthetic inputs for the requested draft counts) go to
-        the device, then one library call plans, verifies, accepts, commits
-        and reads back."""
+    def upload_drafts(self):
+        """The step's draft ids (precomputed synthetic inputs for the
+        requested draft counts) to the device; returns the counts."""
         s = self.step_no
-        loop = self.loop
-        B = loop.B
         ks = self.ks[s % self.ks.shape[0]].tolist()
-        loop.req_np[:B, 1] = np.asarray(ks, dtype=np.int32)
         pre = self.pre.get(s)
         if pre is None or pre[0] != ks:
             raise RuntimeError("draft ids of step %d were not precomputed" % s)
         self.tok_d.copy_(pre[1], non_blocking=True)
+        return ks
+
+    def native_step(self, ev=None, ks=None):
+        """One transaction by ``gdn_decode_transaction``: the step's draft ids
+        go to the device (unless ``ks`` says they already did), then one
+        library call plans, verifies, accepts, commits and reads back."""
+        s = self.step_no
+        loop = self.loop
+        B = loop.B
+        if ks is None:
+            ks = self.upload_drafts()
+        loop.req_np[:B, 1] = np.asarray(ks, dtype=np.int32)
         ring = s % self.spec.ring
         acc = loop.transaction(self.rows[ring], self.logits[ring], self.tok_d,
                                kernel_ms=self._kms if ev is not None else None)
@@ -617,17 +624,25 @@ def run_e2e(b: Bench, host, stages, steps, warmup):
     saved_rows, saved_logits = b.rows, b.logits
     copy_stream = torch.cuda.Stream()
     compute = torch.cuda.current_stream()
-    done = [torch.cuda.Event(), torch.cuda.Event()]
+    done = [torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)]
     free = [torch.cuda.Event(), torch.cuda.Event()]
     moved_bytes = [0]
+    copies = []   # (start, done) events of the input copies issued in the timed region
 
-    def issue_copy(step_no, slot):
+    def issue_copy(step_no, slot, timed_copy=False):
         hb = host[step_no % spec.ring]
         db = stages[slot][0]
         with torch.cuda.stream(copy_stream):
             copy_stream.wait_event(free[slot])  # the staging set's previous reader is done
+            if timed_copy:
+                st = torch.cuda.Event(enable_timing=True)
+                st.record(copy_stream)
             db.copy_(hb, non_blocking=True)
             done[slot].record(copy_stream)
+            if timed_copy:
+                en = torch.cuda.Event(enable_timing=True)
+                en.record(copy_stream)
+                copies.append((st, en))
         moved_bytes[0] += hb.numel()
 
     marks = []   # (start, end) events of the timed steps on the compute stream
@@ -642,10 +657,12 @@ def run_e2e(b: Bench, host, stages, steps, warmup):
             marks[-1][0].record(compute)
         if b.native:
             # the library's host driver blocks until the step is done: the
-            # next step's inputs are queued first (their staging set was
-            # released by the step before)
-            issue_copy(b.step_no + 1, slot ^ 1)
-            r = b.native_step()
+            # step's draft ids go first, then the next step's inputs are
+            # queued on the copy stream (their staging set was released by
+            # the step before), then the step runs
+            ks = b.upload_drafts()
+            issue_copy(b.step_no + 1, slot ^ 1, timed_copy=mark)
+            r = b.native_step(ks=ks)
             free[slot].record(compute)
             if mark:
                 marks[-1][1].record(compute)
@@ -654,7 +671,7 @@ def run_e2e(b: Bench, host, stages, steps, warmup):
         free[slot].record(compute)
         if mark:
             marks[-1][1].record(compute)
-        issue_copy(b.step_no + 1, slot ^ 1)       # next step's inputs, overlapped
+        issue_copy(b.step_no + 1, slot ^ 1, timed_copy=mark)       # next step's inputs, overlapped
         return b.finish(p)                        # the step's one readback
 
     try:
@@ -689,9 +706,12 @@ def run_e2e(b: Bench, host, stages, steps, warmup):
     # (the host's readback, planning and launch of the next step)
     gaps = [marks[i][1].elapsed_time(marks[i + 1][0]) for i in range(len(marks) - 1)]
     gap_ms = sum(gaps) / len(gaps) if gaps else 0.0
+    # the input copies as they ran beside the steps (HBM shared with the kernels)
+    in_step = [a.elapsed_time(c) for a, c in copies]
+    copy_in_step_ms = sum(in_step) / len(in_step) if in_step else 0.0
     h2d = moved_bytes[0] / steps + (b.loop.B + 1) * 3 * 4 + b.cap * 4   # inputs + tables + tokens
     d2h = (2 * spec.batch + b.cap) * 4
-    return tok / dt, h2d, d2h, copy_ms, gap_ms
+    return tok / dt, h2d, d2h, copy_ms, gap_ms, copy_in_step_ms
 
 
 # ---------------------------------------------------------------------------
@@ -878,7 +898,7 @@ def main():
     e2e = None
     if not args.no_e2e:
         host, stages = stage_e2e(b)
-        val, h2d, d2h, copy_ms, gap_ms = run_e2e(b, host, stages, args.e2e_steps, 3)
+        val, h2d, d2h, copy_ms, gap_ms, copy_in_step_ms = run_e2e(b, host, stages, args.e2e_steps, 3)
         del host, stages
         if world > 1:
             t = torch.tensor([val], device=dev, dtype=torch.float64)
@@ -887,7 +907,7 @@ def main():
         e2e = {"value": val, "unit": "verified tokens/s", "h2d_bytes_per_step": int(h2d),
                "d2h_bytes_per_step": int(d2h), "steps": args.e2e_steps,
                "input_copy_ms_alone": copy_ms, "input_copy_gbs": h2d / (copy_ms * 1e-3) / 1e9,
-               "device_idle_ms_between_steps": gap_ms}
+               "device_idle_ms_between_steps": gap_ms, "input_copy_ms_beside_steps": copy_in_step_ms}
 
     if rank != 0:
         if world > 1:

@@ -9,7 +9,9 @@
 // was (recovery after abort).
 //
 // The calls made here are the library's own entry points, in the order a
-// caller would make them; this file only removes the host glue between them.
+// caller would make them; this file only removes the host glue between them
+// (plus one small kernel that moves the step's tables through mapped host
+// memory instead of the copy engines).
 #include <cuda_runtime.h>
 #include <string.h>
 
@@ -40,6 +42,32 @@ bool step_events(StepEvents &se) {
 }
 
 thread_local StepEvents t_events;
+
+// Small host <-> device table moves by a kernel over page-locked host memory
+// mapped into the device address space, so that they never queue behind a
+// large copy the caller has put on a copy engine (the next transaction's
+// inputs, say).  Three spans of n0, n1, n2 int32 (n0 + n1 + n2 <= 3 * span).
+struct Spans {
+    const int32_t *src[3];
+    int32_t *dst[3];
+    int32_t n[3];
+};
+
+__global__ void move_spans_kernel(const Spans sp) {
+#pragma unroll
+    for (int k = 0; k < 3; ++k)
+        for (int i = threadIdx.x; i < sp.n[k]; i += blockDim.x) sp.dst[k][i] = sp.src[k][i];
+}
+
+// The device address of mapped page-locked host memory, or nullptr.
+int32_t *mapped(int32_t *host) {
+    void *d = nullptr;
+    if (cudaHostGetDevicePointer(&d, host, 0) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return nullptr;
+    }
+    return static_cast<int32_t *>(d);
+}
 
 // One decode transaction; `arena` selects the zero-copy form (start states
 // at arena locations, checkpoints in the area of the transaction's parity,
@@ -81,8 +109,14 @@ int run_transaction(const gdn_dims *dims, int32_t num_layers, int32_t row_capaci
         gdn_pool_abort(pool, plan, n_reqs);
         return code;
     };
-    if (cudaMemcpyAsync(io->tables, h, size_t(3) * W * 4, cudaMemcpyHostToDevice, s) != cudaSuccess)
+    int32_t *h_dev = mapped(h);
+    if (h_dev) {
+        Spans sp{{h_dev, h_dev + W, h_dev + 2 * W}, {io->tables, io->tables + W, io->tables + 2 * W}, {B + 1, B, B}};
+        move_spans_kernel<<<1, 256, 0, s>>>(sp);
+        if (cudaGetLastError() != cudaSuccess) return fail(GDN_ERR_CUDA);
+    } else if (cudaMemcpyAsync(io->tables, h, size_t(3) * W * 4, cudaMemcpyHostToDevice, s) != cudaSuccess) {
         return fail(GDN_ERR_CUDA);
+    }
     if (timing) cudaEventRecord(ev[0], s);
     if (arena)
         st = gdn_verify_at_layers(dims, num_layers, B, row_capacity, cu, io->rows, arena->arena, arena->elems_total,
@@ -116,12 +150,20 @@ int run_transaction(const gdn_dims *dims, int32_t num_layers, int32_t row_capaci
     if (timing) cudaEventRecord(ev[5], s);
     *txn = t;
     int32_t *ho = io->host_out;
-    if (cudaMemcpyAsync(ho, io->accept_len, size_t(B) * 4, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
-        cudaMemcpyAsync(ho + n_reqs, io->bonus, size_t(B) * 4, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
-        cudaMemcpyAsync(ho + 2 * n_reqs, io->out_tokens, size_t(rows) * 4, cudaMemcpyDeviceToHost, s) !=
-            cudaSuccess ||
-        cudaStreamSynchronize(s) != cudaSuccess)
-        return fail(GDN_ERR_CUDA);
+    int32_t *ho_dev = mapped(ho);
+    bool moved = false;
+    if (ho_dev) {
+        Spans sp{{io->accept_len, io->bonus, io->out_tokens}, {ho_dev, ho_dev + n_reqs, ho_dev + 2 * n_reqs},
+                 {B, B, rows}};
+        move_spans_kernel<<<1, 256, 0, s>>>(sp);
+        moved = cudaGetLastError() == cudaSuccess;
+    } else {
+        moved = cudaMemcpyAsync(ho, io->accept_len, size_t(B) * 4, cudaMemcpyDeviceToHost, s) == cudaSuccess &&
+                cudaMemcpyAsync(ho + n_reqs, io->bonus, size_t(B) * 4, cudaMemcpyDeviceToHost, s) == cudaSuccess &&
+                cudaMemcpyAsync(ho + 2 * n_reqs, io->out_tokens, size_t(rows) * 4, cudaMemcpyDeviceToHost, s) ==
+                    cudaSuccess;
+    }
+    if (!moved || cudaStreamSynchronize(s) != cudaSuccess) return fail(GDN_ERR_CUDA);
     if (timing) {
         for (int i = 0; i < 3; ++i)
             if (cudaEventElapsedTime(&kernel_ms[i], ev[2 * i], ev[2 * i + 1]) != cudaSuccess) kernel_ms[i] = -1.f;
