@@ -464,6 +464,10 @@ int gdn_pool_abort(gdn_pool *pool, const gdn_plan *plan, int32_t n);
  * returned.  Blocks the host until the transaction is done (it waits for
  * `stream`, so it cannot be captured into a CUDA graph).
  * Device-detected errors accumulate in *io->dev_status as usual.
+ * The two host buffers must be page-locked; when they are mapped into the
+ * device address space (so with unified addressing) a one-block kernel moves
+ * the tables in and the results out, so neither waits behind a large copy
+ * the caller has queued on a copy engine; otherwise cudaMemcpyAsync does.
  */
 typedef struct gdn_decode_io {
     int32_t *tables;                  /* device [3][n_reqs+1] */
