@@ -60,8 +60,8 @@ WORKLOAD_TEXT = {
 # DRAM traffic of one gdn_verify launch from an ncu capture (dram__bytes_read.sum + dram__bytes_write.sum)
 # on the full paged256 workload (profiles/dram_verify_paged256.md); reported only while the kernel source
 # is the one that was captured (its digest), otherwise null.
-TRAFFIC = {"gdn_verify": {"src_sha": "3fdbecb81ca3fcf0", "workload": "paged256",
-                          "bytes_per_launch": 554256384 + 2094016512, "alg_bytes_per_launch": 2709782528}}
+TRAFFIC = {"gdn_verify": {"src_sha": "ceb52e182cbc4f89", "workload": "paged256",
+                          "bytes_per_launch": 554062080 + 2093852416, "alg_bytes_per_launch": 2709782528}}
 
 
 def src_digest(path):

@@ -170,8 +170,10 @@ __device__ __forceinline__ float4 bf16x4_to_f32(uint2 w) {
                        __uint_as_float(w.y & 0xffff0000u));
 }
 
+// Four CTAs per SM; replay (bound by its per-token chain rather than by HBM)
+// is held to 48 registers so that five fit (its shared memory allows five).
 template <int DK, int MODE>
-__global__ void __launch_bounds__(kThreads, 4) gdn_recurrent_kernel(const RecArgs a) {
+__global__ void __launch_bounds__(kThreads, MODE == kReplay ? 5 : 4) gdn_recurrent_kernel(const RecArgs a) {
     using L = Lay<DK>;
     constexpr bool VERIFY = (MODE == kVerify || MODE == kVerifyAt);
     constexpr bool AT = (MODE == kVerifyAt);
