@@ -103,3 +103,33 @@ def test_decode_transaction_checks_arguments_before_planning(lib):
     assert st == gs.GDN_ERR_ARG
     assert (pool.refcount == before[0]).all() and pool.free_list() == before[1] and txn.value == 7
     assert reqs[0].slot == held and reqs[0].cur_len == 1
+
+
+def test_arena_transaction_needs_every_request(lib):
+    """gdn_decode_transaction_at keeps one location per request and layer:
+    a plan that leaves a request out (row budget too small) is undone before
+    anything is launched, and the pool keeps its slots."""
+    from speculative_decoding_hybrid_gb300 import binding as gs
+    d = gs.dims(2, 4, 16, 16)
+    pool = gs.Pool(4)
+    held = [pool.alloc(), pool.alloc()]
+    plan = gs.Plan(2)
+    reqs = (gs.gdn_req * 2)()
+    for i in range(2):
+        reqs[i] = gs.gdn_req(gs.REQ_DECODE, 3, 0, 1, 1 << 20, held[i])
+    lim = gs.gdn_plan_limits(4, 2, 3)        # room for one request of 4 rows only
+    txn = ctypes.c_uint32(3)
+    io = gs.gdn_decode_io()
+    for name, _ in gs.gdn_decode_io._fields_:
+        if name not in ("slot_stride", "layer_stride", "num_slots", "ckpt_layer_stride", "o_layer_stride", "vocab",
+                        "logit_row_stride", "workspace_bytes"):
+            setattr(io, name, 16)
+    ar = gs.gdn_arena_io()
+    ar.arena, ar.loc, ar.elems_total = 16, 16, 1 << 20
+    before = (pool.refcount.copy(), pool.free_list())
+    st = gs.lib.gdn_decode_transaction_at(ctypes.byref(d), 1, 8, reqs, 2, ctypes.byref(lim), ctypes.byref(pool.c),
+                                          ctypes.byref(plan.c), ctypes.byref(txn), ctypes.byref(io), ctypes.byref(ar),
+                                          None, None)
+    assert st == gs.GDN_ERR_ARG
+    assert (pool.refcount == before[0]).all() and sorted(pool.free_list()) == sorted(before[1])
+    assert txn.value == 3 and [reqs[i].slot for i in range(2)] == held
