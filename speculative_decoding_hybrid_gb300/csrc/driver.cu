@@ -46,7 +46,7 @@ thread_local StepEvents t_events;
 // Small host <-> device table moves by a kernel over page-locked host memory
 // mapped into the device address space, so that they never queue behind a
 // large copy the caller has put on a copy engine (the next transaction's
-// inputs, say).  Three spans of n0, n1, n2 int32 (n0 + n1 + n2 <= 3 * span).
+// inputs, say): three spans of n[k] int32 each, copied by one block.
 struct Spans {
     const int32_t *src[3];
     int32_t *dst[3];
