@@ -967,7 +967,9 @@ def main():
         "kernels_ms": {"gdn_verify": v_ms, "mtp_greedy_accept": a_ms, "gdn_commit": c_ms,
                        "commit_gbs": cbytes / args.steps / (c_ms * 1e-3) / 1e9,
                        "accept_gbs": abytes / args.steps / (a_ms * 1e-3) / 1e9},
-        "gpu_launches": args.steps * (spec.layers + 3),
+        # per step: every layer's verify, the two accept kernels, the commit,
+        # and with the host driver its two table-moving kernels
+        "gpu_launches": args.steps * (spec.layers + 3 + (2 if native_driver else 0)),
         "clocks": clocks,
         "e2e": e2e,
         "cpu_baseline": cpu,
