@@ -57,16 +57,41 @@ WORKLOAD_TEXT = {
     "small": "ncu case: 32 requests, 64 slots, 2 layers, K=3",
 }
 
-# DRAM traffic of one gdn_verify launch from an ncu capture (dram__bytes_read.sum + dram__bytes_write.sum)
-# on the full paged256 workload (profiles/dram_verify_paged256.md); reported only while the kernel source
-# is the one that was captured (its digest), otherwise null.
-TRAFFIC = {"gdn_verify": {"src_sha": "ceb52e182cbc4f89", "workload": "paged256",
-                          "bytes_per_launch": 554062080 + 2093852416, "alg_bytes_per_launch": 2709782528}}
+METRIC = "verified tokens/s and GDN verify+commit HBM GB/s (% of GB300 peak)"
+HBM_SPEC_GBS = 7900.0   # nominal HBM3e bandwidth of one GB300, for context beside the measured peak
 
 
 def src_digest(path):
     with open(path, "rb") as f:
         return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def committed_traffic(kernel: str, src_path: str):
+    """DRAM traffic of one launch of ``kernel`` from the committed ncu summary
+    under profiles/ (a line ``traffic: kernel=K src_sha=H workload=W
+    alg_bytes_per_launch=A dram_bytes_per_launch=D``, written from a small-case
+    capture).  Returns (dram/alg ratio, note); the ratio is None, with the
+    reason, when no summary holds one or the kernel source changed since."""
+    import glob
+    want = src_digest(src_path)
+    found = None
+    for f in sorted(glob.glob(os.path.join(ROOT, "profiles", "*.md"))):
+        with open(f) as fh:
+            for ln in fh:
+                ln = ln.strip().strip("`")
+                if not ln.startswith("traffic:"):
+                    continue
+                kv = dict(x.split("=", 1) for x in ln[len("traffic:"):].split() if "=" in x)
+                if kv.get("kernel") == kernel:
+                    found = (kv, os.path.basename(f))
+    if found is None:
+        return None, "no committed ncu DRAM capture of %s" % kernel
+    kv, fname = found
+    if kv.get("src_sha") != want:
+        return None, "%s changed since the DRAM capture in profiles/%s" % (os.path.basename(src_path), fname)
+    ratio = float(kv["dram_bytes_per_launch"]) / float(kv["alg_bytes_per_launch"])
+    return ratio, "profiles/%s: %s workload, DRAM/algorithmic bytes %.4f, scaled to this launch's bytes" % (
+        fname, kv.get("workload", "?"), ratio)
 
 
 def prefill_flops(lengths, h_v, d=128, C=64):
@@ -568,6 +593,76 @@ def run_zero_copy(spec, dev, args, replay=False, graph=False):
     return res
 
 
+def run_workload_block(spec, dev, warmup=5, steps=None):
+    """Another decode workload timed like the headline line (copy commit through
+    gdn_decode_transaction, event-timed verify/commit), for the line's
+    secondary blocks: verified tokens/s and the verify+commit HBM fraction."""
+    b = Bench(spec, dev, 0)
+    steps = steps or spec.steps
+    b.precompute_drafts(warmup + steps)
+    for _ in range(warmup):
+        b.step()
+    torch.cuda.synchronize()
+    ev = {}
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record()
+    tok = vbytes = cbytes = 0
+    for _ in range(steps):
+        n, p = b.step(ev)
+        tok += n
+        v, c, _ = b.step_bytes(p)
+        vbytes += v
+        cbytes += c
+    end.record()
+    torch.cuda.synchronize()
+    ms = start.elapsed_time(end)
+    if int(b.vs.status.item()) != 0:
+        raise RuntimeError("%s loop status %d" % (spec.name, int(b.vs.status.item())))
+    v_ms, n_ver = per_launch_ms(ev, "verify")
+    c_ms, _ = per_launch_ms(ev, "commit")
+    peak, _ = load_peaks()
+    gbs = (vbytes + cbytes) / ((v_ms * n_ver + c_ms * steps) * 1e-3) / 1e9
+    res = {"workload": spec.name, "desc": WORKLOAD_TEXT.get(spec.name, spec.name), "value": tok / (ms * 1e-3),
+           "unit": "verified tokens/s", "steps": steps, "ms_per_step": ms / steps,
+           "verify_ms_per_launch": v_ms, "commit_ms": c_ms, "verify_commit_gbs": gbs,
+           "verify_commit_frac": gbs / peak, "verify_commit_frac_of_spec": gbs / HBM_SPEC_GBS,
+           "driver": "gdn_decode_transaction"}
+    del b
+    torch.cuda.empty_cache()
+    return res
+
+
+def bench_accept_logits(b: Bench, reps=20):
+    """mtp_greedy_accept over every row of the batch on logits as the workload
+    states them (N(0, 2^2), nothing planted) beside the benchmark's ring
+    logits (one target per row planted at +16 so the greedy choice is known
+    by construction).  Both 311 MB sets are larger than L2."""
+    vs, loop = b.vs, b.loop
+    B = loop.B
+    R = int(loop.d_tab[0, B].item())
+    g = sy.generator(sy.mix_seed(b.spec.seed, 4040), b.dev)
+    plain = torch.empty((b.cap, b.spec.vocab), dtype=torch.float32, device=b.dev)
+    plain.normal_(0.0, b.spec.logit_std, generator=g)
+    lg_plain = plain.to(torch.bfloat16)
+    del plain
+    out = {"rows": R, "vocab": b.spec.vocab}
+    for name, lg in (("stated_N(0,4)", lg_plain), ("planted_ring", b.logits[0])):
+        for _ in range(3):
+            vs.accept(B, loop.cu_rows, lg, b.tok_d)
+        torch.cuda.synchronize()
+        a, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(reps):
+            vs.accept(B, loop.cu_rows, lg, b.tok_d)
+        e.record()
+        torch.cuda.synchronize()
+        ms = a.elapsed_time(e) / reps
+        out[name] = {"ms": ms, "gbs": R * b.spec.vocab * 2 / (ms * 1e-3) / 1e9}
+    del lg_plain
+    torch.cuda.empty_cache()
+    return out
+
+
 def _packed_layout(b: Bench):
     """Byte offsets of every layer's row inputs and the logits in one packed
     buffer (each piece 256-byte aligned)."""
@@ -782,7 +877,7 @@ def run_reference(args, spec):
         tok += oracle_sample_step(spec, args.warmup + s, n_req)
     dt = time.perf_counter() - t0
     val = tok / dt
-    line = {"impl": "reference", "metric": "verified tokens/s", "value": val, "unit": "verified tokens/s",
+    line = {"impl": "reference", "metric": METRIC, "value": val, "unit": "verified tokens/s",
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000 * dt / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": args.workload, "desc": WORKLOAD_TEXT[args.workload],
@@ -807,6 +902,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-prefill", action="store_true")
+    ap.add_argument("--no-cb16", action="store_true",
+                    help="skip the continuous-batch (cb16) block that runs after the paged256 line's loop")
     ap.add_argument("--zero-copy", dest="zero_copy", action="store_true", default=True,
                     help="also time the zero-copy commit (state arena) on the same workload")
     ap.add_argument("--no-zero-copy", dest="zero_copy", action="store_false")
@@ -889,9 +986,8 @@ def main():
     achieved = v_per_launch / (v_ms * 1e-3) / 1e9
     vc_gbs = (vbytes + cbytes) / ((v_ms * n_ver_launch + c_ms * args.steps) * 1e-3) / 1e9
     src = os.path.join(ROOT, "speculative_decoding_hybrid_gb300", "csrc", "gdn_recurrent.cu")
-    tr = TRAFFIC.get("gdn_verify")
-    traffic = tr["bytes_per_launch"] * (v_per_launch / tr["alg_bytes_per_launch"]) \
-        if tr and tr["src_sha"] == src_digest(src) and tr.get("workload") == args.workload else None
+    ratio, traffic_note = committed_traffic("gdn_verify", src)
+    traffic = ratio * v_per_launch if ratio is not None else None
 
     l2desc = "inputs larger than L2: state pool %.1f GiB, checkpoints %.1f GiB, ring of %d input sets" % (
         b.vs.pool.numel() * 4 / 2 ** 30, b.vs.ckpt.numel() * 4 / 2 ** 30, spec.ring)
@@ -927,10 +1023,16 @@ def main():
     if not args.no_prefill and args.workload == "paged256":
         prefill = guarded(bench_prefill, dev, sy.prefill_lengths())
         mixed = guarded(bench_mixed, dev, sy.prefill_lengths())
-    zero_copy = replay = replay_graph = None
+    accept_plain = None
+    if world == 1:
+        accept_plain = guarded(bench_accept_logits, b)
+    zero_copy = replay = replay_graph = cb16 = None
     if (args.zero_copy or args.replay) and world == 1:
         del b
         torch.cuda.empty_cache()
+        if args.workload == "paged256" and not args.no_cb16:
+            cb16 = guarded(run_workload_block, WORKLOADS["cb16"], dev, warmup=args.warmup)
+            torch.cuda.empty_cache()
         if args.replay:
             replay = guarded(run_zero_copy, spec, dev, args, replay=True)
             torch.cuda.empty_cache()
@@ -942,7 +1044,7 @@ def main():
     if not args.no_cpu_baseline and world == 1:
         cpu = guarded(cpu_baseline, spec)
     line = {
-        "metric": "verified tokens/s and GDN verify+commit HBM GB/s (% of GB300 peak)",
+        "metric": METRIC,
         "value": tok_all / (ms * 1e-3),
         "unit": "verified tokens/s",
         "n_gpus": world,
@@ -961,19 +1063,23 @@ def main():
                    "parallelism": "replicas (requests sharded, no collective)" if world > 1 else "single GPU"},
         "verify_commit_gbs": vc_gbs,
         "verify_commit_frac": vc_gbs / peak,
+        "verify_commit_frac_of_spec": vc_gbs / HBM_SPEC_GBS,
         "roofline": {"bound": "hbm", "kernel": "gdn_verify", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "traffic": traffic, "peak_source": peak_kind,
+                     "frac": achieved / peak, "traffic": traffic, "traffic_source": traffic_note,
+                     "peak_source": peak_kind, "peak_spec": HBM_SPEC_GBS, "frac_of_spec": achieved / HBM_SPEC_GBS,
                      "alg_bytes_per_launch": v_per_launch, "avg_launch_ms": v_ms},
         "kernels_ms": {"gdn_verify": v_ms, "mtp_greedy_accept": a_ms, "gdn_commit": c_ms,
                        "commit_gbs": cbytes / args.steps / (c_ms * 1e-3) / 1e9,
                        "accept_gbs": abytes / args.steps / (a_ms * 1e-3) / 1e9},
         # per step: every layer's verify, the two accept kernels, the commit,
-        # and with the host driver its two table-moving kernels
-        "gpu_launches": args.steps * (spec.layers + 3 + (2 if native_driver else 0)),
+        # and with the host driver its commit gate and two table-moving kernels
+        "gpu_launches": args.steps * (spec.layers + 3 + (3 if native_driver else 0)),
         "clocks": clocks,
         "e2e": e2e,
         "cpu_baseline": cpu,
         "acceptance": {"verified_tokens": tok, "requests": spec.batch},
+        "accept_stated_logits": accept_plain,
+        "cb16": cb16,
         "prefill": prefill,
         "mixed_transaction": mixed,
         "zero_copy_commit": zero_copy,

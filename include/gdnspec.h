@@ -72,7 +72,8 @@ enum {
     GDN_ERR_DUP_SLOT = -4,   /* two requests would write one slot */
     GDN_ERR_NO_SLOT = -5,    /* free list empty */
     GDN_ERR_CUDA = -6,       /* a CUDA launch or query failed */
-    GDN_ERR_WORKSPACE = -7   /* workspace missing or too small */
+    GDN_ERR_WORKSPACE = -7,  /* workspace missing or too small */
+    GDN_ERR_REFUSED = -8     /* a device-side check refused a driven transaction; nothing committed */
 };
 
 /* Bits of *dev_status */
@@ -200,7 +201,9 @@ int mtp_greedy_accept(int32_t B, int32_t row_capacity, const int32_t *cu_rows,
  *   that overlap on the GPU race on the scratch: order them on one stream.
  *   The first call on a device resolves the array's address with that device
  *   current (make it before any stream capture); the stream must belong to
- *   the current device.  No call allocates or frees memory.
+ *   the current device.  No call allocates or frees memory.  The resolved
+ *   address is kept for the life of the process: after a cudaDeviceReset
+ *   of that device it is stale, so do not call this entry point there again.
  */
 int mtp_greedy_accept_noalloc(int32_t B, int32_t row_capacity, const int32_t *cu_rows,
                               const gdn_bf16 *logits, int64_t vocab, int64_t row_stride,
@@ -454,9 +457,20 @@ int gdn_pool_abort(gdn_pool *pool, const gdn_plan *plan, int32_t n);
  * 2*n_reqs..); a wait for `stream`; gdn_pool_apply; then for every decoded
  * request i: reqs[i].slot = its destination slot and reqs[i].cur_len +=
  * accept_len + 1.  *txn is the transaction counter (incremented).
+ * The commit is all or nothing: before it, one small kernel checks every
+ * (request, layer) pair as gdn_commit would (checkpoint tag of this
+ * transaction, accept length, destination slot, rows) and that no bounded
+ * wait ran out (GDN_DEV_TIMEOUT, which stays set until the caller clears
+ * *dev_status: results computed after it are not trusted).  If any check
+ * fails, the cause is set in *dev_status, every accept_len becomes -1, no
+ * state is written, and the call returns GDN_ERR_REFUSED after undoing the
+ * plan: the pool, reqs and *txn are left as they were ([NATIVE] Results:
+ * recovery after abort), so the zero-copy form below keeps writing its
+ * checkpoints into the area the locations do not point into.
  * ckpt_tag holds num_layers x B tags (B = decode requests of the plan).
  * kernel_ms (host, 3 floats, or NULL): device time of the verify launches of
- * all layers, of the accept and of the commit, from events on `stream`.
+ * all layers, of the accept and of the commit with its check, from events
+ * on `stream`.
  * Decode requests only: a request list holding a prefill returns
  * GDN_ERR_ARG before anything is planned.  A plan that selects no request,
  * or a call that fails after planning, is undone with gdn_pool_abort (its

@@ -21,7 +21,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libgdnspec.so")
 
 GDN_OK, GDN_ERR_NULL, GDN_ERR_SHAPE, GDN_ERR_ARG = 0, -1, -2, -3
-GDN_ERR_DUP_SLOT, GDN_ERR_NO_SLOT, GDN_ERR_CUDA, GDN_ERR_WORKSPACE = -4, -5, -6, -7
+GDN_ERR_DUP_SLOT, GDN_ERR_NO_SLOT, GDN_ERR_CUDA, GDN_ERR_WORKSPACE, GDN_ERR_REFUSED = -4, -5, -6, -7, -8
 DEV_SLOT_OOR, DEV_ROWS_BAD, DEV_TOKEN_OOR, DEV_CKPT_UNWRITTEN, DEV_ACCEPT_BAD, DEV_TIMEOUT = 1, 2, 4, 8, 16, 32
 K_MAX = 15
 MAX_ROWS = K_MAX + 1

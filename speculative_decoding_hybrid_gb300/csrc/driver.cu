@@ -17,6 +17,17 @@
 
 #include "gdnspec.h"
 
+// The all-or-nothing commit of a driven transaction (gdn_commit.cu): a gate
+// kernel checks every (request, layer) pair first and, if any fails, sets
+// every accept length to -1 so that nothing is committed.
+int gdn_gated_commit(const gdn_dims *dims, int32_t B, int32_t num_layers, int32_t row_capacity,
+                     const int32_t *cu_rows, int32_t *accept_len, const float *ckpt, int64_t ckpt_layer_stride,
+                     const uint64_t *ckpt_tag, uint32_t txn, float *pool, int64_t slot_stride, int64_t layer_stride,
+                     int32_t num_slots, const int32_t *dst_slot, uint32_t *dev_status, void *stream);
+int gdn_gated_commit_at(const gdn_dims *dims, int32_t B, int32_t num_layers, int32_t row_capacity,
+                        const int32_t *cu_rows, int32_t *accept_len, int64_t ckpt_off, int64_t ckpt_layer_stride,
+                        const uint64_t *ckpt_tag, uint32_t txn, int64_t *loc, uint32_t *dev_status, void *stream);
+
 namespace {
 
 // Six timing events per host thread and device, created on first use.
@@ -139,16 +150,18 @@ int run_transaction(const gdn_dims *dims, int32_t num_layers, int32_t row_capaci
         cudaEventRecord(ev[3], s);
         cudaEventRecord(ev[4], s);
     }
+    // All or nothing: a device-detected problem anywhere in the transaction
+    // (a stale or missing checkpoint, a bad accept length or slot, a wait
+    // that ran out) commits no pair at all and marks every accept length -1.
     if (arena)
-        st = gdn_commit_at(dims, B, num_layers, row_capacity, cu, io->accept_len, area, io->ckpt_layer_stride,
-                           io->ckpt_tag, t, arena->loc, io->dev_status, stream);
+        st = gdn_gated_commit_at(dims, B, num_layers, row_capacity, cu, io->accept_len, area,
+                                 io->ckpt_layer_stride, io->ckpt_tag, t, arena->loc, io->dev_status, stream);
     else
-        st = gdn_commit(dims, B, num_layers, row_capacity, cu, io->accept_len, io->ckpt, io->ckpt_layer_stride,
-                        io->ckpt_tag, t, io->pool, io->slot_stride, io->layer_stride, io->num_slots, dst,
-                        io->dev_status, stream);
+        st = gdn_gated_commit(dims, B, num_layers, row_capacity, cu, io->accept_len, io->ckpt,
+                              io->ckpt_layer_stride, io->ckpt_tag, t, io->pool, io->slot_stride, io->layer_stride,
+                              io->num_slots, dst, io->dev_status, stream);
     if (st != GDN_OK) return fail(st);
     if (timing) cudaEventRecord(ev[5], s);
-    *txn = t;
     int32_t *ho = io->host_out;
     int32_t *ho_dev = mapped(ho);
     bool moved = false;
@@ -168,15 +181,21 @@ int run_transaction(const gdn_dims *dims, int32_t num_layers, int32_t row_capaci
         for (int i = 0; i < 3; ++i)
             if (cudaEventElapsedTime(&kernel_ms[i], ev[2 * i], ev[2 * i + 1]) != cudaSuccess) kernel_ms[i] = -1.f;
     }
+    // A refused transaction committed nothing: its fresh slots return to the
+    // pool and the requests, the pool and the transaction counter stay as
+    // they were (in the zero-copy form the next transaction then writes the
+    // same checkpoint area again, never the one the locations point into).
+    for (int32_t j = 0; j < B; ++j)
+        if (ho[j] < 0) return fail(GDN_ERR_REFUSED);
+    *txn = t;
     // The commit is done: requests that moved release their old slot, and
     // every decode request advances by its accepted drafts plus the bonus.
     st = gdn_pool_apply(pool, plan, n_reqs);
     if (st != GDN_OK) return st;
     for (int32_t j = 0; j < B; ++j) {
         const int32_t i = plan->dec_req[j];
-        const int32_t acc = ho[j];
         reqs[i].slot = plan->dst[i];
-        if (acc >= 0) reqs[i].cur_len += acc + 1;
+        reqs[i].cur_len += ho[j] + 1;
     }
     return GDN_OK;
 }

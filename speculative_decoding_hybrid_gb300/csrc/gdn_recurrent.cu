@@ -83,9 +83,13 @@ struct RecArgs {
     uint32_t *status;
     int32_t B, h_qk, h_v, dv, row_capacity, grp, bph;
     float q_scale;
-    // The previous launch on the stream writes none of the tables or slots
-    // this one reads (a later layer of a multi-layer call): the tables and
-    // the state tile are read before waiting for that launch to finish.
+    // A later layer of a multi-layer call: the tables and this layer's state
+    // tile are read before waiting for the previous layer's launch.  That is
+    // safe because the previous layers write neither, and because the first
+    // layer's launch (not early) does not let its successor start before
+    // every earlier launch on the stream -- the commit that wrote the slots
+    // -- has completed: a launch can only start once its predecessor has
+    // started, so every later layer starts after that point too.
     int32_t early;
 };
 
@@ -188,8 +192,17 @@ __global__ void __launch_bounds__(kThreads, MODE == kReplay ? 5 : 4) gdn_recurre
     float *vsm = reinterpret_cast<float *>(smem + (REPLAY ? L::kVOffR : L::kVOff));
     float *gsm = reinterpret_cast<float *>(smem + (REPLAY ? L::kGOffR : L::kGOff));
     float *bsm = gsm + GDN_MAX_ROWS;
-    gdn::pdl_launch_dependents();
-    if (!a.early) gdn::pdl_wait();  // otherwise after the tile's copy has started
+    // Programmatic dependent launch.  A first (non-early) launch waits for
+    // everything before it on the stream (a commit writing the slots, say)
+    // before it lets the next launch start; an early launch (a later layer of
+    // a multi-layer call) lets the next layer start at once and waits only
+    // once its own state tile's copy is under way (see RecArgs::early).
+    if (a.early) {
+        gdn::pdl_launch_dependents();
+    } else {
+        gdn::pdl_wait();
+        gdn::pdl_launch_dependents();
+    }
 
     const int tid = threadIdx.x;
     const int bid = blockIdx.x;
@@ -683,10 +696,11 @@ extern "C" int gdn_verify_replay(const gdn_dims *dims, int32_t B, int32_t row_ca
 
 // Multi-layer issue of the per-layer verify calls: one host call walks the
 // layers in order and makes the same calls a caller would make layer by
-// layer (same kernels, arguments and stream).  A layer after the first
-// follows the previous layer's launch, which writes none of the tables or
-// slots it reads, so it may read those and start its state tile's copy
-// before that launch has finished (the rows still wait for it).
+// layer (same kernels, arguments and stream).  A layer after the first may
+// read its tables and start its state tile's copy before the previous
+// layer's launch has finished (the rows still wait for it): the layers
+// write none of them, and the first layer lets no successor start until
+// every launch queued before the call (a commit, a prefill) is complete.
 extern "C" int gdn_verify_layers(const gdn_dims *dims, int32_t num_layers, int32_t B, int32_t row_capacity,
                                  const int32_t *cu_rows, const gdn_layer_rows *rows, const float *pool,
                                  int64_t slot_stride, int64_t layer_stride, int32_t num_slots,

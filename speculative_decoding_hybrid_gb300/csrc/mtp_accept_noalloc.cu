@@ -21,6 +21,8 @@
 //  * The first call on a device looks up the array's device address with
 //    cudaGetSymbolAddress (with that device current) and caches it; make that
 //    first call before any stream capture.  No call allocates or frees memory.
+//    The cached address is not refreshed: after a cudaDeviceReset of that
+//    device it is stale, and the entry point must not be called there again.
 #include <mutex>
 
 #include "common.cuh"

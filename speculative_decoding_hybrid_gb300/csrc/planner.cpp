@@ -240,6 +240,7 @@ extern "C" const char *gdn_status_string(int status) {
         case GDN_ERR_NO_SLOT: return "no free slot";
         case GDN_ERR_CUDA: return "CUDA error";
         case GDN_ERR_WORKSPACE: return "workspace missing or too small";
+        case GDN_ERR_REFUSED: return "transaction refused by a device-side check; nothing committed";
         default: return "unknown status";
     }
 }

@@ -76,3 +76,75 @@ def test_native_transaction_refuses_a_prefill(gs, cuda_dev):
     loop.req_np[0] = before[2][0]
     assert np.array_equal(loop.req_np, before[2])
     assert b.vs.txn == 0
+
+
+def _snapshot(b, arena):
+    return (b.pool_c.refcount.copy(), b.pool_c.free_list(), b.loop.req_np.copy(), b.vs.txn,
+            b.vs.pool.clone(), b.vs.loc.clone() if arena else None)
+
+
+def _assert_unchanged(b, arena, before):
+    ref, free, req, txn, pool, loc = before
+    assert np.array_equal(b.pool_c.refcount, ref) and b.pool_c.free_list() == free
+    keep = [0, 2, 3, 4, 5]                      # all but k_draft, which the step itself sets before the call
+    assert np.array_equal(b.loop.req_np[:, keep], req[:, keep])
+    assert b.vs.txn == txn and b.loop._txn.value == txn
+    assert torch.equal(b.vs.pool, pool)
+    if arena:
+        assert torch.equal(b.vs.loc, loc)
+
+
+@pytest.mark.parametrize("arena", [False, True])
+def test_native_transaction_refused_on_device_commits_nothing(gs, cuda_dev, arena):
+    """A problem only the device sees makes the host driver refuse the whole
+    transaction ([NATIVE] Results, recovery after abort): no state, slot or
+    location is written, the slot pool, the requests and the transaction
+    counter are left as they were, every accept length reads -1, and the
+    status word names the cause.  Two injected causes, both made on the
+    host: a bounded wait reported as run out (GDN_DEV_TIMEOUT already in the
+    status word), and a start state the device finds out of range.  After
+    the status word is cleared the same loop goes on and commits."""
+    import bench
+    b = bench.Bench(SPEC, cuda_dev, arena=arena)
+    b.precompute_drafts(4)
+    b.step()                                   # one committed transaction first (COW moves included)
+    torch.cuda.synchronize()
+    loop = b.loop
+    B = loop.B
+
+    before = _snapshot(b, arena)
+    b.vs.status.fill_(gs.DEV_TIMEOUT)
+    with pytest.raises(gs.GdnError) as e:
+        b.native_step()
+    torch.cuda.synchronize()
+    assert e.value.status == gs.GDN_ERR_REFUSED
+    assert int(b.vs.status.item()) & gs.DEV_TIMEOUT
+    assert (b.vs.accept_len[:B] == -1).all()
+    _assert_unchanged(b, arena, before)
+
+    b.vs.status.zero_()
+    if arena:
+        saved = b.vs.loc[1, 3].clone()
+        b.vs.loc[1, 3] = -4                     # layer 1 of request 3 points outside the arena
+    else:
+        saved = loop._io.num_slots
+        loop._io.num_slots = int(max(loop.slot)) # the request on the highest slot is out of range
+    before = _snapshot(b, arena)
+    with pytest.raises(gs.GdnError) as e:
+        b.native_step()
+    torch.cuda.synchronize()
+    assert e.value.status == gs.GDN_ERR_REFUSED
+    st = int(b.vs.status.item())
+    assert st & gs.DEV_SLOT_OOR and st & gs.DEV_CKPT_UNWRITTEN
+    assert (b.vs.accept_len[:B] == -1).all()
+    _assert_unchanged(b, arena, before)
+    if arena:
+        b.vs.loc[1, 3] = saved
+    else:
+        loop._io.num_slots = saved
+
+    b.vs.status.zero_()
+    n, p = b.step()                            # the loop goes on from where it was
+    torch.cuda.synchronize()
+    assert int(b.vs.status.item()) == 0 and n > 0
+    assert b.vs.txn == before[3] + 1

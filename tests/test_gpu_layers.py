@@ -113,3 +113,48 @@ def test_verify_replay_layers_matches_per_layer_calls(gs, cuda_dev):
     assert torch.equal(a.o[:, :R], b.o[:, :R])
     assert torch.equal(a.pool, b.pool)
     assert not torch.equal(b.pool, pool)                                    # the replay wrote the slots
+
+
+def test_commit_then_verify_layers_back_to_back(gs, cuda_dev):
+    """A commit followed at once (same stream, nothing in between) by a
+    multi-layer verify on a batch small enough for one wave: every layer,
+    the later ones included, must start from the committed state.  Checked
+    against the FP64 oracle run from the committed checkpoints and bit for
+    bit against the same calls with a device synchronisation in between."""
+    import oracle
+    from gpu_util import state_err, out_err
+    dims = sy.DIMS_FULL
+    d = gs.dims(dims.h_qk, dims.h_v, dims.d_k, dims.d_v)
+    Lb, rows_n, j = 3, 4, 2
+    cu = torch.tensor([0, rows_n], dtype=torch.int32, device=cuda_dev)
+    slot = torch.zeros(1, dtype=torch.int32, device=cuda_dev)
+    from speculative_decoding_hybrid_gb300.step import LayerRows, VerifyStep
+    steps = [[LayerRows(*(t for t in (r.q, r.k, r.v, r.g, r.beta)))
+              for r in (sy.rows(sy.generator(900 + 10 * s + l), rows_n, dims, cuda_dev) for l in range(Lb))]
+             for s in range(2)]
+    pool0 = sy.state(sy.generator(950), (1, Lb, dims.h_v, dims.d_v, dims.d_k)).to(cuda_dev)
+    results = []
+    for sync in (False, True):
+        vs = VerifyStep(d, Lb, 1, rows_n, 1, 64, cuda_dev, pool=pool0.clone())
+        vs.accept_len.fill_(j)
+        vs.txn = 1
+        vs.verify_all(1, cu, slot, steps[0])
+        vs.commit(1, cu, slot)
+        if sync:
+            torch.cuda.synchronize()
+        vs.txn = 2
+        vs.verify_all(1, cu, slot, steps[1])
+        torch.cuda.synchronize()
+        assert int(vs.status.item()) == 0
+        results.append((vs.ckpt[:, :rows_n].clone(), vs.o[:, :rows_n].clone(), vs.pool.clone()))
+    assert torch.equal(results[0][0], results[1][0]) and torch.equal(results[0][1], results[1][1])
+    ck, o, pool = results[0]
+    for l in range(Lb):
+        h0 = [t.cpu() for t in (steps[0][l].q, steps[0][l].k, steps[0][l].v, steps[0][l].g, steps[0][l].beta)]
+        _, _, ck0 = oracle.gdn_recurrent(*h0, pool0[0, l].cpu(), 1.0, want_ckpt=True)
+        committed = ck0[j]
+        assert state_err(pool[0, l].cpu().numpy(), committed) <= 1.0
+        h1 = [t.cpu() for t in (steps[1][l].q, steps[1][l].k, steps[1][l].v, steps[1][l].g, steps[1][l].beta)]
+        _, o_ref, ck1 = oracle.gdn_recurrent(*h1, torch.from_numpy(committed), 1.0, want_ckpt=True)
+        assert state_err(ck[l].cpu().numpy(), ck1) <= 1.0, l
+        assert out_err(o[l], o_ref) <= 1.0, l
