@@ -105,6 +105,25 @@ def prefill_flops(lengths, h_v, d=128, C=64):
     return tot * h_v
 
 
+# MMA work the prefill kernel issues per (chunk, v-head), in units of one
+# M128 x N64 x K16 bf16 product (2 * 128 * 64 * 16 flop): phase A 40 (S W^T
+# three split terms, S Q^T two, over K = 128), [K;Q] K^T 8, phase B 28
+# (U^T P^T three terms, (U^T diag(dec)) K two terms at N = 128, K = 64), W^T
+# and Ut^T 16 (two terms each).  Split terms and padding rows count; the
+# algorithmic flops do not.
+PREFILL_MMA_UNITS_PER_CHUNK = 92
+PREFILL_MMA_UNIT_FLOP = 2 * 128 * 64 * 16
+
+
+def load_tensor_peak():
+    """Dense bf16 tensor peak (TFLOP/s): the measured burst figure, else the fallback."""
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            return float(json.load(f)["bf16_tflops"])
+    return 1900.0
+
+
 PREFILL_SETS = {
     "prefill": None,                  # 8 sequences, log-uniform lengths in [512, 32768]
     "prefill_small": [2048, 2048, 2048, 2048],
@@ -149,9 +168,16 @@ def bench_prefill(dev, lengths, reps=5, warmup=3):
     flops = prefill_flops(lengths, dims.h_v)
     if int(st.item()) != 0:
         raise RuntimeError("prefill status %d" % int(st.item()))
+    chunks = sum((L + 63) // 64 for L in lengths)
+    issued = chunks * dims.h_v * PREFILL_MMA_UNITS_PER_CHUNK * PREFILL_MMA_UNIT_FLOP
+    bf16_peak = load_tensor_peak()
     return {"tokens": R, "sequences": n, "ms_per_call": ms, "tokens_per_s": R / (ms * 1e-3),
-            "alg_tflops": flops / (ms * 1e-3) / 1e12, "launches_per_call": 3,
-            "workspace_gb": ws_bytes / 1e9}
+            "alg_tflops": flops / (ms * 1e-3) / 1e12,
+            "tensor_frac_alg": flops / (ms * 1e-3) / 1e12 / bf16_peak,
+            "issued_mma_tflops": issued / (ms * 1e-3) / 1e12,
+            "tensor_frac_issued": issued / (ms * 1e-3) / 1e12 / bf16_peak,
+            "bf16_peak_tflops": bf16_peak, "launches_per_call": 2,
+            "workspace_bytes": ws_bytes}
 
 
 def bench_mixed(dev, lengths, n_decode=256, layers=30, reps=3, warmup=1, vocab=151936):

@@ -356,9 +356,15 @@ int gdn_verify_replay_layers(const gdn_dims *dims, int32_t num_layers, int32_t B
  * Work is ordered on `stream`, so a decode/verify queued after it on the
  * same stream reads the published state ([NATIVE] What changed).
  * max_seqlen (host, >= 0) is accepted for callers that track it; every
- * length is read from cu_seqlens on the device.
- * Workspace (gdn_prefill_workspace_bytes): 128.25 KB per (chunk slot, v-head)
- * for ceil(row_capacity / 64) + nseq chunk slots, plus small tables.
+ * length is read from cu_seqlens on the device.  d_k = d_v = 128 runs on the
+ * tensor cores (one CTA per sequence and v-head keeps the state on chip for
+ * the whole sequence; nothing but the final state and o is written).
+ * Workspace (gdn_prefill_workspace_bytes): the sequences' length order,
+ * nseq int32 (16-byte aligned).
+ * A sequence whose bounded wait ran out (GDN_DEV_TIMEOUT), and every sequence
+ * of a call made while *dev_status already holds GDN_DEV_TIMEOUT, publishes
+ * nothing: its destination slot keeps its bytes ([ENGINE] Correctness fix:
+ * never publish a state that was not computed in full).
  */
 size_t gdn_prefill_workspace_bytes(const gdn_dims *dims, int32_t nseq, int32_t row_capacity);
 int gdn_chunked_prefill(const gdn_dims *dims, int32_t nseq, int32_t row_capacity,
@@ -535,6 +541,21 @@ int gdn_decode_transaction_at(const gdn_dims *dims, int32_t num_layers, int32_t 
                               float *kernel_ms, void *stream);
 
 const char *gdn_status_string(int status);
+
+/* Failure-detection self-test of the chunked prefill: gdn_chunked_prefill
+ * (chunk 64) with every wait bounded by limit_ns (1 .. 1e9) of device time,
+ * and with the tensor copy of each sequence's last chunk of K and Q
+ * withheld, so that the wait for it runs out: every sequence sets
+ * GDN_DEV_TIMEOUT and publishes nothing.  (Test-only; it computes nothing
+ * a caller would use.) */
+int gdn_selftest_prefill_timeout(const gdn_dims *dims, int32_t nseq, int32_t row_capacity,
+                                 const int32_t *cu_seqlens,
+                                 const gdn_bf16 *q, const gdn_bf16 *k, const gdn_bf16 *v,
+                                 const float *g, const float *beta,
+                                 float *pool_layer, int64_t slot_stride, int32_t num_slots,
+                                 const int32_t *src_slot, const int32_t *dst_slot, gdn_bf16 *o,
+                                 void *workspace, size_t workspace_bytes,
+                                 uint32_t *dev_status, uint64_t limit_ns, void *stream);
 
 /* Failure-detection self-test: a kernel waits on an mbarrier that is never
  * completed, gives up after limit_ns (1 .. 1e9) of device time and sets

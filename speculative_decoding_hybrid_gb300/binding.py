@@ -34,7 +34,8 @@ EXPORTS = ["gdn_decode_step", "gdn_verify", "mtp_accept_workspace_bytes", "mtp_g
            "gdn_verify_replay_layers",
            "gdn_prefill_workspace_bytes", "gdn_chunked_prefill", "gdn_pool_init", "gdn_pool_alloc",
            "gdn_pool_share", "gdn_pool_release", "plan_transaction", "gdn_pool_apply", "gdn_pool_abort",
-           "gdn_decode_transaction", "gdn_decode_transaction_at", "gdn_status_string"]
+           "gdn_decode_transaction", "gdn_decode_transaction_at", "gdn_status_string",
+           "gdn_selftest_prefill_timeout"]
 
 
 class GdnError(RuntimeError):
@@ -137,6 +138,8 @@ def _load():
         "gdn_verify_at_layers": [DP, I32, I32, I32, P, P, P, I64, P, P, I64, P, U32, P, I64, P, P],
         "gdn_verify_replay_layers": [DP, I32, I32, I32, P, P, I32, P, P, P, P, I64, I64, I32, P, P, P, I64, P, P],
         "gdn_selftest_wait_timeout": [P, ctypes.c_uint64, P],
+        "gdn_selftest_prefill_timeout": [DP, I32, I32, P, P, P, P, P, P, P, I64, I32, P, P, P, P, SZ, P,
+                                         ctypes.c_uint64, P],
         "gdn_decode_transaction": [DP, I32, I32, ctypes.POINTER(gdn_req), I32, ctypes.POINTER(gdn_plan_limits),
                                    ctypes.POINTER(gdn_pool), ctypes.POINTER(gdn_plan), ctypes.POINTER(ctypes.c_uint32),
                                    ctypes.POINTER(gdn_decode_io), P, P],
@@ -337,6 +340,15 @@ def gdn_verify_replay_layers(d: gdn_dims, num_layers, B, row_capacity, cu_rows, 
 def gdn_selftest_wait_timeout(dev_status, limit_ns: int, stream=None):
     return _check("gdn_selftest_wait_timeout",
                   lib.gdn_selftest_wait_timeout(_ptr(dev_status), int(limit_ns), _stream(stream)))
+
+
+def gdn_selftest_prefill_timeout(d: gdn_dims, nseq, row_capacity, cu_seqlens, q, k, v, g, beta, pool_layer,
+                                 slot_stride, num_slots, src_slot, dst_slot, o, workspace, workspace_bytes,
+                                 dev_status, limit_ns: int, stream=None):
+    return _check("gdn_selftest_prefill_timeout", lib.gdn_selftest_prefill_timeout(
+        ctypes.byref(d), nseq, row_capacity, _ptr(cu_seqlens), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
+        _ptr(pool_layer), slot_stride, num_slots, _ptr(src_slot), _ptr(dst_slot), _ptr(o), _ptr(workspace),
+        workspace_bytes, _ptr(dev_status), int(limit_ns), _stream(stream)))
 
 
 # ---------------------------------------------------------------------------

@@ -1,26 +1,34 @@
-// Chunked (WY/UT) GatedDeltaNet prefill (sm_103a).
+// Chunked (WY/UT) GatedDeltaNet prefill (sm_103a): one fused kernel.
 //
 // "Run chained MTP drafting in the batch Engine", Correctness fix: the
 // chunked plan runs a whole prompt at once and publishes only its final
-// state (no per-row checkpoints).  Within a chunk of C tokens with start
-// state S0 and G = cumsum(g) (the chunk form of the gated delta rule):
+// state (no per-row checkpoints).  Within a chunk of C = 64 tokens with start
+// state S (d_v x d_k) and G = cumsum(g) (the chunk form of the gated delta
+// rule):
 //   A[t][i] = beta_t e^{G_t-G_i} k_t.k_i  (i < t),   T = (I + A)^{-1}
-//   W  = T diag(beta e^G) K,   Ut = T diag(beta) V,   U = Ut - W S0^T
-//   O  = diag(e^G) Q S0^T + (M o Q K^T) U,   M[t][i] = e^{G_t-G_i} (i <= t)
-//   S' = e^{G_C} S0 + U^T diag(e^{G_C-G}) K
+//   W  = T diag(beta e^G) K,   Ut = T diag(beta) V,   U = Ut - W S^T
+//   O  = diag(e^G) Q S^T + (M o Q K^T) U,   M[t][i] = e^{G_t-G_i} (i <= t)
+//   S' = e^{G_last} S + U^T diag(dec) K,    dec_i = e^{G_last-G_i}
 //
-// Two kernels, both on the 5th-generation tensor cores (tcgen05).
-//  (1) gdn_chunk_wy_kernel -- one CTA per (chunk, v-head), all chunks of all
-//      sequences at once (state-independent): [K;Q] K^T, the unit
-//      lower-triangular inverse T in 16x16 blocks, W and Ut, the masked,
-//      decayed P = M o Q K^T and dec o K; they go to the workspace already in
-//      the scan's operand-tile layout (128.25 KB per chunk and head).
-//  (2) gdn_chunk_scan_kernel -- one CTA per (sequence, v-head): the only
-//      sequential part.  The state stays on chip across the sequence's
-//      chunks; per chunk it forms U, the outputs and the next state.
-// Sequence i's chunks start at cu_seqlens[i]; chunk c of sequence i uses
-// workspace slot (cu_seqlens[i] + 64c)/64 + i, unique and below
-// ceil(row_capacity/64) + nseq.
+// One CTA (16 warps) per (sequence, v-head) walks the sequence's chunks; the
+// state stays on chip from the first chunk to the last, and no intermediate
+// quantity leaves the SM (no workspace round trip through HBM).  All products
+// run on the 5th-generation tensor cores (tcgen05, kind::f16, fp32
+// accumulators in tensor memory).  Iteration c overlaps the state-dependent
+// work of chunk c (the "scan": U, O, S') with the state-independent work of
+// chunk c+1 (the "producer": [K;Q] K^T, A and P, T, W and Ut), in five slots:
+//   1  MMA  phase A(c): U^T += -S W^T, Oi = S Q^T;  MMA1(c+1): [K;Q] K^T
+//   2  SIMT U^T -> bf16 parts of U and of U diag(dec) (tensor memory);
+//           A(c+1) (fp32, shared) and P(c+1) (bf16 parts)
+//      MMA  phase B(c): Oa = U^T P^T, dS = (U^T diag(dec)) K  (A from tensor memory)
+//   3  SIMT T(c+1) = (I + A)^{-1}, then the operands T diag(beta e^G), T diag(beta)
+//      MMA  MMA2(c+1): W^T = K^T (T diag(beta e^G))^T,  Ut^T = V^T (T diag(beta))^T
+//   4  SIMT S <- e^{G_last} S + dS (fp32 in registers, bf16 parts in shared),
+//           o = e^G Oi + Oa;  tensor copy of chunk c+2's K and Q
+//   5  SIMT W^T(c+1) -> bf16 parts;  tensor copy of chunk c+2's V
+// Operands that are not exact bf16 (S, U, W, P, T-derived tiles) are split
+// into two bf16 parts x = x1 + x2 and every product keeps the terms
+// a1 b1 + a1 b2 + a2 b1 (or a1 b + a2 b when b is exact: q, k, v).
 #include <cuda.h>
 
 #include "common.cuh"
@@ -28,55 +36,82 @@
 
 namespace {
 
-constexpr int kC = 64;         // chunk length
-constexpr int kD = 128;        // d_k = d_v supported by this kernel pair
-constexpr int kThreads = 256;       // per-chunk kernel
-constexpr int kScanThreads = 512;   // scan: 4 warps per tensor-memory lane quadrant
+constexpr int kC = 64;              // chunk length
+constexpr int kD = 128;             // d_k = d_v of this kernel
+constexpr int kSimt = 512;          // warps 0..15: 4 per tensor-memory lane quadrant
+constexpr int kThreads = kSimt + 32;  // + warp 16, which issues the copies and the products
+constexpr int kCtl = kSimt / 32;
+constexpr int kAs = 68;             // row stride (floats) of the fp32 matrix A -> T
 
-__device__ __forceinline__ int chunk_slot(int seq_start, int c, int seq) { return (seq_start + kC * c) / kC + seq; }
+// Barrier 1 over the 16 SIMT warps only (barrier 0 is the whole CTA's).
+__device__ __forceinline__ void simt_sync() { asm volatile("bar.sync 1, 512;" ::: "memory"); }
 
 struct PrefArgs {
     const int32_t *cu;
     int32_t nseq, h_qk, h_v, grp, row_capacity, num_slots;
-    const uint16_t *q, *k, *v;
     const float *g, *beta;
     float *pool;
     int64_t slot_stride;
     const int32_t *src_slot, *dst_slot;
     uint16_t *o;
-    float *ws;             // per (chunk slot, v-head) blobs, see namespace blob
-    const int32_t *order;      // sequences by decreasing length (written by gdn_prefill_tables_kernel)
-    const int32_t *chunk_seq;  // per chunk slot: its sequence, or -1 (same kernel)
+    const int32_t *order;  // sequences by decreasing length (gdn_prefill_order_kernel)
     float q_scale;
     uint32_t *status;
+    uint64_t wait_ns;      // bound of every wait on a copy or a product
+    int32_t withhold;      // self-test only: the last chunk's K/Q copy is never issued
     // q, k (rows x h_qk x 128) and v (rows x h_v x 128) as 3-D bf16 tensors
     // for the copy engine: boxes of 64 columns x 1 head x 64 rows, 128-byte
-    // swizzle, zero fill past row_capacity
+    // swizzle (the operand-tile layout), zero fill past row_capacity
     CUtensorMap tm_q, tm_k, tm_v;
 };
 
-// Workspace per (chunk slot, v-head): everything the scan needs for one chunk,
-// written by the per-chunk kernel in the scan's own shared-memory layout so
-// that the scan fetches it with bulk copies and starts its products at once.
-// Operand tiles are 128-byte-swizzled K-major bf16 tiles (tc.cuh); "parts"
-// are the two-term bf16 split x = x1 + x2, x1 = bf16(x), x2 = bf16(x - x1).
-namespace blob {
-// [W1; Q]: W's high part (rows 0..63) stacked on Q (exact bf16, rows 64..127),
-// one 128-row tile (atoms 16 KB apart) so that one N = 128 product gives
-// S W1^T and S Q^T together; W's low part W2 is a 64-row tile.
-constexpr uint32_t kW1Q = 0;                 // 128 rows (t, then t) x 128 (d_k)
-constexpr uint32_t kW2 = 32768;              // 64 rows (t) x 128 (d_k)
-constexpr uint32_t kP1 = 49152, kP2 = 57344; // P = M o Q K^T parts:         64 rows (t) x  64 (i)
-constexpr uint32_t kK1 = 65536, kK2 = 81920; // dec o K parts, MN-major B:  64 rows (i) x 128 (d_k)
-constexpr uint32_t kTiles = 98304;           // bytes of operand tiles (one contiguous block)
-constexpr uint32_t kUt = 98304;              // Ut = T diag(beta) V, fp32 [t][d_v] (pieces permuted, ut_index)
-constexpr uint32_t kEG = 131072;             // e^{G_t}, fp32 x 64
-constexpr uint32_t kBytes = 131328;
-}  // namespace blob
-constexpr size_t kWsFloats = blob::kBytes / 4;
+// Shared-memory map (bytes from a 1024-aligned base).  Operand tiles are
+// 128-byte-swizzled bf16 tiles (tc.cuh); K-major unless marked MN-major.
+namespace smap {
+constexpr uint32_t kS1 = 0, kS2 = 32768;   // S parts: 128 rows (d_v) x 128 (d_k), two 64-column atoms
+// [K;Q] of a chunk, one per chunk parity: atom a (16 KB) holds K rows 0..63
+// then Q rows 0..63 of columns 64a..64a+63.  Read as: the M = 128 A operand
+// [K;Q] and the N = 64 B operand K (MMA1), MN-major K^T (MMA2) and K (phase
+// B), and Q as the N = 64 B operand (phase A).
+constexpr uint32_t kKQ = 65536;
+constexpr uint32_t kV = 131072;            // V: 64 rows x 128, atoms 8 KB apart; MN-major V^T in MMA2
+constexpr uint32_t kP = 147456;            // P parts (P1 then P2, 64 rows t x 64 i), one pair per parity
+constexpr uint32_t kX = 180224;            // 32 KB, shared in turn by:
+constexpr uint32_t kScratch = kX + 64 * kAs * 4;  //   A -> T (fp32 [64][kAs]) and a 4.5 KB scratch,
+constexpr uint32_t kBW1 = kX, kBW2 = kX + 8192;   //   T diag(beta e^G) parts (64 rows t x 64 i),
+constexpr uint32_t kBU1 = kX + 16384, kBU2 = kX + 24576;  // T diag(beta) parts,
+constexpr uint32_t kW1 = kX, kW2 = kX + 16384;    //   W parts, MN-major: 128 rows d x 64 t
+constexpr uint32_t kMisc = 212992;
+// per chunk parity b (64 fp32 each, +256 b): G, e^G, dec, raw g, raw beta
+constexpr uint32_t kG = kMisc, kEG = kMisc + 512, kDec = kMisc + 1024, kGraw = kMisc + 1536,
+                   kBraw = kMisc + 2048;
+constexpr uint32_t kBars = kMisc + 2560;   // mbarriers (16 slots)
+constexpr uint32_t kTbase = kMisc + 2688;
+constexpr uint32_t kFlags = kMisc + 2704;  // four rotating wait-result flags
+constexpr uint32_t kAbort = kMisc + 2720;  // set by any thread whose bounded wait ran out
+constexpr size_t kSmem = size_t(kMisc) + 2752 + 1024;  // + alignment slack
+}  // namespace smap
 
-// G[t] = g[0] + ... + g[t] over the chunk (g = 0 past its n tokens), by warp 0
-// with a shuffle scan.
+// Tensor-memory columns (512): fp32 accumulators, then packed bf16 A operands.
+namespace tcol {
+constexpr uint32_t kU = 0;      // U^T (lanes d_v, columns t): Ut^T from MMA2, then += -S W^T
+constexpr uint32_t kOi = 64;    // S Q^T
+constexpr uint32_t kOa = 128;   // U^T P^T
+constexpr uint32_t kdS = 192;   // (U^T diag(dec)) K, 128 columns
+constexpr uint32_t kD1 = 320;   // [K;Q] K^T (lanes t, then q rows), later W^T (lanes d_k)
+constexpr uint32_t kU1 = 384, kU2 = 416;    // U^T parts, 64 t packed in 32 columns
+constexpr uint32_t kUd1 = 448, kUd2 = 480;  // (U^T diag(dec)) parts
+constexpr uint32_t kCols = 512;
+}  // namespace tcol
+
+// mbarriers: the two [K;Q] copies, the V copy, and the products, each of
+// which commits on its own so that its consumer waits for it alone: phase A's
+// U part (A) and its Oi part (OI), [K;Q] K^T (D1), phase B (B), MMA2's W^T
+// part (M2W) and its Ut^T part (M2).
+enum { BKQ0 = 0, BKQ1 = 1, BV = 2, BA = 3, BD1 = 4, BB = 5, BM2 = 6, BOI = 7, BM2W = 8, kBars = 9 };
+
+// G[t] = g[0] + ... + g[t] over the chunk (g = 0 past its n tokens), by one
+// warp with a shuffle scan; in place allowed.
 __device__ __forceinline__ void chunk_cumsum(const float *g, int n, float *G) {
     const int lane = threadIdx.x & 31;
     const float g0 = 2 * lane < n ? g[2 * lane] : 0.f;
@@ -89,12 +124,9 @@ __device__ __forceinline__ void chunk_cumsum(const float *g, int n, float *G) {
         if (lane >= off) incl += y;
     }
     const float excl = incl - pair;
+    __syncwarp();
     G[2 * lane] = excl + g0;
     G[2 * lane + 1] = excl + pair;
-}
-
-__device__ __forceinline__ unsigned char *ws_blob(const PrefArgs &a, int slot, int h) {
-    return reinterpret_cast<unsigned char *>(a.ws) + (size_t(slot) * a.h_v + h) * blob::kBytes;
 }
 
 // x0 and x1 rounded to nearest-even bf16, packed with x0 in the low half.
@@ -104,455 +136,128 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float x0, float x1) {
     return d;
 }
 
-// e^x for the gates inside a chunk (x <= 0): 2^(x log2 e).
-__device__ __forceinline__ float gate_exp(float x) { return exp2f(x * 1.4426950408889634f); }
+// e^x for the gates inside a chunk (x <= 0): 2^(x log2 e) by the hardware's
+// base-2 exponential (relative error about 2^-22).
+__device__ __forceinline__ float gate_exp(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x * 1.4426950408889634f));
+    return y;
+}
 
-// Two-term bf16 split of 8 consecutive values, packed as two 16-byte chunks.
-__device__ __forceinline__ void split8(const float *x, uint4 &hi, uint4 &lo) {
-    uint32_t h[4], l[4];
+// Two-term bf16 split of 8 consecutive values: hi = bf16(x), lo = bf16(x - hi),
+// each packed as four pairs.
+__device__ __forceinline__ void split8(const float *x, uint32_t (&hi)[4], uint32_t (&lo)[4]) {
 #pragma unroll
     for (int p = 0; p < 4; ++p) {
-        h[p] = pack_bf16x2(x[2 * p], x[2 * p + 1]);
-        l[p] = pack_bf16x2(x[2 * p] - __uint_as_float(h[p] << 16), x[2 * p + 1] - __uint_as_float(h[p] & 0xffff0000u));
+        hi[p] = pack_bf16x2(x[2 * p], x[2 * p + 1]);
+        lo[p] = pack_bf16x2(x[2 * p] - __uint_as_float(hi[p] << 16),
+                            x[2 * p + 1] - __uint_as_float(hi[p] & 0xffff0000u));
     }
-    hi = make_uint4(h[0], h[1], h[2], h[3]);
-    lo = make_uint4(l[0], l[1], l[2], l[3]);
+}
+__device__ __forceinline__ void st16(unsigned char *p, const uint32_t (&w)[4]) {
+    *reinterpret_cast<uint4 *>(p) = make_uint4(w[0], w[1], w[2], w[3]);
 }
 
-// ---------------------------------------------------------------------------
-// (1) per-chunk WY/UT quantities on the tensor cores (tcgen05, kind::f16)
-// ---------------------------------------------------------------------------
-// Shared-memory map (bytes from a 1024-aligned base), bf16 128-byte-swizzled tiles:
-//   A1   [K; Q]   128 rows (tokens, then q rows) x 128 (d_k), K-major   32 KB
-//   VN   V        64 rows (tokens) x 128 (d_v) in two 64-column atoms 16 KB
-//                 apart, right after A1: with the K rows of A1 this is
-//                 [K | V] as an MN-major B operand (N = 256, 64-element
-//                 blocks 16 KB apart), so no transposed copy is needed
-//   AB   [T diag(beta e^G); T diag(beta)], hi and lo parts,
-//                 128 rows (t, twice) x 64 (i), K-major                2 x 16 KB
-//   (the fp32 matrix A -> T, [64][68], lives in the AB area before those
-//    tiles are written)
-//   misc G, beta, e^G, mbarrier, tensor-memory base, flag, dec
-// Outputs: the Q tile (rows 64..127 of both A1 atoms as the copy engine left
-// them) leaves by bulk copies once the first product is done, and the P and
-// dec o K parts go from registers straight to the workspace; the W and Ut
-// parts are staged (the W parts in the K rows of A1 and the V rows of VN,
-// both consumed by the second product, Ut where AB was) and leave by bulk
-// copies at the very end: written from registers, their rows would scatter.
-// Tensor memory (256 columns): first D1 = [K;Q] K^T at columns 0..63 (rows
-// 0..63: K K^T, rows 64..127: Q K^T), then D2 = AB [K | V] at 0..255:
-// rows 0..63 x columns 0..127 hold W, rows 64..127 x columns 128..255 hold Ut
-// (the two cross blocks are not used).
-namespace wy {
-constexpr uint32_t kA1 = 0, kVN = 32768, kT = 65536, kMisc = 98304;
-constexpr uint32_t kAbHi = kT, kAbLo = kT + 16384;
-// Staging (8 KB pieces): the two 64-column atoms of W1 in the K rows of the
-// A1 atoms and those of W2 in the V rows of the VN atoms; Ut in AB.
-__device__ __forceinline__ uint32_t st_w1(int atom) { return kA1 + 16384u * uint32_t(atom); }
-__device__ __forceinline__ uint32_t st_w2(int atom) { return kVN + 16384u * uint32_t(atom); }
-constexpr uint32_t kStUt = kT;  // 32 KB
-constexpr int kAs = 68;         // row stride (floats) of the fp32 matrix A -> T: 16-byte rows, no bank conflicts
-constexpr size_t kSmem = kMisc + 2048 + 1024;  // + alignment slack
-constexpr uint32_t kTmemCols = 256;
-}  // namespace wy
-
-// Ut in the workspace: fp32 rows t of 128 values whose 16-byte pieces are
-// permuted within each 128-byte segment by (piece ^ (t & 7)), so that the
-// per-chunk kernel stages it without bank conflicts while a warp of the scan
-// still reads 32 consecutive values of one row from one segment.
-__host__ __device__ constexpr int ut_index(int t, int j) { return t * kD + ((((j >> 2) ^ (t & 7))) << 2) + (j & 3); }
-
-__global__ void __launch_bounds__(kThreads) gdn_chunk_wy_kernel(const __grid_constant__ PrefArgs a) {
-    // One CTA per chunk slot and v-head; slots that hold no chunk exit.
-    const int seq = a.chunk_seq[blockIdx.x];
-    if (seq < 0) return;
-    const int h = blockIdx.y;
-    const int s0 = a.cu[seq];
-    const int s1 = a.cu[seq + 1];
-    const int len = s1 - s0;
-    if (s0 < 0 || len < 0 || s1 > a.row_capacity) return;  // reported by the scan kernel
-    const int c = int(blockIdx.x) - seq - s0 / kC;         // inverse of chunk_slot
-    if (c < 0 || c * kC >= len) return;
-    const int t0 = s0 + c * kC;
-    const int n = min(kC, len - c * kC);
-    const int hq = h / a.grp;
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    unsigned char *out = ws_blob(a, chunk_slot(s0, c, seq), h);
-
-    extern __shared__ unsigned char smraw[];
-    const uint32_t raw_u = gdn::smem_u32(smraw);
-    unsigned char *sm = smraw + (((raw_u + 1023u) & ~1023u) - raw_u);
-    const uint32_t sb = gdn::smem_u32(sm);
-    float *Af = reinterpret_cast<float *>(sm + wy::kT);
-    float *Gs = reinterpret_cast<float *>(sm + wy::kMisc);
-    float *Bs = Gs + kC;
-    float *eG = Bs + kC;
-    uint64_t *bar = reinterpret_cast<uint64_t *>(sm + wy::kMisc + 768);
-    uint32_t *tbase = reinterpret_cast<uint32_t *>(sm + wy::kMisc + 776);
-    int *flag = reinterpret_cast<int *>(sm + wy::kMisc + 780);
-    float *dec = reinterpret_cast<float *>(sm + wy::kMisc + 1024);
-
-    uint64_t *bar_ld = reinterpret_cast<uint64_t *>(sm + wy::kMisc + 784);
-    int *staged_flag = reinterpret_cast<int *>(sm + wy::kMisc + 792);
-
-    // Stage K, Q (rows of A1) and V (rows of VN) by six tensor copies of
-    // 64 rows x 64 columns each, 128-byte swizzled by the copy engine (the
-    // layout of the operand tiles); the gates by the threads meanwhile.
-    if (tid == 0) {
-        gdn::mbar_init(bar, 1);
-        gdn::mbar_init(bar_ld, 1);
-        gdn::mbar_arrive_expect_tx(bar_ld, 6u * 8192u);
+// T = (I + A)^{-1} in place (64 x 64 fp32, row stride kAs; A strictly lower
+// triangular with zeros on and above the diagonal), by the 512 SIMT threads.
+// The four 16 x 16 diagonal blocks by forward substitution (one thread per
+// column, rows read as float4), then the blocks below them from the block
+// identities of a unit lower-triangular inverse, T_ba = -T_bb A_ba T_aa: for
+// the 16-row pairs (1,0) and (3,2), then for the 32-row halves.  X: 4.5 KB.
+__device__ void solve_unit_lower(float *Af, float *X, int tid) {
+    if (tid < 64) {
+        const int I = tid >> 4, j = tid & 15;
+        const float *Ab = Af + (16 * I) * kAs + 16 * I;
+        float x[16];
 #pragma unroll
-        for (int at = 0; at < 2; ++at) {
-            gdn::tma_load_3d(sm + wy::kA1 + at * 16384, &a.tm_k, 64 * at, hq, t0, bar_ld);
-            gdn::tma_load_3d(sm + wy::kA1 + at * 16384 + 8192, &a.tm_q, 64 * at, hq, t0, bar_ld);
-            gdn::tma_load_3d(sm + wy::kVN + at * 16384, &a.tm_v, 64 * at, h, t0, bar_ld);
-        }
-    }
-    __syncwarp();
-    if (warp == 0) tc::tmem_alloc(tbase, wy::kTmemCols);
-    if (tid < kC) {
-        Bs[tid] = tid < n ? a.beta[size_t(t0 + tid) * a.h_v + h] : 0.f;
-        Gs[tid] = tid < n ? a.g[size_t(t0 + tid) * a.h_v + h] : 0.f;
-    }
-    if (tid == 0) *staged_flag = gdn::mbar_wait_bounded(bar_ld, 0) ? 1 : 0;
-    __syncthreads();
-    const bool staged = *staged_flag != 0;
-    if (staged && n < kC) {
-        // Rows n..63 (the next sequence's rows or padding) become zero: K,
-        // Q and V rows, 128 bytes per row and atom.
-        for (int e = tid; e < (kC - n) * 48; e += kThreads) {
-            const int piece = e & 7, rest = e >> 3;
-            const int which = rest % 6, row = n + rest / 6;
-            const uint32_t off = which < 4 ? wy::kA1 + (which >> 1) * 16384 + (which & 1) * 8192
-                                           : wy::kVN + (which - 4) * 16384;
-            *reinterpret_cast<uint4 *>(sm + off + row * 128 + piece * 16) = make_uint4(0, 0, 0, 0);
-        }
-    }
-    gdn::fence_proxy_async_smem();
-    tc::fence_before();
-    __syncthreads();
-    tc::fence_after();
-    const uint32_t tm = *tbase;
-
-    // D1 = A1 K^T: rows 0..63 are K K^T, rows 64..127 are Q K^T.
-    if (tid == 0 && staged) {
-        constexpr uint32_t idesc = tc::idesc_bf16(128, 64);
+        for (int r = 0; r < 16; ++r) {
+            float acc = r == j ? 1.f : 0.f;
 #pragma unroll
-        for (int at = 0; at < 2; ++at)
-#pragma unroll
-            for (int s = 0; s < 4; ++s) {
-                const uint64_t d = tc::smem_desc(sb + wy::kA1 + at * 16384 + s * 32);
-                tc::mma_bf16(tm, d, d, idesc, (at | s) ? 1u : 0u);
+            for (int q = 0; q < (r + 3) / 4; ++q) {
+                const float4 a4 = *reinterpret_cast<const float4 *>(Ab + r * kAs + 4 * q);
+                if (4 * q + 0 < r) acc = fmaf(-a4.x, x[4 * q + 0], acc);
+                if (4 * q + 1 < r) acc = fmaf(-a4.y, x[4 * q + 1], acc);
+                if (4 * q + 2 < r) acc = fmaf(-a4.z, x[4 * q + 2], acc);
+                if (4 * q + 3 < r) acc = fmaf(-a4.w, x[4 * q + 3], acc);
             }
-        tc::commit(bar);
-    }
-    if (warp == 0) {
-        // While the product runs: G = cumsum(g) (in place: each lane owns two
-        // entries), e^G and dec_i = e^{G_last - G_i} (0 past the n tokens).
-        chunk_cumsum(Gs, n, Gs);
-        __syncwarp();
-        const float gl = Gs[n - 1];
-#pragma unroll
-        for (int e = lane; e < kC; e += 32) {
-            const float ge = Gs[e];
-            const float x = expf(ge);
-            eG[e] = x;
-            dec[e] = e < n ? expf(gl - ge) : 0.f;
-            reinterpret_cast<float *>(out + blob::kEG)[e] = x;
+            x[r] = acc;
         }
-        if (lane == 0) *flag = staged && gdn::mbar_wait_bounded(bar, 0) ? 1 : 0;
+        __syncwarp();  // the block's A entries are read before its T column is written
+#pragma unroll
+        for (int r = 0; r < 16; ++r) Af[(16 * I + r) * kAs + 16 * I + j] = x[r];
     }
-    __syncthreads();
-    bool ok = *flag != 0;
-    if (ok) {
-        (void)gdn::mbar_try_wait(bar, 0);
-        tc::fence_after();
-        if (tid == 0) {
-            // The Q tile as it stands; the copy is done long before the
-            // second product is issued.
-            gdn::bulk_s2g(out + blob::kW1Q + 8192, sm + wy::kA1 + 8192, 8192u);
-            gdn::bulk_s2g(out + blob::kW1Q + 16384 + 8192, sm + wy::kA1 + 16384 + 8192, 8192u);
-            gdn::bulk_commit();
+    simt_sync();
+    {
+        const int p = tid >> 8, r = (tid >> 4) & 15, j = tid & 15;
+        const int R0 = 32 * p + 16, C0 = 32 * p;
+        float acc = 0.f;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const float4 a4 = *reinterpret_cast<const float4 *>(Af + (R0 + r) * kAs + C0 + 4 * q);
+            acc = fmaf(a4.x, Af[(C0 + 4 * q + 0) * kAs + C0 + j], acc);
+            acc = fmaf(a4.y, Af[(C0 + 4 * q + 1) * kAs + C0 + j], acc);
+            acc = fmaf(a4.z, Af[(C0 + 4 * q + 2) * kAs + C0 + j], acc);
+            acc = fmaf(a4.w, Af[(C0 + 4 * q + 3) * kAs + C0 + j], acc);
         }
-        // Rows 0..63: A[t][i] = beta_t e^{G_t-G_i} (k_t.k_i), i < t (0 elsewhere).
-        // Rows 64..127: P[t][i] = e^{G_t-G_i} (q_t.k_i), i <= t, split into its
-        // two parts in the staging area (rows 0..63 of the A1 atoms: the K rows,
-        // consumed by the product above).
-        // Masked entries take e^{-inf} = 0 (K and Q rows past n are zero, so
-        // every product is finite): no divergent branch per element.
-        const int q4 = warp & 3, hc = warp >> 2;
-        const int t = 32 * (q4 & 1) + lane;
-        const float gt = Gs[t], bt = Bs[t];
+        X[p * 256 + r * 16 + j] = acc;
+        simt_sync();
+        float t = 0.f;
 #pragma unroll
-        for (int part = 0; part < 2; ++part) {
-            float v16[16];
-            const int col0 = 32 * hc + 16 * part;
-            tc::ld16(tm + (uint32_t(32 * q4) << 16) + uint32_t(col0), v16);
-            if (q4 < 2) {
+        for (int q = 0; q < 4; ++q) {
+            const float4 b4 = *reinterpret_cast<const float4 *>(Af + (R0 + r) * kAs + R0 + 4 * q);
+            t = fmaf(b4.x, X[p * 256 + (4 * q + 0) * 16 + j], t);
+            t = fmaf(b4.y, X[p * 256 + (4 * q + 1) * 16 + j], t);
+            t = fmaf(b4.z, X[p * 256 + (4 * q + 2) * 16 + j], t);
+            t = fmaf(b4.w, X[p * 256 + (4 * q + 3) * 16 + j], t);
+        }
+        Af[(R0 + r) * kAs + C0 + j] = -t;
+        simt_sync();
+    }
+    if (tid < 256) {
+        // the lower half: row 32 + r (r = lane) by warp cg for columns 4 cg ..
+        // 4 cg + 3, with T's upper zeros skipped in the first product; X rows
+        // padded to 36 floats so that the lanes' float4 rows use all banks
+        const int r = tid & 31, cg = tid >> 5;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int q = cg; q < 8; ++q) {
+            const float4 a4 = *reinterpret_cast<const float4 *>(Af + (32 + r) * kAs + 4 * q);
+            const float av[4] = {a4.x, a4.y, a4.z, a4.w};
 #pragma unroll
-                for (int x = 0; x < 16; x += 4) {
-                    float av[4];
-#pragma unroll
-                    for (int y = 0; y < 4; ++y) {
-                        const int i = col0 + x + y;
-                        av[y] = bt * gate_exp(i < t && t < n ? gt - Gs[i] : -INFINITY) * v16[x + y];
-                    }
-                    *reinterpret_cast<float4 *>(Af + t * wy::kAs + col0 + x) = make_float4(av[0], av[1], av[2], av[3]);
-                }
-            } else {
-                float pe[16];
-#pragma unroll
-                for (int x = 0; x < 16; ++x) {
-                    const int i = col0 + x;
-                    pe[x] = gate_exp(i <= t && t < n ? gt - Gs[i] : -INFINITY) * v16[x];
-                }
-#pragma unroll
-                for (int x = 0; x < 16; x += 8) {
-                    uint4 hi, lo;
-                    split8(pe + x, hi, lo);
-                    const uint32_t off = tc::swz_off(64, t, col0 + x);
-                    *reinterpret_cast<uint4 *>(out + blob::kP1 + off) = hi;
-                    *reinterpret_cast<uint4 *>(out + blob::kP2 + off) = lo;
-                }
+            for (int z = 0; z < 4; ++z) {
+                const float4 tv = *reinterpret_cast<const float4 *>(Af + (4 * q + z) * kAs + 4 * cg);
+                acc.x = fmaf(av[z], tv.x, acc.x);
+                acc.y = fmaf(av[z], tv.y, acc.y);
+                acc.z = fmaf(av[z], tv.z, acc.z);
+                acc.w = fmaf(av[z], tv.w, acc.w);
             }
         }
-        gdn::fence_proxy_async_smem();
+        *reinterpret_cast<float4 *>(X + r * 36 + 4 * cg) = acc;
     }
-    __syncthreads();
-    if (ok) {
-        // T = (I + A)^{-1} by forward substitution, column by column, four
-        // pivot rows at a time: T[t][j] = delta_tj - sum_{i<t} A[t][i] T[i][j].
-        // Four threads own a column j (rows 4m + q, m = 0..15) and keep the
-        // running sums p of their rows.  For pivot rows 4 tau .. 4 tau + 3 the
-        // owners' right-hand sides b = delta - p go to all four threads, which
-        // solve the unit lower-triangular 4 x 4 diagonal block of (I + A) in
-        // closed form (D = its inverse) and add A[r][4 tau .. 4 tau + 3] v to
-        // the sums of their later rows r.  Pivots above a warp's first column
-        // give zeros and are skipped; column blocks are assigned so that the
-        // two warps sharing a scheduler (w, w + 4) have the same number of steps.
-        {
-            const int cb = warp < 4 ? warp : 11 - warp;
-            const int j = 8 * cb + (lane >> 2), q = lane & 3;
-            const int base = lane & ~3;
-            float p[16];
+    simt_sync();
+    if (tid < 256) {
+        const int r = tid & 31, cg = tid >> 5;
+        float4 t = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-            for (int m = 0; m < 16; ++m) p[m] = 0.f;
+        for (int q = 0; q < 8; ++q) {
+            const float4 b4 = *reinterpret_cast<const float4 *>(Af + (32 + r) * kAs + 32 + 4 * q);
+            const float bv[4] = {b4.x, b4.y, b4.z, b4.w};
 #pragma unroll
-            for (int tau = 0; tau < 16; ++tau) {
-                if (tau >= 2 * cb) {
-                    const float4 a1 = *reinterpret_cast<const float4 *>(Af + (4 * tau + 1) * wy::kAs + 4 * tau);
-                    const float4 a2 = *reinterpret_cast<const float4 *>(Af + (4 * tau + 2) * wy::kAs + 4 * tau);
-                    const float4 a3 = *reinterpret_cast<const float4 *>(Af + (4 * tau + 3) * wy::kAs + 4 * tau);
-                    const float d10 = -a1.x, d21 = -a2.y, d32 = -a3.z;
-                    const float d20 = -fmaf(a2.y, d10, a2.x);
-                    const float d31 = -fmaf(a3.z, d21, a3.y);
-                    const float d30 = -fmaf(a3.z, d20, fmaf(a3.y, d10, a3.x));
-                    const float bq = (4 * tau + q == j ? 1.f : 0.f) - p[tau];
-                    const float b0 = __shfl_sync(0xffffffffu, bq, base);
-                    const float b1 = __shfl_sync(0xffffffffu, bq, base | 1);
-                    const float b2 = __shfl_sync(0xffffffffu, bq, base | 2);
-                    const float b3 = __shfl_sync(0xffffffffu, bq, base | 3);
-                    const float v0 = b0;
-                    const float v1 = fmaf(d10, b0, b1);
-                    const float v2 = fmaf(d21, b1, fmaf(d20, b0, b2));
-                    const float v3 = fmaf(d32, b2, fmaf(d31, b1, fmaf(d30, b0, b3)));
-                    p[tau] = q == 0 ? v0 : (q == 1 ? v1 : (q == 2 ? v2 : v3));
-#pragma unroll
-                    for (int m = tau + 1; m < 16; ++m) {
-                        const float4 am = *reinterpret_cast<const float4 *>(Af + (4 * m + q) * wy::kAs + 4 * tau);
-                        p[m] = fmaf(am.w, v3, fmaf(am.z, v2, fmaf(am.y, v1, fmaf(am.x, v0, p[m]))));
-                    }
-                }
+            for (int z = 0; z < 4; ++z) {
+                const float4 xv = *reinterpret_cast<const float4 *>(X + (4 * q + z) * 36 + 4 * cg);
+                t.x = fmaf(bv[z], xv.x, t.x);
+                t.y = fmaf(bv[z], xv.y, t.y);
+                t.z = fmaf(bv[z], xv.z, t.z);
+                t.w = fmaf(bv[z], xv.w, t.w);
             }
-            if (warp >= 4) {
-                // The warps with few pivot steps (column blocks 4..7) then
-                // write the dec o K parts for the scan's state update, an
-                // MN-major operand with the K rows' layout (64-column atoms
-                // 8 KB apart): 16-byte piece e of the output (atom e/512,
-                // token row i) is the same piece of A1's K row i, scaled by dec_i.
-                for (int e = tid - 128; e < kD * kC / 8; e += kThreads - 128) {
-                    const int atom = e >> 9, i = (e >> 3) & (kC - 1);
-                    const uint4 kr = *reinterpret_cast<const uint4 *>(sm + wy::kA1 + atom * 16384 + (e & 511) * 16);
-                    const uint32_t kw[4] = {kr.x, kr.y, kr.z, kr.w};
-                    const float di = dec[i];
-                    float kv[8];
-#pragma unroll
-                    for (int y = 0; y < 8; ++y)
-                        kv[y] = gdn::bf16_to_f32(uint16_t(y & 1 ? kw[y >> 1] >> 16 : kw[y >> 1] & 0xffffu)) * di;
-                    uint4 hi, lo;
-                    split8(kv, hi, lo);
-                    *reinterpret_cast<uint4 *>(out + blob::kK1 + e * 16) = hi;
-                    *reinterpret_cast<uint4 *>(out + blob::kK2 + e * 16) = lo;
-                }
-            }
-            __syncthreads();  // every A entry is read before T overwrites it
-#pragma unroll
-            for (int m = 0; m < 16; ++m) Af[(4 * m + q) * wy::kAs + j] = p[m];
         }
-        __syncthreads();
-        // AB rows t: T diag(beta e^G); rows 64 + t: T diag(beta); hi and lo parts.
-        const int t = tid >> 2, i0 = (tid & 3) * 16;
-        float tv[16];
-#pragma unroll
-        for (int x = 0; x < 16; x += 4) {
-            const float4 tr = *reinterpret_cast<const float4 *>(Af + t * wy::kAs + i0 + x);
-            tv[x] = tr.x;
-            tv[x + 1] = tr.y;
-            tv[x + 2] = tr.z;
-            tv[x + 3] = tr.w;
-        }
-        __syncthreads();  // every T entry is read before the tiles overwrite it
-#pragma unroll
-        for (int half = 0; half < 2; ++half) {
-            float xb[8], xv[8];
-#pragma unroll
-            for (int y = 0; y < 8; ++y) {
-                const int i = i0 + half * 8 + y;
-                xv[y] = tv[half * 8 + y] * Bs[i];
-                xb[y] = xv[y] * eG[i];
-            }
-            uint4 bh, bl, vh, vl;
-            split8(xb, bh, bl);
-            split8(xv, vh, vl);
-            const uint32_t ob = tc::swz_off(128, t, i0 + half * 8), ov = tc::swz_off(128, kC + t, i0 + half * 8);
-            *reinterpret_cast<uint4 *>(sm + wy::kAbHi + ob) = bh;
-            *reinterpret_cast<uint4 *>(sm + wy::kAbLo + ob) = bl;
-            *reinterpret_cast<uint4 *>(sm + wy::kAbHi + ov) = vh;
-            *reinterpret_cast<uint4 *>(sm + wy::kAbLo + ov) = vl;
-        }
-        gdn::fence_proxy_async_smem();
-        tc::fence_before();
+        *reinterpret_cast<float4 *>(Af + (32 + r) * kAs + 4 * cg) = make_float4(-t.x, -t.y, -t.z, -t.w);
     }
-    __syncthreads();
-    if (ok && tid == 0) {
-        tc::fence_after();
-        // D2 = AB [K | V] (M = 128, N = 256, B MN-major: four 64-column
-        // blocks 16 KB apart from A1's K rows to VN); hi and lo parts accumulate.
-        constexpr uint32_t idesc = tc::idesc_bf16(128, 256) | tc::kBMnMajor;
-        const uint64_t bkv = tc::smem_desc_mn(sb + wy::kA1, 16384);
-#pragma unroll
-        for (int s = 0; s < 4; ++s) {
-            const uint64_t b = tc::desc_at(bkv, s * 2048);
-            tc::mma_bf16(tm, tc::smem_desc(sb + wy::kAbHi + s * 32), b, idesc, s ? 1u : 0u);
-            tc::mma_bf16(tm, tc::smem_desc(sb + wy::kAbLo + s * 32), b, idesc, 1u);
-        }
-        tc::commit(bar);
-        *flag = gdn::mbar_wait_bounded(bar, 1) ? 1 : 0;
-    }
-    __syncthreads();
-    ok = ok && *flag != 0;
-    if (ok) {
-        (void)gdn::mbar_try_wait(bar, 1);
-        tc::fence_after();
-        const int q4 = warp & 3, hc = warp >> 2;
-        const int t = 32 * (q4 & 1) + lane;  // token row = accumulator lane (mod 64)
-        const uint32_t lane_base = uint32_t(32 * q4) << 16;
-        if (q4 < 2) {
-            // W row t -> its two bf16 parts (columns 64hc.. in atom hc)
-#pragma unroll
-            for (int part = 0; part < 4; ++part) {
-                const int col = 16 * part;
-                float w16[16];
-                tc::ld16(tm + lane_base + uint32_t(64 * hc + col), w16);
-#pragma unroll
-                for (int x = 0; x < 16; x += 8) {
-                    uint4 hi, lo;
-                    split8(w16 + x, hi, lo);
-                    const uint32_t off = tc::swz_off(64, t, col + x);
-                    *reinterpret_cast<uint4 *>(sm + wy::st_w1(hc) + off) = hi;
-                    *reinterpret_cast<uint4 *>(sm + wy::st_w2(hc) + off) = lo;
-                }
-            }
-        } else {
-            // Ut row t, fp32, staged where AB was
-            float *Ut = reinterpret_cast<float *>(sm + wy::kStUt);
-#pragma unroll
-            for (int part = 0; part < 4; ++part) {
-                const int col = 64 * hc + 16 * part;
-                float u16[16];
-                tc::ld16(tm + lane_base + 128u + uint32_t(col), u16);
-#pragma unroll
-                for (int x = 0; x < 16; x += 4)
-                    *reinterpret_cast<float4 *>(Ut + ut_index(t, col + x)) =
-                        make_float4(u16[x], u16[x + 1], u16[x + 2], u16[x + 3]);
-            }
-        }
-        gdn::fence_proxy_async_smem();
-    } else if (tid == 0) {
-        gdn::set_status(a.status, GDN_DEV_TIMEOUT);
-    }
-    tc::fence_before();
-    __syncthreads();
-    if (tid == 0) {
-        if (ok) {
-            // W and Ut parts.
-            for (int at = 0; at < 2; ++at) {
-                gdn::bulk_s2g(out + blob::kW1Q + at * 16384, sm + wy::st_w1(at), 8192u);
-                gdn::bulk_s2g(out + blob::kW2 + at * 8192, sm + wy::st_w2(at), 8192u);
-            }
-            gdn::bulk_s2g(out + blob::kUt, sm + wy::kStUt, 16384u);
-            gdn::bulk_s2g(out + blob::kUt + 16384, sm + wy::kStUt + 16384, 16384u);
-            gdn::bulk_commit();
-        }
-        // The stores have read their shared-memory sources before it is
-        // released; their writes are complete when the grid is.
-        gdn::bulk_wait_read_all();
-    }
-    if (warp == 0) tc::tmem_dealloc(tm, wy::kTmemCols);
+    simt_sync();
 }
 
-// ---------------------------------------------------------------------------
-// (2) sequential scan over chunks on the tensor cores (tcgen05, kind::f16)
-// ---------------------------------------------------------------------------
-// One CTA per (sequence, v-head); the 128 value rows of S are the M = 128
-// side of every product, so each thread owns one row of S (lane quadrant of
-// its warp) and a quarter of its columns (16 warps).  The FP32 master copy of S stays in
-// registers for the whole sequence.  S and U are split into two bf16 parts
-// here; W, P and dec o K arrive split from the per-chunk kernel; a product
-// keeps the three leading terms a1 b1 + a1 b2 + a2 b1; q and k are exact
-// bf16.  Per chunk:
-//   phase A:  Uacc = S W^T         (M128 N64  K128)  -> U^T = Ut^T - Uacc
-//             Oi   = S Q^T         (M128 N64  K128)
-//   phase B:  Oa   = U^T P^T       (M128 N64  K64)
-//             dS   = U^T (dec o K) (M128 N128 K64),   S <- e^{G_last} S + dS
-//   o_t = q_scale (e^{G_t} Oi[:,t] + Oa[:,t]),  dec_i = e^{G_last - G_i}.
-// Shared-memory map (bytes from a 1024-aligned base), bf16 K-major tiles:
-namespace sc {
-constexpr uint32_t kS1 = 0, kS2 = 32768;  // S parts       128 rows (d_v) x 128 (d_k)
-constexpr uint32_t kTiles = 65536;        // the chunk's W, Q, P and dec o K tiles, in the workspace layout
-constexpr uint32_t kW1Q = kTiles + blob::kW1Q, kW2 = kTiles + blob::kW2;
-constexpr uint32_t kP1 = kTiles + blob::kP1, kP2 = kTiles + blob::kP2;
-constexpr uint32_t kK1 = kTiles + blob::kK1, kK2 = kTiles + blob::kK2;
-constexpr uint32_t kU1 = kTiles + blob::kTiles, kU2 = kU1 + 16384;  // U^T parts 128 rows (d_v) x 64 (i)
-constexpr uint32_t kMisc = kU2 + 16384;   // e^G (two chunks' worth), mbarriers, tensor-memory base, flag
-constexpr size_t kSmem = kMisc + 1024 + 1024;
-constexpr uint32_t kTmemCols = 512;  // Uacc 0..63, dS 256..383, Oi/Oa two buffers
-}  // namespace sc
-
-// Fetches of chunk c's workspace blob, issued by one thread: part A (the W
-// and Q tiles, 48 KB) is needed by the chunk's first products and may land
-// once the previous chunk's first products are done; part B (P and dec o K,
-// 48 KB, and e^G into buffer c % 2) is needed from the second products on.
-__device__ __forceinline__ void scan_fetch_a(const PrefArgs &a, unsigned char *sm, uint64_t *bar, int s0, int seq,
-                                             int h, int c) {
-    const unsigned char *src = ws_blob(a, chunk_slot(s0, c, seq), h);
-    gdn::fence_proxy_async_smem();
-    gdn::mbar_arrive_expect_tx(bar, 3u * 16384u);
-    for (int i = 0; i < 3; ++i) gdn::bulk_g2s(sm + sc::kTiles + i * 16384, src + i * 16384, 16384u, bar);
-}
-__device__ __forceinline__ void scan_fetch_b(const PrefArgs &a, unsigned char *sm, uint64_t *bar, int s0, int seq,
-                                             int h, int c) {
-    const unsigned char *src = ws_blob(a, chunk_slot(s0, c, seq), h);
-    gdn::fence_proxy_async_smem();
-    gdn::mbar_arrive_expect_tx(bar, 3u * 16384u + 256u);
-    for (int i = 3; i < 6; ++i) gdn::bulk_g2s(sm + sc::kTiles + i * 16384, src + i * 16384, 16384u, bar);
-    gdn::bulk_g2s(sm + sc::kMisc + (c & 1) * 256, src + blob::kEG, 256u, bar);
-}
-
-__global__ void __launch_bounds__(kScanThreads, 1) gdn_chunk_scan_kernel(const PrefArgs a) {
+__global__ void __launch_bounds__(kThreads, 1) gdn_prefill_kernel(const __grid_constant__ PrefArgs a) {
     const int h = blockIdx.x % a.h_v;
-    const int seq = a.order[blockIdx.x / a.h_v];  // longest sequences start first
+    const int seq = a.order[blockIdx.x / a.h_v];  // longest sequences first
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int s0 = a.cu[seq];
     const int s1 = a.cu[seq + 1];
@@ -566,277 +271,580 @@ __global__ void __launch_bounds__(kScanThreads, 1) gdn_chunk_scan_kernel(const P
         if (h == 0 && tid == 0) gdn::set_status(a.status, bad);
         return;
     }
+    const int hq = h / a.grp;
+    const int nch = (len + kC - 1) / kC;
+    // Warps 0..15 hold the state and do the element-wise and triangular work
+    // (4 warps per tensor-memory lane quadrant); warp 16 (lane 0) issues the
+    // tensor copies and the tensor-core products, so that a product's issue
+    // (which holds the issuing warp until the product queue has room) never
+    // holds back the element-wise work.
+    const bool ctl = warp == kCtl;
+    const bool issuer = ctl && lane == 0;
+    const int q4 = warp & 3, cq = (warp >> 2) & 3;  // lane quadrant, column quarter
+    const int arow = 32 * q4 + lane;                // tensor-memory lane this thread reads
+    const uint32_t lane_base = uint32_t(32 * q4) << 16;
+    // This thread's share of S: row arow, columns 32cq .. 32cq+31.  Between
+    // chunks S is held only as its two bf16 parts (the MMA operand tiles);
+    // their sum carries about 17 significant bits, and since every chunk
+    // scales the old state by e^{G_last}, the rounding does not accumulate.
+    const size_t row_off = size_t(h) * kD * kD + size_t(arow) * kD + 32 * cq;
+    auto load_s0 = [&](float (&v)[32]) {
+        if (src >= 0) {
+            const float4 *sp = reinterpret_cast<const float4 *>(a.pool + size_t(src) * a.slot_stride + row_off);
+#pragma unroll
+            for (int x = 0; x < 8; ++x) {
+                const float4 w = sp[x];
+                v[4 * x] = w.x;
+                v[4 * x + 1] = w.y;
+                v[4 * x + 2] = w.z;
+                v[4 * x + 3] = w.w;
+            }
+        } else {
+#pragma unroll
+            for (int x = 0; x < 32; ++x) v[x] = 0.f;
+        }
+    };
+    auto store_dst = [&](const float (&v)[32]) {
+        float4 *dp = reinterpret_cast<float4 *>(a.pool + size_t(dst) * a.slot_stride + row_off);
+#pragma unroll
+        for (int x = 0; x < 8; ++x) dp[x] = make_float4(v[4 * x], v[4 * x + 1], v[4 * x + 2], v[4 * x + 3]);
+    };
+    if (nch == 0) {  // an empty sequence publishes its start state
+        if (!ctl) {
+            float v[32];
+            load_s0(v);
+            store_dst(v);
+        }
+        return;
+    }
 
-    extern __shared__ unsigned char smraw[];
+    extern __shared__ __align__(1024) unsigned char smraw[];
     const uint32_t raw_u = gdn::smem_u32(smraw);
     unsigned char *sm = smraw + (((raw_u + 1023u) & ~1023u) - raw_u);
     const uint32_t sb = gdn::smem_u32(sm);
-    uint64_t *bar_u = reinterpret_cast<uint64_t *>(sm + sc::kMisc + 768);   // Uacc done
-    uint64_t *bar_ia = reinterpret_cast<uint64_t *>(sm + sc::kMisc + 784);  // W, Q tiles arrived
-    uint64_t *bar_b = reinterpret_cast<uint64_t *>(sm + sc::kMisc + 792);   // phase B done
-    uint64_t *bar_o = reinterpret_cast<uint64_t *>(sm + sc::kMisc + 800);   // Oi done
-    uint64_t *bar_ib = reinterpret_cast<uint64_t *>(sm + sc::kMisc + 808);  // P, dec o K, e^G arrived
-    uint32_t *tbase = reinterpret_cast<uint32_t *>(sm + sc::kMisc + 776);
-    int *flag = reinterpret_cast<int *>(sm + sc::kMisc + 780);
-    int *oflag = reinterpret_cast<int *>(sm + sc::kMisc + 816);  // the Oi wait of the fetching thread
+    float *Af = reinterpret_cast<float *>(sm + smap::kX);
+    float *Xs = reinterpret_cast<float *>(sm + smap::kScratch);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sm + smap::kBars);
+    uint32_t *tbase = reinterpret_cast<uint32_t *>(sm + smap::kTbase);
+    int *flags = reinterpret_cast<int *>(sm + smap::kFlags);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + smap::kAbort);
+    auto vecp = [&](uint32_t base, int b) { return reinterpret_cast<float *>(sm + base + 256u * uint32_t(b)); };
 
-    if (warp == 0) tc::tmem_alloc(tbase, sc::kTmemCols);
+    if (warp == 0) tc::tmem_alloc(tbase, tcol::kCols);
     if (tid == 0) {
-        gdn::mbar_init(bar_u, 1);
-        gdn::mbar_init(bar_ia, 1);
-        gdn::mbar_init(bar_b, 1);
-        gdn::mbar_init(bar_o, 1);
-        gdn::mbar_init(bar_ib, 1);
+        for (int b = 0; b < kBars; ++b) gdn::mbar_init(&bars[b], 1);
+        *abort_flag = 0;
     }
-
-    const int q4 = warp & 3, cq = warp >> 2;  // lane quadrant, column quarter
-    const int arow = 32 * q4 + lane;          // row of S held by this thread
-    const uint32_t lane_base = uint32_t(32 * q4) << 16;
-    const size_t row_off = size_t(h) * kD * kD + size_t(arow) * kD + 32 * cq;
-    float sv[32];  // S[arow][32cq .. 32cq+31], FP32 master
-    if (src >= 0) {
-        const float4 *sp = reinterpret_cast<const float4 *>(a.pool + size_t(src) * a.slot_stride + row_off);
-#pragma unroll
-        for (int x = 0; x < 8; ++x) {
-            const float4 v = sp[x];
-            sv[4 * x] = v.x;
-            sv[4 * x + 1] = v.y;
-            sv[4 * x + 2] = v.z;
-            sv[4 * x + 3] = v.w;
+    auto chunk_t0 = [&](int c) { return s0 + c * kC; };
+    auto chunk_n = [&](int c) { return min(kC, len - c * kC); };
+    // Raw g and beta of chunk c (0 past its tokens) by threads 64..127.
+    auto load_gb = [&](int c, float &gr, float &br) {
+        const int t = tid - 64;
+        gr = br = 0.f;
+        if (t < chunk_n(c)) {
+            gr = a.g[size_t(chunk_t0(c) + t) * a.h_v + h];
+            br = a.beta[size_t(chunk_t0(c) + t) * a.h_v + h];
         }
-    } else {
-#pragma unroll
-        for (int x = 0; x < 32; ++x) sv[x] = 0.f;
-    }
-    auto write_S = [&]() {
-#pragma unroll
-        for (int x = 0; x < 4; ++x) {
-            uint4 hi, lo;
-            split8(sv + 8 * x, hi, lo);
-            const uint32_t off = tc::swz_off(128, arow, 32 * cq + 8 * x);
-            *reinterpret_cast<uint4 *>(sm + sc::kS1 + off) = hi;
-            *reinterpret_cast<uint4 *>(sm + sc::kS2 + off) = lo;
-        }
-        gdn::fence_proxy_async_smem();
-        tc::fence_before();
     };
-    write_S();
+    const bool gb_thread = tid >= 64 && tid < 128;
+    if (gb_thread) {
+        float gr, br;
+        load_gb(0, gr, br);
+        vecp(smap::kGraw, 0)[tid - 64] = gr;
+        vecp(smap::kBraw, 0)[tid - 64] = br;
+    }
+    gdn::fence_proxy_async_smem();
+    tc::fence_before();
     __syncthreads();
     tc::fence_after();
-    const uint32_t tm = *tbase;
-    constexpr uint32_t id64 = tc::idesc_bf16(128, 64);
-    constexpr uint32_t id128 = tc::idesc_bf16(128, 128);
-    // Tensor-memory columns: dS 256..383, and for chunk c in buffer c % 2
-    // [Uacc | Oi] (128 columns) and Oa (the outputs of chunk c are read while
-    // chunk c + 1's first products run): buffer 0 at 0..127 and 128..191,
-    // buffer 1 at 384..511 and 192..255.
-    const uint64_t dsc = tc::smem_desc(sb);  // descriptors of the fixed tiles: tc::desc_at(dsc, offset)
-    const uint64_t dsc_k = tc::smem_desc_mn(sb + sc::kK1, 8192);  // dec o K parts, MN-major B (K2 at +16 KB)
-    constexpr uint32_t id128k = id128 | tc::kBMnMajor;
-    auto uo_col = [](int b) { return uint32_t(384 * b); };  // Uacc at +0, Oi at +64
-    auto oi_col = [](int b) { return uint32_t(384 * b + 64); };
-    auto oa_col = [](int b) { return uint32_t(128 + 64 * b); };
-    // Phase A of chunk c (thread 0): [Uacc | Oi] = S [W1; Q]^T (N = 128) for
-    // both parts of S, plus S1 W2^T into Uacc (N = 64); committed to bar_u and
-    // bar_o (W and Q are then free for the next chunk's fetch).
-    auto issue_phase_a = [&](int c) {
-        tc::fence_after();
-        const uint32_t d = tm + uo_col(c & 1);
+    const uint32_t tmb = *tbase;
+
+    // Barrier bookkeeping.  `par` (the same in every thread) holds the parity
+    // of each barrier's next phase; it advances at fixed points of the
+    // schedule, after every waiter of that phase.  The issuer also keeps the
+    // phases it started (`armed`, with their parities), which an early exit
+    // still waits for before the shared and tensor memory are released.
+    uint32_t par = 0, armed = 0, arm_par = 0, nwait = 0;
+    // SIMT threads: thread 0 waits (bounded) for the barriers in `mask`, the
+    // others learn the outcome; on success the phases are acquired.
+    auto wait_simt = [&](uint32_t mask) {
+        int *flag = flags + (nwait++ & 3u);
+        if (tid == 0) {
+            bool good = *abort_flag == 0;
+            for (int b = 0; b < kBars; ++b)
+                if (good && ((mask >> b) & 1u)) good = gdn::mbar_wait_bounded(&bars[b], (par >> b) & 1u, a.wait_ns);
+            if (!good) *abort_flag = 1;
+            *flag = good ? 1 : 0;
+        }
+        simt_sync();
+        const bool good = *flag != 0;
+        if (good) {
+            for (int b = 0; b < kBars; ++b)
+                if ((mask >> b) & 1u) (void)gdn::mbar_try_wait(&bars[b], (par >> b) & 1u);
+            tc::fence_after();
+        }
+        return good;
+    };
+    // The issuer waits (bounded) for one barrier before a product or a copy
+    // that depends on it.
+    auto ctl_wait = [&](int b) {
+        if (*abort_flag) return false;
+        if (gdn::mbar_wait_bounded(&bars[b], (par >> b) & 1u, a.wait_ns)) return true;
+        *abort_flag = 1;
+        return false;
+    };
+    auto arm = [&](int b) {
+        armed |= 1u << b;
+        arm_par = (arm_par & ~(1u << b)) | (par & (1u << b));
+    };
+
+    // Tensor copies (issuer).
+    auto issue_kq = [&](int c, int b) {
+        uint64_t *bar = &bars[BKQ0 + b];
+        gdn::mbar_arrive_expect_tx(bar, 32768u);
+        arm(BKQ0 + b);
+        if (a.withhold && c == nch - 1) return;  // self-test: this phase never completes
+        unsigned char *d = sm + smap::kKQ + 32768u * uint32_t(b);
+#pragma unroll
+        for (int at = 0; at < 2; ++at) {
+            gdn::tma_load_3d(d + at * 16384, &a.tm_k, 64 * at, hq, chunk_t0(c), bar);
+            gdn::tma_load_3d(d + at * 16384 + 8192, &a.tm_q, 64 * at, hq, chunk_t0(c), bar);
+        }
+    };
+    auto issue_v = [&](int c) {
+        gdn::mbar_arrive_expect_tx(&bars[BV], 16384u);
+        arm(BV);
+#pragma unroll
+        for (int at = 0; at < 2; ++at) gdn::tma_load_3d(sm + smap::kV + at * 8192, &a.tm_v, 64 * at, h, chunk_t0(c), &bars[BV]);
+    };
+    // Rows n..63 of a partial chunk's tiles hold the next sequence's rows or
+    // padding: zeroed once the copy has landed, before a product reads them.
+    auto zero_kq_rows = [&](int b, int n) {
+        unsigned char *d = sm + smap::kKQ + 32768u * uint32_t(b);
+        for (int e = tid; e < (kC - n) * 32; e += kSimt) {
+            const int row = n + (e >> 5), piece = e & 31, which = piece >> 3;
+            *reinterpret_cast<uint4 *>(d + (which & 1) * 16384 + (which >> 1) * 8192 + row * 128 + (piece & 7) * 16) =
+                make_uint4(0, 0, 0, 0);
+        }
+    };
+    auto zero_v_rows = [&](int n) {
+        for (int e = tid; e < (kC - n) * 16; e += kSimt) {
+            const int row = n + (e >> 4), piece = e & 15;
+            *reinterpret_cast<uint4 *>(sm + smap::kV + (piece >> 3) * 8192 + row * 128 + (piece & 7) * 16) =
+                make_uint4(0, 0, 0, 0);
+        }
+    };
+
+    // Products (issuer).
+    const uint64_t dsc = tc::smem_desc(sb);  // descriptor of any K-major tile: tc::desc_at(dsc, offset)
+    auto kq_off = [](int b) { return smap::kKQ + 32768u * uint32_t(b); };
+    // Phase A of the chunk of parity b, in two commits: U^T += -S W^T (its
+    // consumer, the U split, comes next) and Oi = S Q^T (needed only for the
+    // outputs, at the end of the iteration).
+    auto issue_phase_a_u = [&]() {
+        constexpr uint32_t idU = tc::idesc_bf16(128, 64) | tc::kBMnMajor | tc::kNegA;
+        const uint64_t w1b = tc::smem_desc_mn(sb + smap::kW1, 8192), w2b = tc::smem_desc_mn(sb + smap::kW2, 8192);
 #pragma unroll
         for (int at = 0; at < 2; ++at)
 #pragma unroll
             for (int s = 0; s < 4; ++s) {
                 const uint32_t ka = at * 16384 + s * 32;
-                const uint64_t a1 = tc::desc_at(dsc, sc::kS1 + ka), a2 = tc::desc_at(dsc, sc::kS2 + ka);
-                const uint64_t wq = tc::desc_at(dsc, sc::kW1Q + ka);
-                const uint64_t w2 = tc::desc_at(dsc, sc::kW2 + at * 8192 + s * 32);
-                tc::mma_bf16(d, a1, wq, id128, (at | s) ? 1u : 0u);
-                tc::mma_bf16(d, a1, w2, id64, 1u);
-                tc::mma_bf16(d, a2, wq, id128, 1u);
+                const uint64_t a1 = tc::desc_at(dsc, smap::kS1 + ka), a2 = tc::desc_at(dsc, smap::kS2 + ka);
+                const uint32_t wr = at * 8192 + s * 2048;  // rows d = 64 at + 16 s of the MN-major W tiles
+                const uint64_t w1 = tc::desc_at(w1b, wr), w2 = tc::desc_at(w2b, wr);
+                tc::mma_bf16(tmb + tcol::kU, a1, w1, idU, 1u);
+                tc::mma_bf16(tmb + tcol::kU, a1, w2, idU, 1u);
+                tc::mma_bf16(tmb + tcol::kU, a2, w1, idU, 1u);
             }
-        tc::commit(bar_u);
-        tc::commit(bar_o);
+        tc::commit(&bars[BA]);
+        arm(BA);
     };
-    // Per-thread Ut values of chunk c: Ut[t][arow] for t in [16cq, 16cq+16).
-    float ut[16];
-    auto load_ut = [&](int c) {
-        const float *Ut = reinterpret_cast<const float *>(ws_blob(a, chunk_slot(s0, c, seq), h) + blob::kUt);
+    auto issue_phase_a_o = [&](int b) {
+        constexpr uint32_t idO = tc::idesc_bf16(128, 64);
 #pragma unroll
-        for (int x = 0; x < 16; ++x) ut[x] = Ut[ut_index(16 * cq + x, arow)];
+        for (int at = 0; at < 2; ++at)
+#pragma unroll
+            for (int s = 0; s < 4; ++s) {
+                const uint32_t ka = at * 16384 + s * 32;
+                const uint64_t a1 = tc::desc_at(dsc, smap::kS1 + ka), a2 = tc::desc_at(dsc, smap::kS2 + ka);
+                const uint64_t qd = tc::desc_at(dsc, kq_off(b) + at * 16384 + 8192 + s * 32);
+                tc::mma_bf16(tmb + tcol::kOi, a1, qd, idO, (at | s) ? 1u : 0u);
+                tc::mma_bf16(tmb + tcol::kOi, a2, qd, idO, 1u);
+            }
+        tc::commit(&bars[BOI]);
+        arm(BOI);
+    };
+    auto issue_mma1 = [&](int b) {  // [K;Q] K^T of the chunk in buffer b
+        constexpr uint32_t id1 = tc::idesc_bf16(128, 64);
+#pragma unroll
+        for (int at = 0; at < 2; ++at)
+#pragma unroll
+            for (int s = 0; s < 4; ++s) {
+                const uint64_t d = tc::desc_at(dsc, kq_off(b) + at * 16384 + s * 32);
+                tc::mma_bf16(tmb + tcol::kD1, d, d, id1, (at | s) ? 1u : 0u);
+            }
+        tc::commit(&bars[BD1]);
+        arm(BD1);
+    };
+    auto issue_phase_b = [&](int b) {  // Oa = U^T P^T, dS = (U^T diag(dec)) K, A operands in tensor memory
+        constexpr uint32_t idOa = tc::idesc_bf16(128, 64);
+        constexpr uint32_t idS = tc::idesc_bf16(128, 128) | tc::kBMnMajor;
+        const uint32_t pofs = smap::kP + 16384u * uint32_t(b);
+        const uint64_t kmb = tc::smem_desc_mn(sb + kq_off(b), 16384);
+#pragma unroll
+        for (int s = 0; s < 4; ++s) {
+            const uint64_t p1 = tc::desc_at(dsc, pofs + s * 32), p2 = tc::desc_at(dsc, pofs + 8192 + s * 32);
+            const uint64_t kmn = tc::desc_at(kmb, s * 2048);
+            const uint32_t c8 = 8u * uint32_t(s);
+            tc::mma_bf16_ts(tmb + tcol::kdS, tmb + tcol::kUd1 + c8, kmn, idS, s ? 1u : 0u);
+            tc::mma_bf16_ts(tmb + tcol::kOa, tmb + tcol::kU1 + c8, p1, idOa, s ? 1u : 0u);
+            tc::mma_bf16_ts(tmb + tcol::kdS, tmb + tcol::kUd2 + c8, kmn, idS, 1u);
+            tc::mma_bf16_ts(tmb + tcol::kOa, tmb + tcol::kU1 + c8, p2, idOa, 1u);
+            tc::mma_bf16_ts(tmb + tcol::kOa, tmb + tcol::kU2 + c8, p1, idOa, 1u);
+        }
+        tc::commit(&bars[BB]);
+        arm(BB);
+    };
+    // MMA2 of the chunk in buffer b (A operands MN-major), W^T first (the W
+    // split waits for it alone), then Ut^T into the U accumulator (the next
+    // phase A, issued after it, accumulates onto it).
+    auto issue_mma2 = [&](int b) {
+        constexpr uint32_t id2 = tc::idesc_bf16(128, 64) | tc::kAMnMajor;
+        const uint64_t ktb = tc::smem_desc_mn(sb + kq_off(b), 16384), vtb = tc::smem_desc_mn(sb + smap::kV, 8192);
+#pragma unroll
+        for (int s = 0; s < 4; ++s) {
+            const uint64_t kt = tc::desc_at(ktb, s * 2048);
+            tc::mma_bf16(tmb + tcol::kD1, kt, tc::desc_at(dsc, smap::kBW1 + s * 32), id2, s ? 1u : 0u);
+            tc::mma_bf16(tmb + tcol::kD1, kt, tc::desc_at(dsc, smap::kBW2 + s * 32), id2, 1u);
+        }
+        tc::commit(&bars[BM2W]);
+        arm(BM2W);
+#pragma unroll
+        for (int s = 0; s < 4; ++s) {
+            const uint64_t vt = tc::desc_at(vtb, s * 2048);
+            tc::mma_bf16(tmb + tcol::kU, vt, tc::desc_at(dsc, smap::kBU1 + s * 32), id2, s ? 1u : 0u);
+            tc::mma_bf16(tmb + tcol::kU, vt, tc::desc_at(dsc, smap::kBU2 + s * 32), id2, 1u);
+        }
+        tc::commit(&bars[BM2]);
+        arm(BM2);
     };
 
-    // Outputs of chunk c: o_t = q_scale (e^{G_t} Oi[:,t] + Oa[:,t]) for the
-    // 16 tokens of this thread's column quarter.  They are written one chunk
-    // late, while the next chunk's phase B runs (the other warps wait for it
-    // anyway); thread 0 is then issuing that phase, so the columns of warp 0
-    // (tokens 0..15 of lane quadrant 0) go to warps 4 and 8, eight each.
-    auto outputs_part = [&](int c, int col0, int x0, int x1) {
-        const int t0 = s0 + c * kC;
-        const int n = min(kC, len - c * kC);
-        const float *eG = reinterpret_cast<const float *>(sm + sc::kMisc + (c & 1) * 256);
-        float oi[16], oa[16];
-        tc::ld16(tm + lane_base + oi_col(c & 1) + uint32_t(col0), oi);
-        tc::ld16(tm + lane_base + oa_col(c & 1) + uint32_t(col0), oa);
+    // SIMT steps.
+    auto write_S = [&](const float (&v)[32]) {
+#pragma unroll
+        for (int x = 0; x < 4; ++x) {
+            uint32_t hi[4], lo[4];
+            split8(v + 8 * x, hi, lo);
+            const uint32_t off = tc::swz_off(128, arow, 32 * cq + 8 * x);
+            st16(sm + smap::kS1 + off, hi);
+            st16(sm + smap::kS2 + off, lo);
+        }
+    };
+    // S (this thread's 32 values) = the sum of its two parts.
+    auto read_S = [&](float (&v)[32]) {
+#pragma unroll
+        for (int x = 0; x < 4; ++x) {
+            const uint32_t off = tc::swz_off(128, arow, 32 * cq + 8 * x);
+            const uint4 hi = *reinterpret_cast<const uint4 *>(sm + smap::kS1 + off);
+            const uint4 lo = *reinterpret_cast<const uint4 *>(sm + smap::kS2 + off);
+            const uint32_t hw[4] = {hi.x, hi.y, hi.z, hi.w}, lw[4] = {lo.x, lo.y, lo.z, lo.w};
+#pragma unroll
+            for (int p = 0; p < 4; ++p) {
+                v[8 * x + 2 * p] = __uint_as_float(hw[p] << 16) + __uint_as_float(lw[p] << 16);
+                v[8 * x + 2 * p + 1] = __uint_as_float(hw[p] & 0xffff0000u) + __uint_as_float(lw[p] & 0xffff0000u);
+            }
+        }
+    };
+    // U^T of chunk c -> bf16 parts of U^T and of U^T diag(dec), into tensor memory.
+    auto split_u = [&](int b, const uint32_t (&ur)[16]) {
+        const float *dec = vecp(smap::kDec, b);
+        float u[16];
+#pragma unroll
+        for (int x = 0; x < 16; ++x) u[x] = __uint_as_float(ur[x]);
+        const uint32_t c8 = 8u * uint32_t(cq);
+        uint32_t hh[8], ll[8];
+        split8(u, *reinterpret_cast<uint32_t(*)[4]>(hh), *reinterpret_cast<uint32_t(*)[4]>(ll));
+        split8(u + 8, *reinterpret_cast<uint32_t(*)[4]>(hh + 4), *reinterpret_cast<uint32_t(*)[4]>(ll + 4));
+        tc::st8(tmb + lane_base + tcol::kU1 + c8, hh);
+        tc::st8(tmb + lane_base + tcol::kU2 + c8, ll);
+#pragma unroll
+        for (int x = 0; x < 16; ++x) u[x] *= dec[16 * cq + x];
+        split8(u, *reinterpret_cast<uint32_t(*)[4]>(hh), *reinterpret_cast<uint32_t(*)[4]>(ll));
+        split8(u + 8, *reinterpret_cast<uint32_t(*)[4]>(hh + 4), *reinterpret_cast<uint32_t(*)[4]>(ll + 4));
+        tc::st8(tmb + lane_base + tcol::kUd1 + c8, hh);
+        tc::st8(tmb + lane_base + tcol::kUd2 + c8, ll);
+        tc::st_wait();
+    };
+    // From [K;Q] K^T of chunk c (n tokens, parity b): A (lanes 0..63, fp32 to
+    // shared) and P (lanes 64..127, bf16 parts to the P tiles of parity b).
+    // Masked entries are selected to zero, never multiplied (the products of
+    // rows past n are finite, but not necessarily zero).
+    auto build_a_p = [&](int n, int b, const uint32_t (&vr)[16]) {
+        const float *G = vecp(smap::kG, b);
+        float v16[16];
+#pragma unroll
+        for (int x = 0; x < 16; ++x) v16[x] = __uint_as_float(vr[x]);
+        const int t = arow & 63;
+        const float gt = G[t];
+        if (q4 < 2) {
+            const float bt = vecp(smap::kBraw, b)[t];
+#pragma unroll
+            for (int y = 0; y < 4; ++y) {
+                float av[4];
+#pragma unroll
+                for (int z = 0; z < 4; ++z) {
+                    const int i = 16 * cq + 4 * y + z;
+                    const float e = gate_exp(gt - G[i]);
+                    av[z] = (i < t && t < n) ? bt * e * v16[4 * y + z] : 0.f;
+                }
+                *reinterpret_cast<float4 *>(Af + t * kAs + 16 * cq + 4 * y) = make_float4(av[0], av[1], av[2], av[3]);
+            }
+        } else {
+            float pe[16];
+#pragma unroll
+            for (int x = 0; x < 16; ++x) {
+                const int i = 16 * cq + x;
+                const float e = gate_exp(gt - G[i]);
+                pe[x] = (i <= t && t < n) ? e * v16[x] : 0.f;
+            }
+            const uint32_t pofs = smap::kP + 16384u * uint32_t(b);
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+                uint32_t hi[4], lo[4];
+                split8(pe + 8 * half, hi, lo);
+                const uint32_t off = tc::swz_off(64, t, 16 * cq + 8 * half);
+                st16(sm + pofs + off, hi);
+                st16(sm + pofs + 8192 + off, lo);
+            }
+        }
+    };
+    // T -> T diag(beta e^G) and T diag(beta), bf16 parts (8 entries per thread).
+    auto build_ab = [&](int b) {
+        const int t = tid >> 3, i0 = (tid & 7) * 8;
+        const float4 t0v = *reinterpret_cast<const float4 *>(Af + t * kAs + i0);
+        const float4 t1v = *reinterpret_cast<const float4 *>(Af + t * kAs + i0 + 4);
+        simt_sync();  // every T entry is read before the tiles overwrite it
+        const float tv[8] = {t0v.x, t0v.y, t0v.z, t0v.w, t1v.x, t1v.y, t1v.z, t1v.w};
+        const float *bt = vecp(smap::kBraw, b), *eg = vecp(smap::kEG, b);
+        float xb[8], xv[8];
+#pragma unroll
+        for (int y = 0; y < 8; ++y) {
+            xv[y] = tv[y] * bt[i0 + y];
+            xb[y] = xv[y] * eg[i0 + y];
+        }
+        uint32_t bh[4], bl[4], vh[4], vl[4];
+        split8(xb, bh, bl);
+        split8(xv, vh, vl);
+        const uint32_t off = tc::swz_off(64, t, i0);
+        st16(sm + smap::kBW1 + off, bh);
+        st16(sm + smap::kBW2 + off, bl);
+        st16(sm + smap::kBU1 + off, vh);
+        st16(sm + smap::kBU2 + off, vl);
+    };
+    // W^T (lanes d_k, columns t) -> the MN-major W parts.
+    auto split_w = [&]() {
+        float w[16];
+        tc::ld16(tmb + lane_base + tcol::kD1 + 16 * cq, w);
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+            uint32_t hi[4], lo[4];
+            split8(w + 8 * half, hi, lo);
+            const uint32_t off = tc::swz_off(128, arow, 16 * cq + 8 * half);
+            st16(sm + smap::kW1 + off, hi);
+            st16(sm + smap::kW2 + off, lo);
+        }
+    };
+    // Chunk c (parity b): S <- e^{G_last} S + dS and the chunk's outputs,
+    // staged as bf16 [t][d_v] in the chunk's P tiles (their last reader, phase
+    // B, is done) and written as 16-byte rows.
+    auto update_and_outputs = [&](int c, int b) {
+        const int n = chunk_n(c);
+        const float *eG = vecp(smap::kEG, b);
+        const float egl = eG[n - 1];
+        uint32_t d0[16], d1[16];
+        tc::ld16_async(tmb + lane_base + tcol::kdS + uint32_t(32 * cq), d0);
+        tc::ld16_async(tmb + lane_base + tcol::kdS + uint32_t(32 * cq + 16), d1);
+        float sv[32];
+        read_S(sv);
+        tc::ld_wait();
+        tc::ld_fence_regs(d0);
+        tc::ld_fence_regs(d1);
 #pragma unroll
         for (int x = 0; x < 16; ++x) {
-            const int t = col0 + x;
-            if (x >= x0 && x < x1 && t < n)
-                a.o[(size_t(t0 + t) * a.h_v + h) * kD + arow] =
-                    gdn::f32_to_bf16(a.q_scale * fmaf(eG[t], oi[x], oa[x]));
+            sv[x] = fmaf(egl, sv[x], __uint_as_float(d0[x]));
+            sv[16 + x] = fmaf(egl, sv[16 + x], __uint_as_float(d1[x]));
         }
-    };
-    auto write_outputs = [&](int c) {
-        if (warp != 0) outputs_part(c, 16 * cq, 0, 16);
-        if (warp == 4) outputs_part(c, 0, 0, 8);
-        if (warp == 8) outputs_part(c, 0, 8, 16);
+        uint32_t (&oi)[16] = d0, (&oa)[16] = d1;
+        tc::ld16_async(tmb + lane_base + tcol::kOi + uint32_t(16 * cq), oi);
+        tc::ld16_async(tmb + lane_base + tcol::kOa + uint32_t(16 * cq), oa);
+        write_S(sv);
+        tc::ld_wait();
+        tc::ld_fence_regs(oi);
+        tc::ld_fence_regs(oa);
+        uint16_t *ostage = reinterpret_cast<uint16_t *>(sm + smap::kP + 16384u * uint32_t(b));
+#pragma unroll
+        for (int x = 0; x < 16; ++x) {
+            const int t = 16 * cq + x;
+            ostage[t * kD + arow] =
+                gdn::f32_to_bf16(a.q_scale * fmaf(eG[t], __uint_as_float(oi[x]), __uint_as_float(oa[x])));
+        }
+        simt_sync();
+        const int t0 = chunk_t0(c);
+        for (int e = tid; e < n * 16; e += kSimt) {
+            const int t = e >> 4, ch = e & 15;
+            *reinterpret_cast<uint4 *>(a.o + (size_t(t0 + t) * a.h_v + h) * kD + ch * 8) =
+                *reinterpret_cast<const uint4 *>(ostage + t * kD + ch * 8);
+        }
     };
 
-    uint32_t par_u = 0, par_b = 0, par_o = 0, par_ia = 0, par_ib = 0;
-    bool ok = true;
-    const int nchunks = (len + kC - 1) / kC;
-    if (nchunks > 0) {
-        load_ut(0);
-        if (tid == 0) {
-            scan_fetch_a(a, sm, bar_ia, s0, seq, h, 0);
-            scan_fetch_b(a, sm, bar_ib, s0, seq, h, 0);
-            const bool got = gdn::mbar_wait_bounded(bar_ia, par_ia);
-            *flag = got ? 1 : 0;
-            if (got) issue_phase_a(0);
-        }
-        par_ia ^= 1u;
-        __syncthreads();
-        ok = *flag != 0;
+    if (issuer) {
+        issue_kq(0, 0);
+        issue_v(0);
+        if (nch > 1) issue_kq(1, 1);
     }
-    for (int c = 0; ok && c < nchunks; ++c) {
-        const int t0 = s0 + c * kC;
-        const int n = min(kC, len - c * kC);
-        const bool more = c + 1 < nchunks;
-        const float *eG = reinterpret_cast<const float *>(sm + sc::kMisc + (c & 1) * 256);
-        // Uacc of this chunk.
-        if (tid == 0) *flag = gdn::mbar_wait_bounded(bar_u, par_u) ? 1 : 0;
-        par_u ^= 1u;
-        __syncthreads();
-        if (*flag == 0) {
-            ok = false;
-            break;
-        }
-        tc::fence_after();
-        // The next chunk's W and Q can land as soon as this chunk's Oi product
-        // is done with W and Q: a second thread waits for it and starts the
-        // fetch while the U split and phase B run.
-        if (tid == 32) {
-            const bool got = gdn::mbar_wait_bounded(bar_o, par_o);
-            *oflag = got ? 1 : 0;
-            if (got && more) scan_fetch_a(a, sm, bar_ia, s0, seq, h, c + 1);
-        }
-        par_o ^= 1u;
-        // U^T[arow][t] = Ut[t][arow] - Uacc[arow][t], split into two bf16 parts.
-        {
-            float v16[16];
-            const int col0 = 16 * cq;
-            tc::ld16(tm + lane_base + uo_col(c & 1) + uint32_t(col0), v16);
-#pragma unroll
-            for (int x = 0; x < 16; x += 8) {
-                float u[8];
-#pragma unroll
-                for (int y = 0; y < 8; ++y) u[y] = ut[x + y] - v16[x + y];
-                uint4 hi, lo;
-                split8(u, hi, lo);
-                const uint32_t off = tc::swz_off(128, arow, col0 + x);
-                *reinterpret_cast<uint4 *>(sm + sc::kU1 + off) = hi;
-                *reinterpret_cast<uint4 *>(sm + sc::kU2 + off) = lo;
+    // Iteration c runs the scan of chunk c (c >= 0) beside the producer of
+    // chunk c+1 (c+1 < nch); c = -1 only produces chunk 0 and stages S.
+    bool ok = true;
+    for (int c = -1; c < nch; ++c) {
+        const bool scan = c >= 0, prod = c + 1 < nch, next2 = c + 2 < nch;
+        const int sbuf = c & 1, pbuf = (c + 1) & 1;
+        const int np = prod ? chunk_n(c + 1) : 0;
+        const bool partial = prod && np < kC;
+        // ---- slot 1: phase A(c); MMA1(c+1); G, e^G, dec of chunk c+1; raw g, beta of chunk c+2
+        if (issuer && scan) issue_phase_a_u();
+        if (partial) {
+            // the partial last chunk: its K and Q rows past n become zero first
+            if (!ctl && wait_simt(1u << (BKQ0 + pbuf))) {
+                zero_kq_rows(pbuf, np);
+                gdn::fence_proxy_async_smem();
             }
-        }
-        gdn::fence_proxy_async_smem();
-        tc::fence_before();
-        __syncthreads();
-        // Phase B: Oa = U^T P^T, dS = U^T (dec o K), once this chunk's P and
-        // dec o K have arrived; meanwhile the next chunk's W and Q are fetched
-        // as soon as this chunk's Oi is done with W and Q.
-        bool good_b = true;
-        if (tid == 0) {
-            bool good = gdn::mbar_wait_bounded(bar_ib, par_ib);
-            if (good) {
-                tc::fence_after();
-                const uint32_t oa = tm + oa_col(c & 1);
-#pragma unroll
-                for (int s = 0; s < 4; ++s) {
-                    const uint64_t u1 = tc::desc_at(dsc, sc::kU1 + s * 32), u2 = tc::desc_at(dsc, sc::kU2 + s * 32);
-                    const uint64_t p1 = tc::desc_at(dsc, sc::kP1 + s * 32), p2 = tc::desc_at(dsc, sc::kP2 + s * 32);
-                    const uint64_t k1 = tc::desc_at(dsc_k, s * 2048), k2 = tc::desc_at(dsc_k, (sc::kK2 - sc::kK1) + s * 2048);
-                    tc::mma_bf16(oa, u1, p1, id64, s ? 1u : 0u);
-                    tc::mma_bf16(oa, u1, p2, id64, 1u);
-                    tc::mma_bf16(oa, u2, p1, id64, 1u);
-                    tc::mma_bf16(tm + 256, u1, k1, id128k, s ? 1u : 0u);
-                    tc::mma_bf16(tm + 256, u1, k2, id128k, 1u);
-                    tc::mma_bf16(tm + 256, u2, k1, id128k, 1u);
-                }
-                tc::commit(bar_b);
-            }
-            good_b = good;
-        }
-        if (c > 0) write_outputs(c - 1);  // while phase B runs
-        if (tid == 0) {
-            const bool good = good_b && gdn::mbar_wait_bounded(bar_b, par_b);
-            *flag = (good && *oflag) ? 1 : 0;
-        }
-        par_ib ^= 1u;
-        par_b ^= 1u;
-        __syncthreads();
-        if (*flag == 0) {
-            ok = false;
-            break;
-        }
-        tc::fence_after();
-        // Every product of this chunk is done: P and dec o K are free for the next chunk's.
-        if (more && tid == 0) scan_fetch_b(a, sm, bar_ib, s0, seq, h, c + 1);
-        // S <- e^{G_last} S + dS (FP32 master), then its bf16 parts.
-        const float egl = eG[n - 1];
-#pragma unroll
-        for (int part = 0; part < 2; ++part) {
-            float v16[16];
-            tc::ld16(tm + lane_base + 256u + uint32_t(32 * cq + 16 * part), v16);
-#pragma unroll
-            for (int x = 0; x < 16; ++x) sv[16 * part + x] = fmaf(egl, sv[16 * part + x], v16[x]);
-        }
-        write_S();
-        if (more) {
-            load_ut(c + 1);
-            if (tid == 0) *flag = gdn::mbar_wait_bounded(bar_ia, par_ia) ? 1 : 0;
-            par_ia ^= 1u;
-            __syncthreads();  // the S parts are written and the next chunk's W and Q have arrived
-            if (*flag == 0) {
+            __syncthreads();
+            if (*abort_flag) {
                 ok = false;
                 break;
             }
-            if (tid == 0) issue_phase_a(c + 1);
+            if (issuer) issue_mma1(pbuf);
+        } else if (prod && issuer) {
+            if (ctl_wait(BKQ0 + pbuf)) issue_mma1(pbuf);
         }
-        tc::fence_before();
-    }
-    if (ok && nchunks > 0) {
+        if (issuer && scan) issue_phase_a_o(sbuf);
+        float gr = 0.f, br = 0.f;
+        bool good = true;
+        if (!ctl) {
+            if (prod && warp == 1) {
+                float *G = vecp(smap::kG, pbuf);
+                chunk_cumsum(vecp(smap::kGraw, pbuf), np, G);
+                __syncwarp();
+                const float gl = G[np - 1];
+                for (int e = lane; e < kC; e += 32) {
+                    const float ge = G[e];
+                    vecp(smap::kEG, pbuf)[e] = expf(ge);
+                    vecp(smap::kDec, pbuf)[e] = e < np ? expf(gl - ge) : 0.f;
+                }
+            }
+            if (next2 && gb_thread) load_gb(c + 2, gr, br);
+            good = wait_simt((scan ? 1u << BA : 0u) | (prod ? 1u << BD1 : 0u));
+            // ---- slot 2: U parts of chunk c; A and P of chunk c+1
+            if (good) {
+                if (prod) {
+                    uint32_t vr[16];
+                    tc::ld16_async(tmb + lane_base + tcol::kD1 + 16 * cq, vr);
+                    tc::ld_wait();
+                    tc::ld_fence_regs(vr);
+                    build_a_p(np, pbuf, vr);
+                }
+                if (scan) {
+                    uint32_t ur[16];
+                    tc::ld16_async(tmb + lane_base + tcol::kU + 16 * cq, ur);
+                    tc::ld_wait();
+                    tc::ld_fence_regs(ur);
+                    split_u(sbuf, ur);
+                }
+                gdn::fence_proxy_async_smem();
+                tc::fence_before();
+            }
+        }
+        par ^= (scan ? 1u << BA : 0u) | (prod ? (1u << BD1) | (1u << (BKQ0 + pbuf)) : 0u);
+        __syncthreads();
+        if (*abort_flag) {
+            ok = false;
+            break;
+        }
+        // ---- slot 3: phase B(c) beside T of chunk c+1 and its operands
+        if (issuer && scan) {
+            tc::fence_after();
+            issue_phase_b(sbuf);
+        }
+        if (!ctl && prod) {
+            solve_unit_lower(Af, Xs, tid);
+            build_ab(pbuf);
+            if (partial && wait_simt(1u << BV)) zero_v_rows(np);
+            gdn::fence_proxy_async_smem();
+            tc::fence_before();
+        }
+        __syncthreads();
+        if (*abort_flag) {
+            ok = false;
+            break;
+        }
+        // ---- slot 4: MMA2(c+1); update and outputs of chunk c; W parts of
+        // chunk c+1; chunk c+2's K, Q (once phase B(c) is done) and V (once MMA2 is)
+        if (issuer) {
+            tc::fence_after();
+            if (prod && (partial || ctl_wait(BV))) issue_mma2(pbuf);
+            if (scan && next2 && ctl_wait(BB)) issue_kq(c + 2, sbuf);
+            if (prod && next2 && ctl_wait(BM2)) issue_v(c + 2);
+        }
+        if (!ctl) {
+            good = true;
+            if (scan) {
+                good = wait_simt((1u << BB) | (1u << BOI));
+                if (good) update_and_outputs(c, sbuf);
+            } else {
+                float v[32];
+                load_s0(v);
+                write_S(v);
+            }
+            if (prod && good && wait_simt(1u << BM2W)) split_w();
+            if (next2 && gb_thread) {
+                vecp(smap::kGraw, sbuf)[tid - 64] = gr;
+                vecp(smap::kBraw, sbuf)[tid - 64] = br;
+            }
+            gdn::fence_proxy_async_smem();
+            tc::fence_before();
+        }
+        par ^= (scan ? (1u << BB) | (1u << BOI) : 0u) | (prod ? (1u << BM2) | (1u << BM2W) | (1u << BV) : 0u);
+        __syncthreads();
+        if (*abort_flag) {
+            ok = false;
+            break;
+        }
         tc::fence_after();
-        write_outputs(nchunks - 1);
     }
-    if (ok) {
-        float4 *dp = reinterpret_cast<float4 *>(a.pool + size_t(dst) * a.slot_stride + row_off);
-#pragma unroll
-        for (int x = 0; x < 8; ++x) dp[x] = make_float4(sv[4 * x], sv[4 * x + 1], sv[4 * x + 2], sv[4 * x + 3]);
-    } else if (tid == 0) {
-        gdn::set_status(a.status, GDN_DEV_TIMEOUT);
+    if (!ok) {
+        // A wait ran out: wait (again bounded) for whatever is still in
+        // flight into this CTA's shared or tensor memory, report, and leave
+        // the destination slot untouched.
+        if (issuer) {
+            for (int b = 0; b < kBars; ++b)
+                if ((armed >> b) & 1u) (void)gdn::mbar_wait_bounded(&bars[b], (arm_par >> b) & 1u, a.wait_ns);
+            gdn::set_status(a.status, GDN_DEV_TIMEOUT);
+        }
+    } else if (!ctl && (!a.status || !(*reinterpret_cast<volatile uint32_t *>(a.status) & GDN_DEV_TIMEOUT))) {
+        // Publication: only the final state, and not after any bounded wait
+        // (here or in an earlier launch) has run out.
+        float v[32];
+        read_S(v);
+        store_dst(v);
     }
     tc::fence_before();
     __syncthreads();
-    if (warp == 0) tc::tmem_dealloc(tm, sc::kTmemCols);
+    if (warp == 0) tc::tmem_dealloc(tmb, tcol::kCols);
 }
 
 // order[r] = the sequence with the r-th largest length (ties by index), so
-// that the scan's longest dependency chains are scheduled in its first wave;
-// chunk_seq[x] = the sequence whose chunk sits in workspace slot x (-1 for
-// none), so that the per-chunk kernel's grid covers only the slot range.
-// One block: sequences that fail the scan's row checks get no chunks.
-__global__ void gdn_prefill_tables_kernel(const int32_t *cu, int nseq, int row_capacity, int nslots,
-                                          int32_t *order, int32_t *chunk_seq) {
-    for (int x = threadIdx.x; x < nslots; x += blockDim.x) chunk_seq[x] = -1;
+// that the longest dependency chains start in the first wave.  One block.
+__global__ void gdn_prefill_order_kernel(const int32_t *cu, int nseq, int32_t *order) {
     for (int i = threadIdx.x; i < nseq; i += blockDim.x) {
         const int li = cu[i + 1] - cu[i];
         int r = 0;
@@ -846,30 +854,9 @@ __global__ void gdn_prefill_tables_kernel(const int32_t *cu, int nseq, int row_c
         }
         order[r] = i;
     }
-    __syncthreads();
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
-    for (int i = warp; i < nseq; i += nwarps) {
-        const int s0 = cu[i], s1 = cu[i + 1];
-        if (s0 < 0 || s1 < s0 || s1 > row_capacity) continue;
-        const int nch = (s1 - s0 + kC - 1) / kC;
-        for (int c = lane; c < nch; c += 32) chunk_seq[chunk_slot(s0, c, i)] = i;
-    }
 }
-
-constexpr size_t kWySmem = wy::kSmem;
-constexpr size_t kScanSmem = sc::kSmem;
 
 }  // namespace
-
-// Chunk slots: sequence i's chunk c uses slot chunk_slot(cu[i], c, i), which
-// is below ceil(row_capacity / 64) + nseq for every valid sequence.
-static size_t chunk_slots(int32_t nseq, int32_t row_capacity) {
-    return size_t((int64_t(row_capacity) + kC - 1) / kC) + size_t(nseq);
-}
-
-static size_t blobs_bytes(const gdn_dims *dims, int32_t nseq, int32_t row_capacity) {
-    return chunk_slots(nseq, row_capacity) * size_t(dims->h_v) * kWsFloats * sizeof(float);
-}
 
 static size_t align16(size_t x) { return (x + 15) / 16 * 16; }
 
@@ -905,19 +892,18 @@ static bool encode_rows(CUtensorMap *m, const void *base, int heads, int rows) {
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Workspace: the blobs, then order[nseq], then chunk_seq[slots].
+// Workspace: the length order of the sequences (nseq int32).
 extern "C" size_t gdn_prefill_workspace_bytes(const gdn_dims *dims, int32_t nseq, int32_t row_capacity) {
     if (!dims || nseq < 0 || row_capacity < 0) return 0;
-    return blobs_bytes(dims, nseq, row_capacity) + align16(size_t(nseq) * 4) +
-           align16(chunk_slots(nseq, row_capacity) * 4);
+    return align16(size_t(nseq) * 4);
 }
 
-extern "C" int gdn_chunked_prefill(const gdn_dims *dims, int32_t nseq, int32_t row_capacity,
-                                   const int32_t *cu_seqlens, int32_t max_seqlen, const gdn_bf16 *q,
-                                   const gdn_bf16 *k, const gdn_bf16 *v, const float *g, const float *beta,
-                                   float *pool_layer, int64_t slot_stride, int32_t num_slots,
-                                   const int32_t *src_slot, const int32_t *dst_slot, gdn_bf16 *o, int32_t chunk,
-                                   void *workspace, size_t workspace_bytes, uint32_t *dev_status, void *stream) {
+static int prefill_launch(const gdn_dims *dims, int32_t nseq, int32_t row_capacity, const int32_t *cu_seqlens,
+                          int32_t max_seqlen, const gdn_bf16 *q, const gdn_bf16 *k, const gdn_bf16 *v,
+                          const float *g, const float *beta, float *pool_layer, int64_t slot_stride,
+                          int32_t num_slots, const int32_t *src_slot, const int32_t *dst_slot, gdn_bf16 *o,
+                          int32_t chunk, void *workspace, size_t workspace_bytes, uint32_t *dev_status,
+                          uint64_t wait_ns, int withhold, void *stream) {
     if (!dims) return GDN_ERR_NULL;
     if (!gdn_host::dims_ok(dims)) return GDN_ERR_SHAPE;
     if (dims->d_k != kD) return GDN_ERR_SHAPE;
@@ -929,11 +915,13 @@ extern "C" int gdn_chunked_prefill(const gdn_dims *dims, int32_t nseq, int32_t r
     const int64_t se = int64_t(dims->h_v) * dims->d_v * dims->d_k;
     if (slot_stride < se || (slot_stride % 4) != 0) return GDN_ERR_ARG;
     if (!gdn_host::aligned16(pool_layer) || !gdn_host::aligned16(q) || !gdn_host::aligned16(k) ||
-        !gdn_host::aligned16(v))
+        !gdn_host::aligned16(v) || !gdn_host::aligned16(o))
         return GDN_ERR_ARG;
     const size_t need = gdn_prefill_workspace_bytes(dims, nseq, row_capacity);
     if (!workspace || workspace_bytes < need) return GDN_ERR_WORKSPACE;
     if (!gdn_host::aligned16(workspace)) return GDN_ERR_ARG;
+    const long long grid = (long long)nseq * dims->h_v;
+    if (grid > 0x7fffffffLL) return GDN_ERR_ARG;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     PrefArgs a{};
     a.cu = cu_seqlens;
@@ -943,9 +931,6 @@ extern "C" int gdn_chunked_prefill(const gdn_dims *dims, int32_t nseq, int32_t r
     a.grp = dims->h_v / dims->h_qk;
     a.row_capacity = row_capacity;
     a.num_slots = num_slots;
-    a.q = q;
-    a.k = k;
-    a.v = v;
     a.g = g;
     a.beta = beta;
     a.pool = pool_layer;
@@ -953,29 +938,43 @@ extern "C" int gdn_chunked_prefill(const gdn_dims *dims, int32_t nseq, int32_t r
     a.src_slot = src_slot;
     a.dst_slot = dst_slot;
     a.o = o;
-    a.ws = static_cast<float *>(workspace);
-    unsigned char *tables = static_cast<unsigned char *>(workspace) + blobs_bytes(dims, nseq, row_capacity);
-    int32_t *order = reinterpret_cast<int32_t *>(tables);
-    int32_t *chunk_seq = reinterpret_cast<int32_t *>(tables + align16(size_t(nseq) * 4));
-    a.order = order;
-    a.chunk_seq = chunk_seq;
+    a.order = static_cast<const int32_t *>(workspace);
     a.q_scale = dims->q_scale;
     a.status = dev_status;
+    a.wait_ns = wait_ns;
+    a.withhold = withhold;
     if (!encode_rows(&a.tm_q, q, dims->h_qk, row_capacity) || !encode_rows(&a.tm_k, k, dims->h_qk, row_capacity) ||
         !encode_rows(&a.tm_v, v, dims->h_v, row_capacity))
         return GDN_ERR_CUDA;
-    if (cudaFuncSetAttribute(gdn_chunk_wy_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kWySmem)) !=
-            cudaSuccess ||
-        cudaFuncSetAttribute(gdn_chunk_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kScanSmem)) !=
-            cudaSuccess)
+    if (cudaFuncSetAttribute(gdn_prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smap::kSmem)) !=
+        cudaSuccess)
         return GDN_ERR_CUDA;
-    const size_t slots = chunk_slots(nseq, row_capacity);
-    if (slots > 0x7fffffffULL || dims->h_v > 65535) return GDN_ERR_ARG;
-    gdn_prefill_tables_kernel<<<1, 1024, 0, st>>>(cu_seqlens, nseq, row_capacity, int(slots), order, chunk_seq);
+    gdn_prefill_order_kernel<<<1, 256, 0, st>>>(cu_seqlens, nseq, static_cast<int32_t *>(workspace));
     if (cudaGetLastError() != cudaSuccess) return GDN_ERR_CUDA;
-    gdn_chunk_wy_kernel<<<dim3(unsigned(slots), dims->h_v), kThreads, kWySmem, st>>>(a);
-    if (cudaGetLastError() != cudaSuccess) return GDN_ERR_CUDA;
-    const long long gs = (long long)nseq * dims->h_v;
-    gdn_chunk_scan_kernel<<<unsigned(gs), kScanThreads, kScanSmem, st>>>(a);
+    gdn_prefill_kernel<<<unsigned(grid), kThreads, smap::kSmem, st>>>(a);
     return gdn_host::launch_status(cudaGetLastError());
+}
+
+extern "C" int gdn_chunked_prefill(const gdn_dims *dims, int32_t nseq, int32_t row_capacity,
+                                   const int32_t *cu_seqlens, int32_t max_seqlen, const gdn_bf16 *q,
+                                   const gdn_bf16 *k, const gdn_bf16 *v, const float *g, const float *beta,
+                                   float *pool_layer, int64_t slot_stride, int32_t num_slots,
+                                   const int32_t *src_slot, const int32_t *dst_slot, gdn_bf16 *o, int32_t chunk,
+                                   void *workspace, size_t workspace_bytes, uint32_t *dev_status, void *stream) {
+    return prefill_launch(dims, nseq, row_capacity, cu_seqlens, max_seqlen, q, k, v, g, beta, pool_layer,
+                          slot_stride, num_slots, src_slot, dst_slot, o, chunk, workspace, workspace_bytes,
+                          dev_status, gdn::kWaitLimitNs, 0, stream);
+}
+
+extern "C" int gdn_selftest_prefill_timeout(const gdn_dims *dims, int32_t nseq, int32_t row_capacity,
+                                            const int32_t *cu_seqlens, const gdn_bf16 *q, const gdn_bf16 *k,
+                                            const gdn_bf16 *v, const float *g, const float *beta,
+                                            float *pool_layer, int64_t slot_stride, int32_t num_slots,
+                                            const int32_t *src_slot, const int32_t *dst_slot, gdn_bf16 *o,
+                                            void *workspace, size_t workspace_bytes, uint32_t *dev_status,
+                                            uint64_t limit_ns, void *stream) {
+    if (limit_ns == 0 || limit_ns > gdn::kWaitLimitNs) return GDN_ERR_ARG;
+    return prefill_launch(dims, nseq, row_capacity, cu_seqlens, 0, q, k, v, g, beta, pool_layer, slot_stride,
+                          num_slots, src_slot, dst_slot, o, kC, workspace, workspace_bytes, dev_status, limit_ns, 1,
+                          stream);
 }

@@ -215,11 +215,54 @@ def test_prefill_fail_closed(gs, cuda_dev):
         gs.gdn_chunked_prefill(d, 1, 8, z, 8, pool, pool, pool, pool, pool, pool, pool.stride(0), 4, z, z, pool,
                                32, pool, 1 << 20, z)
     assert e.value.status == gs.GDN_ERR_ARG
-    with pytest.raises(gs.GdnError) as e:          # workspace too small
+    with pytest.raises(gs.GdnError) as e:          # workspace too small (it holds nseq int32)
         gs.gdn_chunked_prefill(d, 1, 8, z, 8, pool, pool, pool, pool, pool, pool, pool.stride(0), 4, z, z, pool,
-                               64, pool, 16, z)
+                               64, pool, 2, z)
     assert e.value.status == gs.GDN_ERR_WORKSPACE
     # a destination slot outside the pool is refused on the device, nothing written
     rows, cu, o, st = run_prefill(gs, cuda_dev, dims, [70], [-1], [9], pool)
     assert st & gs.DEV_SLOT_OOR
     assert torch.count_nonzero(pool) == 0
+
+
+def test_prefill_timed_out_wait_publishes_nothing(gs, cuda_dev):
+    """A bounded wait that runs out makes the prefill refuse to publish
+    ([ENGINE] Correctness fix: never publish a state that was not computed in
+    full).  The self-test entry point withholds the tensor copy of every
+    sequence's last chunk, so the wait for it gives up after 2 ms: the status
+    word carries GDN_DEV_TIMEOUT and every destination slot keeps its bytes.
+    A normal call made afterwards with that bit still set publishes nothing
+    either; once the bit is cleared the same call publishes."""
+    dims = sy.Dims(2, 4, 128, 128)
+    lengths = [40, 130, 64]
+    n = len(lengths)
+    rows, cu, s0 = sy.prefill_inputs(lengths, dims, seed=5)
+    R = int(cu[-1])
+    d = gs.dims(dims.h_qk, dims.h_v, dims.d_k, dims.d_v)
+    pool = sy.state(sy.generator(9), (2 * n, dims.h_v, dims.d_v, dims.d_k)).to(cuda_dev)
+    init = pool.clone()
+    r = rows.to(cuda_dev)
+    ws_bytes = gs.gdn_prefill_workspace_bytes(d, n, R)
+    ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=cuda_dev)
+    o = torch.zeros((R, dims.h_v, dims.d_v), dtype=torch.bfloat16, device=cuda_dev)
+    st = torch.zeros(1, dtype=torch.int32, device=cuda_dev)
+    cu_d = cu.to(cuda_dev)
+    src = torch.tensor([-1, 1, 2], dtype=torch.int32, device=cuda_dev)
+    dst = torch.tensor([3, 4, 5], dtype=torch.int32, device=cuda_dev)
+    gs.gdn_selftest_prefill_timeout(d, n, R, cu_d, r.q, r.k, r.v, r.g, r.beta, pool, pool.stride(0), pool.shape[0],
+                                    src, dst, o, ws, ws_bytes, st, 2_000_000)
+    torch.cuda.synchronize()
+    assert int(st.item()) & gs.DEV_TIMEOUT
+    assert torch.equal(pool, init)
+    gs.gdn_chunked_prefill(d, n, R, cu_d, max(lengths), r.q, r.k, r.v, r.g, r.beta, pool, pool.stride(0),
+                           pool.shape[0], src, dst, o, 64, ws, ws_bytes, st)
+    torch.cuda.synchronize()
+    assert torch.equal(pool, init), "a call made while the timeout bit is set publishes nothing"
+    st.zero_()
+    gs.gdn_chunked_prefill(d, n, R, cu_d, max(lengths), r.q, r.k, r.v, r.g, r.beta, pool, pool.stride(0),
+                           pool.shape[0], src, dst, o, 64, ws, ws_bytes, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    S0s = [np.zeros((dims.h_v, 128, 128)), init[1].cpu().numpy(), init[2].cpu().numpy()]
+    ws_, wo_ = check_sequences(rows, cu, o, S0s, [pool[int(x)].cpu().numpy() for x in dst.tolist()], lengths)
+    assert ws_ <= CHUNK_STATE_RTOL and wo_ <= 1.0, (ws_, wo_)
