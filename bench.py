@@ -619,6 +619,50 @@ def run_zero_copy(spec, dev, args, replay=False, graph=False):
     return res
 
 
+def run_step_graphs(spec, dev, warmup=5, steps=None, arena=False):
+    """The checkpointing transaction of a workload (every layer's verify,
+    the accept and the commit; zero-copy over a state arena with ``arena``)
+    replayed as one CUDA graph per step, with the host planning, uploading
+    and reading back around it."""
+    from speculative_decoding_hybrid_gb300.step import StepGraphs
+    b = Bench(spec, dev, 0, arena=arena, python_driver=True)
+    steps = steps or spec.steps
+    b.precompute_drafts(warmup + 2 * steps)
+    for _ in range(warmup):
+        b.step()
+    torch.cuda.synchronize()
+    graphs = StepGraphs(b.vs, b.loop, b.rows, b.logits, b.tok_d)
+
+    def one():
+        s = b.step_no
+        b.prepare(s)
+        graphs.launch(s)
+        acc, _, _ = b.loop.readback()
+        n = int(acc.sum().item()) + b.loop.B
+        b.loop.finish(acc)
+        b.step_no += 1
+        return n
+    for _ in range(min(steps, 3)):
+        one()
+    torch.cuda.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record()
+    tok = 0
+    for _ in range(steps):
+        tok += one()
+    end.record()
+    torch.cuda.synchronize()
+    ms = start.elapsed_time(end)
+    if int(b.vs.status.item()) != 0:
+        raise RuntimeError("step-graph loop status %d" % int(b.vs.status.item()))
+    res = {"workload": spec.name, "value": tok / (ms * 1e-3), "unit": "verified tokens/s", "steps": steps,
+           "ms_per_step": ms / steps, "launches_per_step": 1, "kernels_per_step": spec.layers + 4,
+           "commit": "zero-copy (state arena)" if arena else "copy"}
+    del graphs, b
+    torch.cuda.empty_cache()
+    return res
+
+
 def run_workload_block(spec, dev, warmup=5, steps=None):
     """Another decode workload timed like the headline line (copy commit through
     gdn_decode_transaction, event-timed verify/commit), for the line's
@@ -930,6 +974,11 @@ def main():
     ap.add_argument("--no-prefill", action="store_true")
     ap.add_argument("--no-cb16", action="store_true",
                     help="skip the continuous-batch (cb16) block that runs after the paged256 line's loop")
+    ap.add_argument("--no-batch1", action="store_true",
+                    help="skip the batch-1 block (host driver and CUDA-graph steps)")
+    ap.add_argument("--step-graph", dest="step_graph", action="store_true", default=True,
+                    help="also time the paged256 checkpointing step as one CUDA graph per step")
+    ap.add_argument("--no-step-graph", dest="step_graph", action="store_false")
     ap.add_argument("--zero-copy", dest="zero_copy", action="store_true", default=True,
                     help="also time the zero-copy commit (state arena) on the same workload")
     ap.add_argument("--no-zero-copy", dest="zero_copy", action="store_false")
@@ -1052,12 +1101,24 @@ def main():
     accept_plain = None
     if world == 1:
         accept_plain = guarded(bench_accept_logits, b)
-    zero_copy = replay = replay_graph = cb16 = None
+    zero_copy = replay = replay_graph = cb16 = batch1 = step_graph = None
     if (args.zero_copy or args.replay) and world == 1:
         del b
         torch.cuda.empty_cache()
         if args.workload == "paged256" and not args.no_cb16:
             cb16 = guarded(run_workload_block, WORKLOADS["cb16"], dev, warmup=args.warmup)
+            torch.cuda.empty_cache()
+        if args.workload == "paged256" and not args.no_batch1:
+            b1 = WORKLOADS["batch1"]
+            batch1 = {"desc": WORKLOAD_TEXT["batch1"] + "; its 16 MB of state and inputs stay in L2 (the case is "
+                              "bound by launches and the host, not HBM)",
+                      "driver": guarded(run_workload_block, b1, dev, warmup=args.warmup, steps=400),
+                      "step_graph_copy": guarded(run_step_graphs, b1, dev, warmup=args.warmup, steps=400),
+                      "step_graph_zero_copy": guarded(run_step_graphs, b1, dev, warmup=args.warmup, steps=400,
+                                                      arena=True)}
+            torch.cuda.empty_cache()
+        if args.workload == "paged256" and args.step_graph:
+            step_graph = guarded(run_step_graphs, spec, dev, warmup=args.warmup, steps=args.steps)
             torch.cuda.empty_cache()
         if args.replay:
             replay = guarded(run_zero_copy, spec, dev, args, replay=True)
@@ -1106,6 +1167,8 @@ def main():
         "acceptance": {"verified_tokens": tok, "requests": spec.batch},
         "accept_stated_logits": accept_plain,
         "cb16": cb16,
+        "batch1": batch1,
+        "step_graph": step_graph,
         "prefill": prefill,
         "mixed_transaction": mixed,
         "zero_copy_commit": zero_copy,

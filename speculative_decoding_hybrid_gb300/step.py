@@ -420,6 +420,70 @@ class ReplayGraphs:
         rs.pending = True
 
 
+class StepGraphs:
+    """CUDA-graph capture of checkpointing transactions: every layer's verify,
+    the greedy accept and the commit, replayed with one launch per step
+    ("Run chained MTP drafting in the batch Engine", H200 RC4 evidence:
+    graph capture of the hybrid fixed-state step).
+
+    A transaction's launches read fixed device buffers (the loop's row and
+    slot tables, the tokens, the checkpoints, tags and locations) plus two
+    arguments passed by value: the input set and the transaction id.  A graph
+    fixes both, so the id cannot advance from one replay to the next; each
+    graph therefore starts by clearing the checkpoint tags, which keeps the
+    commit's guard meaningful (a layer whose verify did not write its tag
+    leaves 0, which no id matches).  The copying commit needs one graph per
+    input set; the zero-copy commit also needs the id's parity (it selects
+    the checkpoint area the locations do not point into), so it takes one
+    graph per residue of lcm(sets, 2) with the id alternating between two
+    values.  The caller plans and uploads the tables and tokens before
+    ``launch`` and reads back after."""
+
+    def __init__(self, vs: VerifyStep, loop: "DecodeLoop", ring_rows: Sequence[Sequence[LayerRows]],
+                 ring_logits: Sequence[torch.Tensor], tokens: torch.Tensor):
+        arena = isinstance(vs, ArenaStep)
+        if isinstance(vs, ReplayStep):
+            raise TypeError("replay transactions are captured by ReplayGraphs")
+        self.vs, self.loop, self.arena = vs, loop, arena
+        self.sets = len(ring_rows)
+        self.n = self.sets if (not arena or self.sets % 2 == 0) else 2 * self.sets
+        self.graphs, self.txns = [], []
+        B = loop.B
+        stream = torch.cuda.Stream()
+        stream.wait_stream(torch.cuda.current_stream())
+        saved = vs.txn
+        try:
+            for i in range(self.n):
+                # the parity an eagerly driven loop would use at step i (ids 1, 2, ...)
+                txn = 2 + ((i + 1) % 2) if arena else 2
+                vs.txn = txn
+                rows, logits = ring_rows[i % self.sets], ring_logits[i % self.sets]
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=stream):
+                    vs._tags.zero_()
+                    if arena:
+                        vs.verify_all_at(B, loop.cu_rows, rows)
+                    else:
+                        vs.verify_all(B, loop.cu_rows, loop.src_slot, rows)
+                    vs.accept(B, loop.cu_rows, logits, tokens)
+                    if arena:
+                        gs.gdn_commit_at(vs.d, B, vs.L, vs.cap, loop.cu_rows, vs.accept_len, vs.area_off[txn & 1],
+                                         vs.ckpt_layer_stride, vs.tags(B), txn, vs.loc, vs.status)
+                    else:
+                        vs.commit(B, loop.cu_rows, loop.dst_slot)
+                self.graphs.append(g)
+                self.txns.append(txn)
+        finally:
+            vs.txn = saved
+        torch.cuda.current_stream().wait_stream(stream)
+
+    def launch(self, step_no: int):
+        """Transaction number ``step_no`` (input set step_no modulo the number of sets)."""
+        i = step_no % self.n
+        self.vs.txn = self.txns[i]
+        self.graphs[i].replay()
+
+
 class MixedTransaction:
     """One planned transaction that holds both prefill sequences and decode
     requests, for every layer.

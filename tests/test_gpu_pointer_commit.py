@@ -31,6 +31,8 @@ def test_arena_loop_matches_copy_loop(gs, cuda_dev):
     ar.pool.copy_(init)
     ar.point_at_slots(slots)
     slot_d = torch.tensor(slots, dtype=torch.int32, device=cuda_dev)
+    from gpu_util import OracleFollow
+    follow = OracleFollow({r: [init[slots[r], l].cpu().numpy() for l in range(L)] for r in (0, 4)})
     kg = sy.generator(2)
     for s in range(steps):
         ks = torch.randint(0, 4, (B,), generator=kg).tolist()
@@ -51,6 +53,13 @@ def test_arena_loop_matches_copy_loop(gs, cuda_dev):
         assert torch.equal(vs.accept_len[:B], ar.accept_len[:B])
         assert torch.equal(vs.out_tokens[:R], ar.out_tokens[:R])
         assert torch.equal(vs.o[:, :R], ar.o[:, :R])
+        # the FP64 oracle, followed for two requests: outputs, accept lengths and
+        # the state each location now points at
+        follow.step(cu, [[t.cpu() for t in (x.q, x.k, x.v, x.g, x.beta)] for x in rows], lg.cpu(), toks.cpu(), vocab,
+                    ar.accept_len[:B].tolist(), ar.o[:, :R])
+        for r in follow.S:
+            follow.check_state(r, [ar.arena[int(ar.loc[l, r]):int(ar.loc[l, r]) + ar.S].view(8, 128, 128).cpu()
+                                   .numpy() for l in range(L)])
         # every location points at the accepted checkpoint of this transaction's area
         area = ar.txn & 1
         acc = ar.accept_len[:B].tolist()
@@ -63,6 +72,9 @@ def test_arena_loop_matches_copy_loop(gs, cuda_dev):
     assert int(ar.status.item()) == 0
     for sl in slots:
         assert torch.equal(ar.pool[sl], vs.pool[sl])
+    print("zero-copy commit vs oracle: worst state %.3f, worst output %.3f of their bounds" %
+          (follow.worst_state, follow.worst_out))
+    assert follow.worst_state <= 1.0 and follow.worst_out <= 1.0
 
 
 def test_commit_at_refuses_stale_tags_and_bad_locations(gs, cuda_dev):

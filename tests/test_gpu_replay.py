@@ -37,6 +37,8 @@ def test_replay_loop_matches_checkpoint_loop(gs, cuda_dev):
     rs = ReplayStep(d, L, num_slots, cap, B, vocab, cuda_dev, pool=init.clone())
     lc = DecodeLoop(vs, slots, _pool(gs, num_slots))
     lr = DecodeLoop(rs, slots, _pool(gs, num_slots))
+    from gpu_util import OracleFollow
+    follow = OracleFollow({r: [init[slots[r], l].cpu().numpy() for l in range(L)] for r in (1, 4)})
     kg = sy.generator(4)
     keep = []
     for s in range(steps):
@@ -61,6 +63,9 @@ def test_replay_loop_matches_checkpoint_loop(gs, cuda_dev):
         assert int(vs.status.item()) == 0 and int(rs.status.item()) == 0
         assert torch.equal(ac, ar) and torch.equal(bc, br) and torch.equal(oc[:R], orr[:R])
         assert torch.equal(vs.o[:, :R], rs.o[:, :R]), "outputs are computed from bit-identical states"
+        # the replay loop's outputs and accept lengths against the FP64 oracle
+        follow.step(cu, [[t.cpu() for t in (x.q, x.k, x.v, x.g, x.beta)] for x in rows], lg.cpu(), toks.cpu(),
+                    vocab, ar.tolist(), rs.o[:, :R])
         lc.finish(ac)
         lr.finish(ar)
     assert lc.slot == lr.slot
@@ -70,6 +75,12 @@ def test_replay_loop_matches_checkpoint_loop(gs, cuda_dev):
     assert int(rs.status.item()) == 0
     for r in range(B):
         assert torch.equal(rs.pool[lr.slot[r]], vs.pool[lc.slot[r]]), r
+    # the replayed (committed) states of the followed requests against the oracle
+    for r in follow.S:
+        follow.check_state(r, [rs.pool[lr.slot[r], l].cpu().numpy() for l in range(L)])
+    print("replay vs oracle: worst state %.3f, worst output %.3f of their bounds" %
+          (follow.worst_state, follow.worst_out))
+    assert follow.worst_state <= 1.0 and follow.worst_out <= 1.0
     # the shared slot was never written by either path
     assert torch.equal(rs.pool[5], init[5]) and torch.equal(vs.pool[5], init[5])
 
@@ -132,6 +143,9 @@ def test_replay_graphs_match_eager_transactions(gs, cuda_dev, ring):
     for _ in range(5):
         lg_.pool.alloc()
     lg_.req_np[:B, 3] = 1
+    from gpu_util import OracleFollow
+    follow = OracleFollow({r: [init[slots[r], l].cpu().numpy() for l in range(L)] for r in (0, 3)})
+    rows_host = [[[t.cpu() for t in (x.q, x.k, x.v, x.g, x.beta)] for x in rr] for rr in rows]
     for s in range(steps):
         i = s % ring
         ks = [3, 2, 3, 1, 3]
@@ -150,6 +164,7 @@ def test_replay_graphs_match_eager_transactions(gs, cuda_dev, ring):
         assert torch.equal(ae, ag), s
         R = pe.dec_cu[-1]
         assert torch.equal(eager.o[:, :R], graph.o[:, :R]), s
+        follow.step(pe.dec_cu, rows_host[i], logits[i][0].cpu(), tk, vocab, ag.tolist(), graph.o[:, :R])
         le.finish(ae)
         lg_.finish(ag)
     cur = torch.tensor(le.slot, dtype=torch.int32, device=cuda_dev)
@@ -158,3 +173,6 @@ def test_replay_graphs_match_eager_transactions(gs, cuda_dev, ring):
     torch.cuda.synchronize()
     assert int(eager.status.item()) == 0 and int(graph.status.item()) == 0
     assert torch.equal(eager.pool, graph.pool)
+    for r in follow.S:
+        follow.check_state(r, [graph.pool[lg_.slot[r], l].cpu().numpy() for l in range(L)])
+    assert follow.worst_state <= 1.0 and follow.worst_out <= 1.0, (follow.worst_state, follow.worst_out)
