@@ -45,6 +45,9 @@ WORKLOADS = {
     "tiny": sy.SPECS["tiny"],
     # a small case for ncu captures: 32 requests, 64 slots, 2 layers (inputs still larger than L2)
     "small": sy.Spec("small", sy.DIMS_FULL, 2, 32, 3, 3, 20, sy.VOCAB_FULL, 2.0, 0.85, 64, 0, 2, 40),
+    # the DRAM-traffic capture case: 128 requests, 256 slots, 2 layers (~3.5 GB on the device; one verify
+    # launch moves 1.35 GB, ten times L2, so lines still dirty in L2 at the end are a small share)
+    "ncu128": sy.Spec("ncu128", sy.DIMS_FULL, 2, 128, 3, 3, 20, sy.VOCAB_FULL, 2.0, 0.85, 256, 0, 2, 41),
 }
 
 WORKLOAD_TEXT = {
@@ -55,6 +58,7 @@ WORKLOAD_TEXT = {
     "batch1": "batch-1 verify: 1 request, 1 GDN layer, K=3, vocab 151936",
     "tiny": "tiny: 1 request, 1 layer, 2 heads, d=16, K=3, vocab 64",
     "small": "ncu case: 32 requests, 64 slots, 2 layers, K=3",
+    "ncu128": "DRAM-traffic case: 128 requests, 256 slots, 2 layers, K=3",
 }
 
 METRIC = "verified tokens/s and GDN verify+commit HBM GB/s (% of GB300 peak)"

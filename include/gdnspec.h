@@ -358,7 +358,8 @@ int gdn_verify_replay_layers(const gdn_dims *dims, int32_t num_layers, int32_t B
  * max_seqlen (host, >= 0) is accepted for callers that track it; every
  * length is read from cu_seqlens on the device.  d_k = d_v = 128 runs on the
  * tensor cores (one CTA per sequence and v-head keeps the state on chip for
- * the whole sequence; nothing but the final state and o is written).
+ * the whole sequence; nothing but the final state and o is written); 16, 32
+ * and 64 run the same chunk form in fp32 on the CUDA cores.
  * Workspace (gdn_prefill_workspace_bytes): the sequences' length order,
  * nseq int32 (16-byte aligned).
  * A sequence whose bounded wait ran out (GDN_DEV_TIMEOUT), and every sequence
@@ -546,8 +547,9 @@ const char *gdn_status_string(int status);
  * (chunk 64) with every wait bounded by limit_ns (1 .. 1e9) of device time,
  * and with the tensor copy of each sequence's last chunk of K and Q
  * withheld, so that the wait for it runs out: every sequence sets
- * GDN_DEV_TIMEOUT and publishes nothing.  (Test-only; it computes nothing
- * a caller would use.) */
+ * GDN_DEV_TIMEOUT and publishes nothing.  d_k = d_v = 128 only (the smaller
+ * sizes run no copy-engine wait).  (Test-only; it computes nothing a caller
+ * would use.) */
 int gdn_selftest_prefill_timeout(const gdn_dims *dims, int32_t nseq, int32_t row_capacity,
                                  const int32_t *cu_seqlens,
                                  const gdn_bf16 *q, const gdn_bf16 *k, const gdn_bf16 *v,

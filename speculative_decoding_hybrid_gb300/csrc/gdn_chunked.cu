@@ -32,6 +32,7 @@
 #include <cuda.h>
 
 #include "common.cuh"
+#include "chunk_math.cuh"
 #include "tc.cuh"
 
 namespace {
@@ -110,38 +111,11 @@ constexpr uint32_t kCols = 512;
 // part (M2W) and its Ut^T part (M2).
 enum { BKQ0 = 0, BKQ1 = 1, BV = 2, BA = 3, BD1 = 4, BB = 5, BM2 = 6, BOI = 7, BM2W = 8, kBars = 9 };
 
-// G[t] = g[0] + ... + g[t] over the chunk (g = 0 past its n tokens), by one
-// warp with a shuffle scan; in place allowed.
-__device__ __forceinline__ void chunk_cumsum(const float *g, int n, float *G) {
-    const int lane = threadIdx.x & 31;
-    const float g0 = 2 * lane < n ? g[2 * lane] : 0.f;
-    const float g1 = 2 * lane + 1 < n ? g[2 * lane + 1] : 0.f;
-    const float pair = g0 + g1;
-    float incl = pair;
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-        const float y = __shfl_up_sync(0xffffffffu, incl, off);
-        if (lane >= off) incl += y;
-    }
-    const float excl = incl - pair;
-    __syncwarp();
-    G[2 * lane] = excl + g0;
-    G[2 * lane + 1] = excl + pair;
-}
-
 // x0 and x1 rounded to nearest-even bf16, packed with x0 in the low half.
 __device__ __forceinline__ uint32_t pack_bf16x2(float x0, float x1) {
     uint32_t d;
     asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(x1), "f"(x0));
     return d;
-}
-
-// e^x for the gates inside a chunk (x <= 0): 2^(x log2 e) by the hardware's
-// base-2 exponential (relative error about 2^-22).
-__device__ __forceinline__ float gate_exp(float x) {
-    float y;
-    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x * 1.4426950408889634f));
-    return y;
 }
 
 // Two-term bf16 split of 8 consecutive values: hi = bf16(x), lo = bf16(x - hi),
@@ -156,103 +130,6 @@ __device__ __forceinline__ void split8(const float *x, uint32_t (&hi)[4], uint32
 }
 __device__ __forceinline__ void st16(unsigned char *p, const uint32_t (&w)[4]) {
     *reinterpret_cast<uint4 *>(p) = make_uint4(w[0], w[1], w[2], w[3]);
-}
-
-// T = (I + A)^{-1} in place (64 x 64 fp32, row stride kAs; A strictly lower
-// triangular with zeros on and above the diagonal), by the 512 SIMT threads.
-// The four 16 x 16 diagonal blocks by forward substitution (one thread per
-// column, rows read as float4), then the blocks below them from the block
-// identities of a unit lower-triangular inverse, T_ba = -T_bb A_ba T_aa: for
-// the 16-row pairs (1,0) and (3,2), then for the 32-row halves.  X: 4.5 KB.
-__device__ void solve_unit_lower(float *Af, float *X, int tid) {
-    if (tid < 64) {
-        const int I = tid >> 4, j = tid & 15;
-        const float *Ab = Af + (16 * I) * kAs + 16 * I;
-        float x[16];
-#pragma unroll
-        for (int r = 0; r < 16; ++r) {
-            float acc = r == j ? 1.f : 0.f;
-#pragma unroll
-            for (int q = 0; q < (r + 3) / 4; ++q) {
-                const float4 a4 = *reinterpret_cast<const float4 *>(Ab + r * kAs + 4 * q);
-                if (4 * q + 0 < r) acc = fmaf(-a4.x, x[4 * q + 0], acc);
-                if (4 * q + 1 < r) acc = fmaf(-a4.y, x[4 * q + 1], acc);
-                if (4 * q + 2 < r) acc = fmaf(-a4.z, x[4 * q + 2], acc);
-                if (4 * q + 3 < r) acc = fmaf(-a4.w, x[4 * q + 3], acc);
-            }
-            x[r] = acc;
-        }
-        __syncwarp();  // the block's A entries are read before its T column is written
-#pragma unroll
-        for (int r = 0; r < 16; ++r) Af[(16 * I + r) * kAs + 16 * I + j] = x[r];
-    }
-    simt_sync();
-    {
-        const int p = tid >> 8, r = (tid >> 4) & 15, j = tid & 15;
-        const int R0 = 32 * p + 16, C0 = 32 * p;
-        float acc = 0.f;
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const float4 a4 = *reinterpret_cast<const float4 *>(Af + (R0 + r) * kAs + C0 + 4 * q);
-            acc = fmaf(a4.x, Af[(C0 + 4 * q + 0) * kAs + C0 + j], acc);
-            acc = fmaf(a4.y, Af[(C0 + 4 * q + 1) * kAs + C0 + j], acc);
-            acc = fmaf(a4.z, Af[(C0 + 4 * q + 2) * kAs + C0 + j], acc);
-            acc = fmaf(a4.w, Af[(C0 + 4 * q + 3) * kAs + C0 + j], acc);
-        }
-        X[p * 256 + r * 16 + j] = acc;
-        simt_sync();
-        float t = 0.f;
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const float4 b4 = *reinterpret_cast<const float4 *>(Af + (R0 + r) * kAs + R0 + 4 * q);
-            t = fmaf(b4.x, X[p * 256 + (4 * q + 0) * 16 + j], t);
-            t = fmaf(b4.y, X[p * 256 + (4 * q + 1) * 16 + j], t);
-            t = fmaf(b4.z, X[p * 256 + (4 * q + 2) * 16 + j], t);
-            t = fmaf(b4.w, X[p * 256 + (4 * q + 3) * 16 + j], t);
-        }
-        Af[(R0 + r) * kAs + C0 + j] = -t;
-        simt_sync();
-    }
-    if (tid < 256) {
-        // the lower half: row 32 + r (r = lane) by warp cg for columns 4 cg ..
-        // 4 cg + 3, with T's upper zeros skipped in the first product; X rows
-        // padded to 36 floats so that the lanes' float4 rows use all banks
-        const int r = tid & 31, cg = tid >> 5;
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int q = cg; q < 8; ++q) {
-            const float4 a4 = *reinterpret_cast<const float4 *>(Af + (32 + r) * kAs + 4 * q);
-            const float av[4] = {a4.x, a4.y, a4.z, a4.w};
-#pragma unroll
-            for (int z = 0; z < 4; ++z) {
-                const float4 tv = *reinterpret_cast<const float4 *>(Af + (4 * q + z) * kAs + 4 * cg);
-                acc.x = fmaf(av[z], tv.x, acc.x);
-                acc.y = fmaf(av[z], tv.y, acc.y);
-                acc.z = fmaf(av[z], tv.z, acc.z);
-                acc.w = fmaf(av[z], tv.w, acc.w);
-            }
-        }
-        *reinterpret_cast<float4 *>(X + r * 36 + 4 * cg) = acc;
-    }
-    simt_sync();
-    if (tid < 256) {
-        const int r = tid & 31, cg = tid >> 5;
-        float4 t = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-            const float4 b4 = *reinterpret_cast<const float4 *>(Af + (32 + r) * kAs + 32 + 4 * q);
-            const float bv[4] = {b4.x, b4.y, b4.z, b4.w};
-#pragma unroll
-            for (int z = 0; z < 4; ++z) {
-                const float4 xv = *reinterpret_cast<const float4 *>(X + (4 * q + z) * 36 + 4 * cg);
-                t.x = fmaf(bv[z], xv.x, t.x);
-                t.y = fmaf(bv[z], xv.y, t.y);
-                t.z = fmaf(bv[z], xv.z, t.z);
-                t.w = fmaf(bv[z], xv.w, t.w);
-            }
-        }
-        *reinterpret_cast<float4 *>(Af + (32 + r) * kAs + 4 * cg) = make_float4(-t.x, -t.y, -t.z, -t.w);
-    }
-    simt_sync();
 }
 
 __global__ void __launch_bounds__(kThreads, 1) gdn_prefill_kernel(const __grid_constant__ PrefArgs a) {
@@ -594,7 +471,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_prefill_kernel(const __grid_c
 #pragma unroll
                 for (int z = 0; z < 4; ++z) {
                     const int i = 16 * cq + 4 * y + z;
-                    const float e = gate_exp(gt - G[i]);
+                    const float e = chunkmath::gate_exp(gt - G[i]);
                     av[z] = (i < t && t < n) ? bt * e * v16[4 * y + z] : 0.f;
                 }
                 *reinterpret_cast<float4 *>(Af + t * kAs + 16 * cq + 4 * y) = make_float4(av[0], av[1], av[2], av[3]);
@@ -604,7 +481,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_prefill_kernel(const __grid_c
 #pragma unroll
             for (int x = 0; x < 16; ++x) {
                 const int i = 16 * cq + x;
-                const float e = gate_exp(gt - G[i]);
+                const float e = chunkmath::gate_exp(gt - G[i]);
                 pe[x] = (i <= t && t < n) ? e * v16[x] : 0.f;
             }
             const uint32_t pofs = smap::kP + 16384u * uint32_t(b);
@@ -733,7 +610,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_prefill_kernel(const __grid_c
         if (!ctl) {
             if (prod && warp == 1) {
                 float *G = vecp(smap::kG, pbuf);
-                chunk_cumsum(vecp(smap::kGraw, pbuf), np, G);
+                chunkmath::chunk_cumsum(vecp(smap::kGraw, pbuf), np, G);
                 __syncwarp();
                 const float gl = G[np - 1];
                 for (int e = lane; e < kC; e += 32) {
@@ -776,7 +653,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_prefill_kernel(const __grid_c
             issue_phase_b(sbuf);
         }
         if (!ctl && prod) {
-            solve_unit_lower(Af, Xs, tid);
+            chunkmath::solve_unit_lower<kSimt, kAs>(Af, Xs, tid, [] { simt_sync(); });
             build_ab(pbuf);
             if (partial && wait_simt(1u << BV)) zero_v_rows(np);
             gdn::fence_proxy_async_smem();
@@ -898,6 +775,13 @@ extern "C" size_t gdn_prefill_workspace_bytes(const gdn_dims *dims, int32_t nseq
     return align16(size_t(nseq) * 4);
 }
 
+// d in {16, 32, 64}: the fp32 chunk-form kernel (gdn_prefill_small.cu).
+int gdn_prefill_small_launch(const gdn_dims *dims, int32_t nseq, int32_t row_capacity, const int32_t *cu_seqlens,
+                             const gdn_bf16 *q, const gdn_bf16 *k, const gdn_bf16 *v, const float *g,
+                             const float *beta, float *pool_layer, int64_t slot_stride, int32_t num_slots,
+                             const int32_t *src_slot, const int32_t *dst_slot, gdn_bf16 *o, const int32_t *order,
+                             uint32_t *dev_status, cudaStream_t st);
+
 static int prefill_launch(const gdn_dims *dims, int32_t nseq, int32_t row_capacity, const int32_t *cu_seqlens,
                           int32_t max_seqlen, const gdn_bf16 *q, const gdn_bf16 *k, const gdn_bf16 *v,
                           const float *g, const float *beta, float *pool_layer, int64_t slot_stride,
@@ -906,7 +790,7 @@ static int prefill_launch(const gdn_dims *dims, int32_t nseq, int32_t row_capaci
                           uint64_t wait_ns, int withhold, void *stream) {
     if (!dims) return GDN_ERR_NULL;
     if (!gdn_host::dims_ok(dims)) return GDN_ERR_SHAPE;
-    if (dims->d_k != kD) return GDN_ERR_SHAPE;
+    if (withhold && dims->d_k != kD) return GDN_ERR_SHAPE;  // the self-test needs the copy engine's path
     if (chunk != kC) return GDN_ERR_ARG;
     if (nseq < 0 || row_capacity < 0 || max_seqlen < 0 || num_slots <= 0) return GDN_ERR_ARG;
     if (nseq == 0) return GDN_OK;
@@ -923,6 +807,13 @@ static int prefill_launch(const gdn_dims *dims, int32_t nseq, int32_t row_capaci
     const long long grid = (long long)nseq * dims->h_v;
     if (grid > 0x7fffffffLL) return GDN_ERR_ARG;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (dims->d_k != kD) {
+        gdn_prefill_order_kernel<<<1, 256, 0, st>>>(cu_seqlens, nseq, static_cast<int32_t *>(workspace));
+        if (cudaGetLastError() != cudaSuccess) return GDN_ERR_CUDA;
+        return gdn_prefill_small_launch(dims, nseq, row_capacity, cu_seqlens, q, k, v, g, beta, pool_layer,
+                                        slot_stride, num_slots, src_slot, dst_slot, o,
+                                        static_cast<const int32_t *>(workspace), dev_status, st);
+    }
     PrefArgs a{};
     a.cu = cu_seqlens;
     a.nseq = nseq;

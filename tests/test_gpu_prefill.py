@@ -266,3 +266,32 @@ def test_prefill_timed_out_wait_publishes_nothing(gs, cuda_dev):
     S0s = [np.zeros((dims.h_v, 128, 128)), init[1].cpu().numpy(), init[2].cpu().numpy()]
     ws_, wo_ = check_sequences(rows, cu, o, S0s, [pool[int(x)].cpu().numpy() for x in dst.tolist()], lengths)
     assert ws_ <= CHUNK_STATE_RTOL and wo_ <= 1.0, (ws_, wo_)
+
+
+@pytest.mark.parametrize("d,heads,lengths", [
+    (16, (2, 2), [1, 40, 64, 130]),        # the tiny workload's head shape, ragged lengths, partial chunks
+    (32, (2, 4), [0, 63, 65, 200]),
+    (64, (4, 8), [7, 128, 300]),
+])
+def test_prefill_small_head_sizes(gs, cuda_dev, d, heads, lengths):
+    """d_k = d_v in {16, 32, 64} (the fp32 chunk-form kernel): final states
+    within 5e-3 (Frobenius, per sequence and head) of the FP64 recurrence and
+    outputs within the bf16 bound, from zero and from a given state; slots
+    that are not destinations keep their bytes."""
+    dims = sy.Dims(heads[0], heads[1], d, d)
+    n = len(lengths)
+    pool = sy.state(sy.generator(31 + d), (2 * n + 1, dims.h_v, d, d)).to(cuda_dev)
+    init = pool.clone()
+    src = [(-1 if i % 2 == 0 else i) for i in range(n)]
+    dst = [n + i for i in range(n)]
+    rows, cu, o, st = run_prefill(gs, cuda_dev, dims, lengths, src, dst, pool, seed=40 + d, cap=sum(lengths) + 70)
+    assert st == 0
+    S0s = [np.zeros((dims.h_v, d, d)) if s < 0 else init[s].cpu().numpy() for s in src]
+    finals = [pool[x].cpu().numpy() for x in dst]
+    ws, wo = check_sequences(rows, cu, o, S0s, finals, lengths)
+    print("prefill d=%d: worst state rel %.3e, worst output ratio %.3f" % (d, ws, wo))
+    assert ws <= CHUNK_STATE_RTOL, ws
+    assert wo <= 1.0, wo
+    for s_ in range(2 * n + 1):
+        if s_ not in dst:
+            assert torch.equal(pool[s_], init[s_])
