@@ -14,6 +14,7 @@ caller's device tensors.  All arithmetic happens in the library's kernels.
 from __future__ import annotations
 
 import ctypes
+import os
 from dataclasses import dataclass
 from typing import List, Optional, Sequence
 
@@ -118,6 +119,46 @@ class VerifyStep:
         self.commit(B, cu_rows, dst_slot, stream)
 
 
+class TraceWriter:
+    """Per-(layer, row) trace of decode transactions, for localising a parity
+    failure ("Run chained MTP drafting in the batch Engine", Validation: layer
+    tracing of every row).  Enabled by the environment: GDNSPEC_TRACE_DIR names
+    a directory; GDNSPEC_TRACE_REQS (default 2) how many leading requests get
+    their per-row checkpoints saved.  After each transaction's readback one
+    ``txn_<n>.npz`` holds the row tables, the accept lengths, bonus and emitted
+    tokens, every layer's outputs for every row (bf16 bits) and, for the
+    traced requests, every layer's checkpoint after each of their rows."""
+
+    def __init__(self, directory: str, n_reqs: int = 2):
+        self.dir = directory
+        self.n_reqs = n_reqs
+        self.count = 0
+        os.makedirs(directory, exist_ok=True)
+
+    @staticmethod
+    def from_env() -> "Optional[TraceWriter]":
+        d = os.environ.get("GDNSPEC_TRACE_DIR")
+        if not d:
+            return None
+        return TraceWriter(d, int(os.environ.get("GDNSPEC_TRACE_REQS", "2")))
+
+    def write(self, vs: "VerifyStep", cu_rows: Sequence[int], src: Sequence[int], dst: Sequence[int], accept_len,
+              bonus, out_tokens):
+        B = len(cu_rows) - 1
+        R = int(cu_rows[-1])
+        rec = {"txn": np.int64(vs.txn), "cu_rows": np.asarray(cu_rows, np.int32), "src_slot": np.asarray(src, np.int32),
+               "dst_slot": np.asarray(dst, np.int32), "accept_len": np.asarray(accept_len[:B], np.int32),
+               "bonus": np.asarray(bonus[:B], np.int32), "out_tokens": np.asarray(out_tokens[:R], np.int32),
+               "o_bf16": vs.o[:, :R].detach().contiguous().view(torch.int16).cpu().numpy().view(np.uint16)}
+        ck = getattr(vs, "ckpt", None)
+        if ck is not None:
+            for r in range(min(self.n_reqs, B)):
+                a, b = int(cu_rows[r]), int(cu_rows[r + 1])
+                rec["ckpt_req%d" % r] = ck[:, a:b].detach().cpu().numpy()
+        np.savez_compressed(os.path.join(self.dir, "txn_%06d.npz" % self.count), **rec)
+        self.count += 1
+
+
 class DecodeLoop:
     """Decode-only transactions for a fixed set of requests.
 
@@ -153,6 +194,7 @@ class DecodeLoop:
         self._io = None
         self._arena_io = None
         self._txn = ctypes.c_uint32(vs.txn)
+        self.trace = TraceWriter.from_env()
 
     @property
     def slot(self):
@@ -202,6 +244,10 @@ class DecodeLoop:
         self.h_out[B:2 * B].copy_(self.vs.bonus[:B], non_blocking=True)
         self.h_out[2 * B:].copy_(self.vs.out_tokens, non_blocking=True)
         torch.cuda.current_stream().synchronize()
+        if self.trace is not None:
+            t = self.h_tab_np
+            self.trace.write(self.vs, t[0, :B + 1].tolist(), t[1, :B].tolist(), t[2, :B].tolist(),
+                             self.h_out[:B].numpy(), self.h_out[B:2 * B].numpy(), self.h_out[2 * B:].numpy())
         return self.h_out[:B], self.h_out[B:2 * B], self.h_out[2 * B:]
 
     def transaction(self, layer_rows: Sequence[LayerRows], logits: torch.Tensor, tokens: torch.Tensor,
@@ -249,7 +295,12 @@ class DecodeLoop:
             gs.gdn_decode_transaction(vs.d, vs.L, vs.cap, self.reqs, B, self.lim, self.pool, self.plan, self._txn,
                                       io, kernel_ms, stream)
         vs.txn = self._txn.value
-        return self.h_out.numpy()[:self.plan.c.n_decode]
+        n = self.plan.c.n_decode
+        if self.trace is not None and not isinstance(vs, ArenaStep):
+            t = self.h_tab_np      # the driver wrote the step's tables here
+            self.trace.write(vs, t[0, :n + 1].tolist(), t[1, :n].tolist(), t[2, :n].tolist(), self.h_out[:n].numpy(),
+                             self.h_out[B:B + n].numpy(), self.h_out[2 * B:].numpy())
+        return self.h_out.numpy()[:n]
 
     def finish(self, accept_len):
         st = gs.gdn_pool_apply(self.pool, self.plan, self.B)
