@@ -88,7 +88,7 @@ __device__ void solve_unit_lower(float *Af, float *X, int tid, Sync sync) {
     for (int u = 0; u < 512 / NT; ++u) {
         const int e = tid + u * NT;
         const int p = e >> 8, r = (e >> 4) & 15, j = e & 15;
-        const int R0 = 32 * p + 16, C0 = 32 * p;
+        const int R0 = 32 * p + 16;
         float t = 0.f;
 #pragma unroll
         for (int q = 0; q < 4; ++q) {

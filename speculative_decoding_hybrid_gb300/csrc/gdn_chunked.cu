@@ -518,18 +518,24 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_prefill_kernel(const __grid_c
         st16(sm + smap::kBU1 + off, vh);
         st16(sm + smap::kBU2 + off, vl);
     };
-    // W^T (lanes d_k, columns t) -> the MN-major W parts.
+    // W^T (lanes d_k, columns t) -> the MN-major W parts.  W1 covers the
+    // T diag(beta e^G) tiles, free once W^T is done; W2 covers the
+    // T diag(beta) tiles, which MMA2's Ut^T half reads until all of MMA2 is
+    // done, so the second parts are written after that wait.  All SIMT
+    // threads call it (it waits); false if a wait ran out.
     auto split_w = [&]() {
         float w[16];
         tc::ld16(tmb + lane_base + tcol::kD1 + 16 * cq, w);
+        uint32_t hi[2][4], lo[2][4];
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
-            uint32_t hi[4], lo[4];
-            split8(w + 8 * half, hi, lo);
-            const uint32_t off = tc::swz_off(128, arow, 16 * cq + 8 * half);
-            st16(sm + smap::kW1 + off, hi);
-            st16(sm + smap::kW2 + off, lo);
+            split8(w + 8 * half, hi[half], lo[half]);
+            st16(sm + smap::kW1 + tc::swz_off(128, arow, 16 * cq + 8 * half), hi[half]);
         }
+        if (!wait_simt(1u << BM2)) return false;
+#pragma unroll
+        for (int half = 0; half < 2; ++half) st16(sm + smap::kW2 + tc::swz_off(128, arow, 16 * cq + 8 * half), lo[half]);
+        return true;
     };
     // Chunk c (parity b): S <- e^{G_last} S + dS and the chunk's outputs,
     // staged as bf16 [t][d_v] in the chunk's P tiles (their last reader, phase
@@ -682,7 +688,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_prefill_kernel(const __grid_c
                 load_s0(v);
                 write_S(v);
             }
-            if (prod && good && wait_simt(1u << BM2W)) split_w();
+            if (prod && good && wait_simt(1u << BM2W)) (void)split_w();
             if (next2 && gb_thread) {
                 vecp(smap::kGraw, sbuf)[tid - 64] = gr;
                 vecp(smap::kBraw, sbuf)[tid - 64] = br;
