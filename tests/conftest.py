@@ -24,3 +24,14 @@ def cuda_dev():
     if not torch.cuda.is_available():
         pytest.fail("GPU test selected but no CUDA device is visible")
     return torch.device("cuda:0")
+
+
+def pytest_terminal_summary(terminalreporter):
+    """Worst error / bound ratio of every floating-point parity check that
+    ran (1.0 is the bound), or relative Frobenius error where marked."""
+    gu = sys.modules.get("gpu_util")
+    if gu is None or not getattr(gu, "WORST", None):
+        return
+    terminalreporter.write_sep("-", "worst parity ratios (1.0 = at the bound)")
+    for name in sorted(gu.WORST):
+        terminalreporter.write_line("%-60s %.4g" % (name, gu.WORST[name]))

@@ -15,6 +15,20 @@ OUT_ATOL = 2e-3
 OUT_RREL = 2.0 ** -8 + 1e-4
 
 
+# Worst ratio of error to bound seen per check in this session (printed in
+# the terminal summary by conftest.py, so that drift toward a bound shows
+# even in a passing run).
+WORST = {}
+
+
+def noted(name, ratio):
+    """Records ratio (error / allowed, <= 1 passes) under name; returns it."""
+    r = float(ratio)
+    if r > WORST.get(name, -1.0):
+        WORST[name] = r
+    return r
+
+
 def state_err(gpu, ref):
     """Worst ratio err/allowed over a [..., h_v, d_v, d_k] state (<= 1 passes)."""
     g = np.asarray(gpu, dtype=np.float64)

@@ -122,7 +122,7 @@ def test_commit_then_verify_layers_back_to_back(gs, cuda_dev):
     against the FP64 oracle run from the committed checkpoints and bit for
     bit against the same calls with a device synchronisation in between."""
     import oracle
-    from gpu_util import state_err, out_err
+    from gpu_util import noted, out_err, state_err
     dims = sy.DIMS_FULL
     d = gs.dims(dims.h_qk, dims.h_v, dims.d_k, dims.d_v)
     Lb, rows_n, j = 3, 4, 2
@@ -153,8 +153,8 @@ def test_commit_then_verify_layers_back_to_back(gs, cuda_dev):
         h0 = [t.cpu() for t in (steps[0][l].q, steps[0][l].k, steps[0][l].v, steps[0][l].g, steps[0][l].beta)]
         _, _, ck0 = oracle.gdn_recurrent(*h0, pool0[0, l].cpu(), 1.0, want_ckpt=True)
         committed = ck0[j]
-        assert state_err(pool[0, l].cpu().numpy(), committed) <= 1.0
+        assert noted("commit then verify back to back: committed state", state_err(pool[0, l].cpu().numpy(), committed)) <= 1.0
         h1 = [t.cpu() for t in (steps[1][l].q, steps[1][l].k, steps[1][l].v, steps[1][l].g, steps[1][l].beta)]
         _, o_ref, ck1 = oracle.gdn_recurrent(*h1, torch.from_numpy(committed), 1.0, want_ckpt=True)
-        assert state_err(ck[l].cpu().numpy(), ck1) <= 1.0, l
-        assert out_err(o[l], o_ref) <= 1.0, l
+        assert noted("commit then verify back to back: checkpoints", state_err(ck[l].cpu().numpy(), ck1)) <= 1.0, l
+        assert noted("commit then verify back to back: outputs", out_err(o[l], o_ref)) <= 1.0, l

@@ -13,7 +13,7 @@ import torch
 
 import gdnsynth as sy
 import oracle
-from gpu_util import build_lib, out_err, state_err
+from gpu_util import build_lib, noted, out_err, state_err
 
 pytestmark = pytest.mark.gpu
 
@@ -96,13 +96,13 @@ def test_mixed_transaction_overlapped_equals_in_order(gs, cuda_dev):
             got = a.pool[plan.pre_dst[i], l].cpu().numpy()
             rel = max(np.linalg.norm(got[h] - S[h]) / np.linalg.norm(S[h]) for h in range(DIMS.h_v))
             assert rel <= CHUNK_STATE_RTOL, (l, i, rel)
-            assert out_err(oa[l, s:e], o_ref) <= 1.0
+            assert noted("mixed: prefill outputs", out_err(oa[l, s:e], o_ref)) <= 1.0
         dh = [t.cpu() for t in (dec[l].q, dec[l].k, dec[l].v, dec[l].g, dec[l].beta)]
         for r in range(4):
             S0 = init[plan.dec_src[r], l].cpu().numpy().astype(np.float64)
             S, o_ref, _ = oracle.gdn_recurrent(*(t[r:r + 1] for t in dh), S0)
-            assert state_err(a.pool[plan.dec_dst[r], l].cpu().numpy(), S) <= 1.0
-            assert out_err(a.o[l, r:r + 1], o_ref) <= 1.0
+            assert noted("mixed: decode state", state_err(a.pool[plan.dec_dst[r], l].cpu().numpy(), S)) <= 1.0
+            assert noted("mixed: decode outputs", out_err(a.o[l, r:r + 1], o_ref)) <= 1.0
     # slots nobody wrote are untouched
     written = set(plan.pre_dst) | set(plan.dec_dst)
     for s in range(NUM_SLOTS):
@@ -139,4 +139,4 @@ def test_next_transaction_reads_published_prefill_state(gs, cuda_dev):
         for i in range(3):
             published = vs.pool[plan.pre_dst[i], l].cpu().numpy().astype(np.float64)
             _, _, ck = oracle.gdn_recurrent(*(t[4 * i:4 * i + 4] for t in nh), published, want_ckpt=True)
-            assert state_err(vs2.ckpt[l, 4 * i:4 * i + 4].cpu().numpy(), ck) <= 1.0
+            assert noted("mixed: verify after publish", state_err(vs2.ckpt[l, 4 * i:4 * i + 4].cpu().numpy(), ck)) <= 1.0

@@ -6,7 +6,7 @@ import torch
 
 import gdnsynth as sy
 import oracle
-from gpu_util import build_lib, out_err, state_err
+from gpu_util import build_lib, noted, out_err, state_err
 
 pytestmark = pytest.mark.gpu
 
@@ -76,8 +76,8 @@ def test_prefill_small_ragged(gs, cuda_dev, lengths):
     S0s = [np.zeros((dims.h_v, 128, 128)) if s < 0 else init[s].cpu().numpy() for s in src]
     finals = [pool[d].cpu().numpy() for d in dst]
     ws, wo = check_sequences(rows, cu, o, S0s, finals, lengths)
-    assert ws <= CHUNK_STATE_RTOL, ws
-    assert wo <= 1.0, wo
+    assert noted("prefill small_ragged: state (rel. Frobenius / 5e-3)", ws / CHUNK_STATE_RTOL) <= 1.0, ws
+    assert noted("prefill small_ragged: outputs", wo) <= 1.0, wo
     for s in range(2 * n + 1):
         if s not in dst:
             assert torch.equal(pool[s], init[s]), "only destination slots are written"
@@ -97,8 +97,8 @@ def test_prefill_unused_rows_do_not_leak(gs, cuda_dev):
     finals = [pool[n + i].cpu().numpy() for i in range(n)]
     assert all(np.isfinite(f).all() for f in finals)
     ws, wo = check_sequences(rows, cu, o, [np.zeros((dims.h_v, 128, 128))] * n, finals, lengths)
-    assert ws <= CHUNK_STATE_RTOL, ws
-    assert wo <= 1.0, wo
+    assert noted("prefill unused_rows_do_not_leak: state (rel. Frobenius / 5e-3)", ws / CHUNK_STATE_RTOL) <= 1.0, ws
+    assert noted("prefill unused_rows_do_not_leak: outputs", wo) <= 1.0, wo
 
 
 def test_prefill_workload_full_size(gs, cuda_dev):
@@ -117,8 +117,8 @@ def test_prefill_workload_full_size(gs, cuda_dev):
     finals = [pool[d].cpu().numpy() for d in dst]
     ws, wo = check_sequences(rows, cu, o, [s0[i].numpy() for i in range(n)], finals, lengths)
     print("prefill full size: worst state rel %.3e, worst output ratio %.3f" % (ws, wo))
-    assert ws <= CHUNK_STATE_RTOL, ws
-    assert wo <= 1.0, wo
+    assert noted("prefill workload_full_size: state (rel. Frobenius / 5e-3)", ws / CHUNK_STATE_RTOL) <= 1.0, ws
+    assert noted("prefill workload_full_size: outputs", wo) <= 1.0, wo
 
 
 def test_mixed_transaction_defers_then_resumes(gs, cuda_dev):
@@ -184,7 +184,7 @@ def test_mixed_transaction_defers_then_resumes(gs, cuda_dev):
     for i, s in enumerate(dec_slots):
         S, _, _ = oracle.gdn_recurrent(drh.q[i:i + 1], drh.k[i:i + 1], drh.v[i:i + 1], drh.g[i:i + 1],
                                        drh.beta[i:i + 1], init[s, 0].cpu().numpy())
-        assert state_err(vs.pool[plan.dec_dst[i], 0].cpu().numpy(), S) <= 1.0
+        assert noted("mixed transaction: decode state", state_err(vs.pool[plan.dec_dst[i], 0].cpu().numpy(), S)) <= 1.0
     assert gs.gdn_pool_apply(pool_c, plan, 8) == gs.GDN_OK
     # next transaction: decode-only (the four prefilled sequences now decode too) -> K = 3 again
     slots2 = plan.dst
@@ -203,7 +203,7 @@ def test_mixed_transaction_defers_then_resumes(gs, cuda_dev):
     r2h = r2.to("cpu")
     S, o_ref, ck = oracle.gdn_recurrent(r2h.q[0:4], r2h.k[0:4], r2h.v[0:4], r2h.g[0:4], r2h.beta[0:4],
                                         published.cpu().numpy(), want_ckpt=True)
-    assert state_err(vs2.ckpt[0, 0:4].cpu().numpy(), ck) <= 1.0       # verify read the published state
+    assert noted("mixed transaction: verify after publish", state_err(vs2.ckpt[0, 0:4].cpu().numpy(), ck)) <= 1.0       # verify read the published state
 
 
 def test_prefill_fail_closed(gs, cuda_dev):
@@ -265,7 +265,8 @@ def test_prefill_timed_out_wait_publishes_nothing(gs, cuda_dev):
     assert int(st.item()) == 0
     S0s = [np.zeros((dims.h_v, 128, 128)), init[1].cpu().numpy(), init[2].cpu().numpy()]
     ws_, wo_ = check_sequences(rows, cu, o, S0s, [pool[int(x)].cpu().numpy() for x in dst.tolist()], lengths)
-    assert ws_ <= CHUNK_STATE_RTOL and wo_ <= 1.0, (ws_, wo_)
+    assert noted("prefill timed_out_wait_publishes_nothing: state (rel. Frobenius / 5e-3)", ws_ / CHUNK_STATE_RTOL) <= 1.0, ws_
+    assert noted("prefill timed_out_wait_publishes_nothing: outputs", wo_) <= 1.0, wo_
 
 
 @pytest.mark.parametrize("d,heads,lengths", [
@@ -290,8 +291,8 @@ def test_prefill_small_head_sizes(gs, cuda_dev, d, heads, lengths):
     finals = [pool[x].cpu().numpy() for x in dst]
     ws, wo = check_sequences(rows, cu, o, S0s, finals, lengths)
     print("prefill d=%d: worst state rel %.3e, worst output ratio %.3f" % (d, ws, wo))
-    assert ws <= CHUNK_STATE_RTOL, ws
-    assert wo <= 1.0, wo
+    assert noted("prefill small_head_sizes: state (rel. Frobenius / 5e-3)", ws / CHUNK_STATE_RTOL) <= 1.0, ws
+    assert noted("prefill small_head_sizes: outputs", wo) <= 1.0, wo
     for s_ in range(2 * n + 1):
         if s_ not in dst:
             assert torch.equal(pool[s_], init[s_])

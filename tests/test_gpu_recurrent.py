@@ -6,7 +6,7 @@ import torch
 
 import gdnsynth as sy
 import oracle
-from gpu_util import build_lib, oracle_request, out_err, rows_to_host, state_err
+from gpu_util import build_lib, noted, oracle_request, out_err, rows_to_host, state_err
 
 pytestmark = pytest.mark.gpu
 
@@ -75,8 +75,8 @@ def test_verify_matches_oracle(gs, cuda_dev, name, dims, rows_per_req, num_slots
     for r in range(B):
         assert int(tg[r]) == (7 << 32) | rows_per_req[r]
         S, o_ref, ck_ref = oracle_request(host, cu[r], cu[r + 1], pool[int(perm[r])], q_scale)
-        assert state_err(ck[cu[r]:cu[r + 1]].cpu().numpy(), ck_ref) <= 1.0
-        assert out_err(o[cu[r]:cu[r + 1]], o_ref) <= 1.0
+        assert noted("verify %s: checkpoints" % name, state_err(ck[cu[r]:cu[r + 1]].cpu().numpy(), ck_ref)) <= 1.0
+        assert noted("verify %s: outputs" % name, out_err(o[cu[r]:cu[r + 1]], o_ref)) <= 1.0
 
 
 @pytest.mark.parametrize("name,dims,rows_per_req,num_slots", CASES[:4], ids=[c[0] for c in CASES[:4]])
@@ -120,8 +120,8 @@ def test_decode_step_matches_oracle_and_copy_on_write(gs, cuda_dev):
     host = rows_to_host(rows)
     for i, (s, t) in enumerate([(0, 4), (0, 5), (3, 3)]):
         S, o_ref, _ = oracle_request(host, i, i + 1, pool[s])
-        assert state_err(pool_d[t].cpu().numpy()[None], S[None]) <= 1.0
-        assert out_err(o[i:i + 1], o_ref) <= 1.0
+        assert noted("decode step: state", state_err(pool_d[t].cpu().numpy()[None], S[None])) <= 1.0
+        assert noted("decode step: outputs", out_err(o[i:i + 1], o_ref)) <= 1.0
 
 
 def test_batch_invariance(gs, cuda_dev):

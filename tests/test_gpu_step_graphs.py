@@ -10,7 +10,7 @@ import pytest
 import torch
 
 import gdnsynth as sy
-from gpu_util import OracleFollow, build_lib
+from gpu_util import OracleFollow, build_lib, noted
 
 pytestmark = pytest.mark.gpu
 
@@ -105,4 +105,6 @@ def test_step_graphs_match_eager_and_oracle(gs, cuda_dev, arena):
     assert le.slot == lg.slot
     print("step graphs (%s): worst state %.3f, worst output %.3f of their bounds" %
           ("arena" if arena else "copy", follow.worst_state, follow.worst_out))
-    assert follow.worst_state <= 1.0 and follow.worst_out <= 1.0
+    mode = "arena" if arena else "copy"
+    assert noted("step graphs (%s): state" % mode, follow.worst_state) <= 1.0
+    assert noted("step graphs (%s): outputs" % mode, follow.worst_out) <= 1.0

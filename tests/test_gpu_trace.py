@@ -12,7 +12,7 @@ import torch
 
 import gdnsynth as sy
 import oracle
-from gpu_util import build_lib, out_err, state_err
+from gpu_util import build_lib, noted, out_err, state_err
 
 pytestmark = pytest.mark.gpu
 
@@ -73,4 +73,5 @@ def test_trace_rows_match_oracle(gs, cuda_dev, tmp_path, monkeypatch):
                 S[r][l] = ck_ref[int(z["accept_len"][r])]
     print("trace: %d (layer, row) pairs, worst output %.3f, worst checkpoint %.3f of their bounds" %
           (checked_rows, worst_o, worst_s))
-    assert checked_rows == steps * L * (4 + 2) and worst_o <= 1.0 and worst_s <= 1.0
+    assert checked_rows == steps * L * (4 + 2)
+    assert noted("trace: outputs", worst_o) <= 1.0 and noted("trace: checkpoints", worst_s) <= 1.0
