@@ -720,7 +720,7 @@ def bench_accept_logits(b: Bench, reps=20):
     lg_plain = plain.to(torch.bfloat16)
     del plain
     out = {"rows": R, "vocab": b.spec.vocab}
-    for name, lg in (("stated_N(0,4)", lg_plain), ("planted_ring", b.logits[0])):
+    for name, lg in (("stated_N(0,2^2)", lg_plain), ("planted_ring", b.logits[0])):
         for _ in range(3):
             vs.accept(B, loop.cu_rows, lg, b.tok_d)
         torch.cuda.synchronize()
