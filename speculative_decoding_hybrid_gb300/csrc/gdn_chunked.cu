@@ -16,16 +16,17 @@
 // run on the 5th-generation tensor cores (tcgen05, kind::f16, fp32
 // accumulators in tensor memory).  Iteration c overlaps the state-dependent
 // work of chunk c (the "scan": U, O, S') with the state-independent work of
-// chunk c+1 (the "producer": [K;Q] K^T, A and P, T, W and Ut), in five slots:
-//   1  MMA  phase A(c): U^T += -S W^T, Oi = S Q^T;  MMA1(c+1): [K;Q] K^T
+// chunk c+1 (the "producer": [K;Q] K^T, A and P, T, W and Ut), in four slots:
+//   1  MMA  phase A(c): U^T += -S W^T;  MMA1(c+1): [K;Q] K^T
+//      SIMT the outputs of chunk c-1, o = e^G Oi + Oa (while phase A runs)
 //   2  SIMT U^T -> bf16 parts of U and of U diag(dec) (tensor memory);
 //           A(c+1) (fp32, shared) and P(c+1) (bf16 parts)
-//      MMA  phase B(c): Oa = U^T P^T, dS = (U^T diag(dec)) K  (A from tensor memory)
-//   3  SIMT T(c+1) = (I + A)^{-1}, then the operands T diag(beta e^G), T diag(beta)
-//      MMA  MMA2(c+1): W^T = K^T (T diag(beta e^G))^T,  Ut^T = V^T (T diag(beta))^T
-//   4  SIMT S <- e^{G_last} S + dS (fp32 in registers, bf16 parts in shared),
-//           o = e^G Oi + Oa;  tensor copy of chunk c+2's K and Q
-//   5  SIMT W^T(c+1) -> bf16 parts;  tensor copy of chunk c+2's V
+//   3  MMA  phase B(c): Oa = U^T P^T, dS = (U^T diag(dec)) K  (A from tensor
+//           memory), then Oi(c) = S Q^T
+//      SIMT T(c+1) = (I + A)^{-1}, then the operands T diag(beta e^G), T diag(beta)
+//   4  MMA  MMA2(c+1): W^T = K^T (T diag(beta e^G))^T,  Ut^T = V^T (T diag(beta))^T
+//      SIMT S <- e^{G_last} S + dS (fp32 in registers, bf16 parts in shared);
+//           W^T(c+1) -> bf16 parts;  tensor copies of chunk c+2's K, Q and V
 // Operands that are not exact bf16 (S, U, W, P, T-derived tiles) are split
 // into two bf16 parts x = x1 + x2 and every product keeps the terms
 // a1 b1 + a1 b2 + a2 b1 (or a1 b + a2 b when b is exact: q, k, v).
@@ -315,9 +316,9 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_prefill_kernel(const __grid_c
     // Products (issuer).
     const uint64_t dsc = tc::smem_desc(sb);  // descriptor of any K-major tile: tc::desc_at(dsc, offset)
     auto kq_off = [](int b) { return smap::kKQ + 32768u * uint32_t(b); };
-    // Phase A of the chunk of parity b, in two commits: U^T += -S W^T (its
-    // consumer, the U split, comes next) and Oi = S Q^T (needed only for the
-    // outputs, at the end of the iteration).
+    // Phase A of the chunk of parity b: U^T += -S W^T (its consumer, the U
+    // split, comes next).  Oi = S Q^T, needed only for the outputs, is issued
+    // on its own after phase B.
     auto issue_phase_a_u = [&]() {
         constexpr uint32_t idU = tc::idesc_bf16(128, 64) | tc::kBMnMajor | tc::kNegA;
         const uint64_t w1b = tc::smem_desc_mn(sb + smap::kW1, 8192), w2b = tc::smem_desc_mn(sb + smap::kW2, 8192);
@@ -452,29 +453,22 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_prefill_kernel(const __grid_c
         tc::st8(tmb + lane_base + tcol::kUd2 + c8, ll);
         tc::st_wait();
     };
-    // From [K;Q] K^T of chunk c (n tokens, parity b): A (lanes 0..63, fp32 to
-    // shared) and P (lanes 64..127, bf16 parts to the P tiles of parity b).
-    // Masked entries are selected to zero, never multiplied (the products of
-    // rows past n are finite, but not necessarily zero).
-    auto build_a_p = [&](int n, int b, const uint32_t (&vr)[16]) {
+    // From [K;Q] K^T of chunk c (n tokens, parity b), passed in v16: A
+    // (lanes 0..63, fp32, left in v16 for store_a) and P (lanes 64..127, bf16
+    // parts to the P tiles of parity b).  Masked entries are selected to
+    // zero, never multiplied (the products of rows past n are finite, but not
+    // necessarily zero).
+    auto build_a_p = [&](int n, int b, float (&v16)[16]) {
         const float *G = vecp(smap::kG, b);
-        float v16[16];
-#pragma unroll
-        for (int x = 0; x < 16; ++x) v16[x] = __uint_as_float(vr[x]);
         const int t = arow & 63;
         const float gt = G[t];
         if (q4 < 2) {
             const float bt = vecp(smap::kBraw, b)[t];
 #pragma unroll
-            for (int y = 0; y < 4; ++y) {
-                float av[4];
-#pragma unroll
-                for (int z = 0; z < 4; ++z) {
-                    const int i = 16 * cq + 4 * y + z;
-                    const float e = chunkmath::gate_exp(gt - G[i]);
-                    av[z] = (i < t && t < n) ? bt * e * v16[4 * y + z] : 0.f;
-                }
-                *reinterpret_cast<float4 *>(Af + t * kAs + 16 * cq + 4 * y) = make_float4(av[0], av[1], av[2], av[3]);
+            for (int x = 0; x < 16; ++x) {
+                const int i = 16 * cq + x;
+                const float e = chunkmath::gate_exp(gt - G[i]);
+                v16[x] = (i < t && t < n) ? bt * e * v16[x] : 0.f;
             }
         } else {
             float pe[16];
@@ -493,6 +487,15 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_prefill_kernel(const __grid_c
                 st16(sm + pofs + off, hi);
                 st16(sm + pofs + 8192 + off, lo);
             }
+        }
+    };
+    auto store_a = [&](const float (&v16)[16]) {
+        if (q4 < 2) {
+            const int t = arow & 63;
+#pragma unroll
+            for (int y = 0; y < 4; ++y)
+                *reinterpret_cast<float4 *>(Af + t * kAs + 16 * cq + 4 * y) =
+                    make_float4(v16[4 * y], v16[4 * y + 1], v16[4 * y + 2], v16[4 * y + 3]);
         }
     };
     // T -> T diag(beta e^G) and T diag(beta), bf16 parts (8 entries per thread).
@@ -537,10 +540,8 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_prefill_kernel(const __grid_c
         for (int half = 0; half < 2; ++half) st16(sm + smap::kW2 + tc::swz_off(128, arow, 16 * cq + 8 * half), lo[half]);
         return true;
     };
-    // Chunk c (parity b): S <- e^{G_last} S + dS and the chunk's outputs,
-    // staged as bf16 [t][d_v] in the chunk's P tiles (their last reader, phase
-    // B, is done) and written as 16-byte rows.
-    auto update_and_outputs = [&](int c, int b) {
+    // Chunk c (parity b): S <- e^{G_last} S + dS.
+    auto update_S = [&](int c, int b) {
         const int n = chunk_n(c);
         const float *eG = vecp(smap::kEG, b);
         const float egl = eG[n - 1];
@@ -557,10 +558,20 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_prefill_kernel(const __grid_c
             sv[x] = fmaf(egl, sv[x], __uint_as_float(d0[x]));
             sv[16 + x] = fmaf(egl, sv[16 + x], __uint_as_float(d1[x]));
         }
-        uint32_t (&oi)[16] = d0, (&oa)[16] = d1;
+        write_S(sv);
+    };
+    // The outputs of chunk c (parity b), o = q_scale (e^G Oi + Oa), staged
+    // as bf16 [t][d_v] in the chunk's P tiles (their last reader, phase B, is
+    // done) and written as 16-byte rows.  They run at the start of the next
+    // iteration, while phase A(c+1) executes (Oi and Oa are overwritten only
+    // by that iteration's phase B and Oi, the P tiles only by its A/P build,
+    // e^G only by its gate sums, all after the barrier that follows).
+    auto outputs = [&](int c, int b) {
+        const int n = chunk_n(c);
+        const float *eG = vecp(smap::kEG, b);
+        uint32_t oi[16], oa[16];
         tc::ld16_async(tmb + lane_base + tcol::kOi + uint32_t(16 * cq), oi);
         tc::ld16_async(tmb + lane_base + tcol::kOa + uint32_t(16 * cq), oa);
-        write_S(sv);
         tc::ld_wait();
         tc::ld_fence_regs(oi);
         tc::ld_fence_regs(oa);
@@ -593,7 +604,8 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_prefill_kernel(const __grid_c
         const int sbuf = c & 1, pbuf = (c + 1) & 1;
         const int np = prod ? chunk_n(c + 1) : 0;
         const bool partial = prod && np < kC;
-        // ---- slot 1: phase A(c); MMA1(c+1); G, e^G, dec of chunk c+1; raw g, beta of chunk c+2
+        // ---- slot 1: phase A(c); MMA1(c+1); the outputs of chunk c-1; G, e^G,
+        // dec of chunk c+1; raw g, beta of chunk c+2
         if (issuer && scan) issue_phase_a_u();
         if (partial) {
             // the partial last chunk: its K and Q rows past n become zero first
@@ -610,10 +622,13 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_prefill_kernel(const __grid_c
         } else if (prod && issuer) {
             if (ctl_wait(BKQ0 + pbuf)) issue_mma1(pbuf);
         }
-        if (issuer && scan) issue_phase_a_o(sbuf);
         float gr = 0.f, br = 0.f;
         bool good = true;
         if (!ctl) {
+            if (c >= 1) {  // the outputs of chunk c-1 while phase A(c) executes
+                outputs(c - 1, pbuf);
+                simt_sync();  // e^G of chunk c-1 is read before the gate sums below rewrite it
+            }
             if (prod && warp == 1) {
                 float *G = vecp(smap::kG, pbuf);
                 chunkmath::chunk_cumsum(vecp(smap::kGraw, pbuf), np, G);
@@ -634,7 +649,11 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_prefill_kernel(const __grid_c
                     tc::ld16_async(tmb + lane_base + tcol::kD1 + 16 * cq, vr);
                     tc::ld_wait();
                     tc::ld_fence_regs(vr);
-                    build_a_p(np, pbuf, vr);
+                    float av[16];
+#pragma unroll
+                    for (int x = 0; x < 16; ++x) av[x] = __uint_as_float(vr[x]);
+                    build_a_p(np, pbuf, av);
+                    store_a(av);
                 }
                 if (scan) {
                     uint32_t ur[16];
@@ -657,6 +676,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_prefill_kernel(const __grid_c
         if (issuer && scan) {
             tc::fence_after();
             issue_phase_b(sbuf);
+            issue_phase_a_o(sbuf);  // Oi(c), after the outputs of chunk c-1 have read Oi(c-1)
         }
         if (!ctl && prod) {
             chunkmath::solve_unit_lower<kSimt, kAs>(Af, Xs, tid, [] { simt_sync(); });
@@ -675,14 +695,14 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_prefill_kernel(const __grid_c
         if (issuer) {
             tc::fence_after();
             if (prod && (partial || ctl_wait(BV))) issue_mma2(pbuf);
-            if (scan && next2 && ctl_wait(BB)) issue_kq(c + 2, sbuf);
+            if (scan && next2 && ctl_wait(BB) && ctl_wait(BOI)) issue_kq(c + 2, sbuf);
             if (prod && next2 && ctl_wait(BM2)) issue_v(c + 2);
         }
         if (!ctl) {
             good = true;
             if (scan) {
                 good = wait_simt((1u << BB) | (1u << BOI));
-                if (good) update_and_outputs(c, sbuf);
+                if (good) update_S(c, sbuf);
             } else {
                 float v[32];
                 load_s0(v);
@@ -713,12 +733,15 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_prefill_kernel(const __grid_c
                 if ((armed >> b) & 1u) (void)gdn::mbar_wait_bounded(&bars[b], (arm_par >> b) & 1u, a.wait_ns);
             gdn::set_status(a.status, GDN_DEV_TIMEOUT);
         }
-    } else if (!ctl && (!a.status || !(*reinterpret_cast<volatile uint32_t *>(a.status) & GDN_DEV_TIMEOUT))) {
-        // Publication: only the final state, and not after any bounded wait
-        // (here or in an earlier launch) has run out.
-        float v[32];
-        read_S(v);
-        store_dst(v);
+    } else if (!ctl) {
+        outputs(nch - 1, (nch - 1) & 1);  // the last chunk's outputs
+        if (!a.status || !(*reinterpret_cast<volatile uint32_t *>(a.status) & GDN_DEV_TIMEOUT)) {
+            // Publication: only the final state, and not after any bounded
+            // wait (here or in an earlier launch) has run out.
+            float v[32];
+            read_S(v);
+            store_dst(v);
+        }
     }
     tc::fence_before();
     __syncthreads();
