@@ -353,6 +353,10 @@ int gdn_verify_replay_layers(const gdn_dims *dims, int32_t num_layers, int32_t B
  * cu_seqlens[i+1]-1 (packed like q,k,v,g,beta,o).  Sequence i starts from
  * slot src_slot[i] (or from zero when src_slot[i] == -1), writes o for every
  * token and publishes only its final state to dst_slot[i].  chunk = 64.
+ * dst_slot[i] may equal src_slot[i] (in place); otherwise the destination
+ * slots of one call must be distinct and none may be another sequence's
+ * source in the same call (sequences run concurrently, so such a read would
+ * race with the write; plan_transaction's destinations satisfy this).
  * Work is ordered on `stream`, so a decode/verify queued after it on the
  * same stream reads the published state ([NATIVE] What changed).
  * max_seqlen (host, >= 0) is accepted for callers that track it; every

@@ -83,6 +83,26 @@ def test_prefill_small_ragged(gs, cuda_dev, lengths):
             assert torch.equal(pool[s], init[s]), "only destination slots are written"
 
 
+@pytest.mark.parametrize("h_qk,h_v", [(4, 4), (1, 4), (2, 8)], ids=["grp1", "grp4", "grp4b"])
+def test_prefill_head_grouping(gs, cuda_dev, h_qk, h_v):
+    """Every v-head reads the q/k head h_v // h_qk of its group (no grouping,
+    four v-heads per q/k head), with the start states of half the sequences
+    taken from slots."""
+    dims = sy.Dims(h_qk, h_v, 128, 128)
+    lengths = [97, 64, 3]
+    n = len(lengths)
+    pool = sy.state(sy.generator(13), (2 * n, dims.h_v, dims.d_v, dims.d_k)).to(cuda_dev)
+    init = pool.clone()
+    src = [-1, 1, 2]
+    dst = [n + i for i in range(n)]
+    rows, cu, o, st = run_prefill(gs, cuda_dev, dims, lengths, src, dst, pool, seed=17)
+    assert st == 0
+    S0s = [np.zeros((dims.h_v, 128, 128)) if x < 0 else init[x].cpu().numpy() for x in src]
+    ws, wo = check_sequences(rows, cu, o, S0s, [pool[d].cpu().numpy() for d in dst], lengths)
+    assert noted("prefill head_grouping: state (rel. Frobenius / 5e-3)", ws / CHUNK_STATE_RTOL) <= 1.0, ws
+    assert noted("prefill head_grouping: outputs", wo) <= 1.0, wo
+
+
 def test_prefill_unused_rows_do_not_leak(gs, cuda_dev):
     """Capacity past the last sequence holds NaN in q, k, v, g and beta; the
     last chunk's 64-row window reaches into it, and nothing of it may reach
