@@ -875,12 +875,15 @@ def run_e2e(b: Bench, host, stages, steps, warmup):
     # (the host's readback, planning and launch of the next step)
     gaps = [marks[i][1].elapsed_time(marks[i + 1][0]) for i in range(len(marks) - 1)]
     gap_ms = sum(gaps) / len(gaps) if gaps else 0.0
+    # the steps' own device time with the input copies beside them
+    spans = [a.elapsed_time(c) for a, c in marks]
+    step_ms = sum(spans) / len(spans) if spans else 0.0
     # the input copies as they ran beside the steps (HBM shared with the kernels)
     in_step = [a.elapsed_time(c) for a, c in copies]
     copy_in_step_ms = sum(in_step) / len(in_step) if in_step else 0.0
     h2d = moved_bytes[0] / steps + (b.loop.B + 1) * 3 * 4 + b.cap * 4   # inputs + tables + tokens
     d2h = (2 * spec.batch + b.cap) * 4
-    return tok / dt, h2d, d2h, copy_ms, gap_ms, copy_in_step_ms
+    return tok / dt, h2d, d2h, copy_ms, gap_ms, copy_in_step_ms, step_ms
 
 
 # ---------------------------------------------------------------------------
@@ -1073,7 +1076,7 @@ def main():
     e2e = None
     if not args.no_e2e:
         host, stages = stage_e2e(b)
-        val, h2d, d2h, copy_ms, gap_ms, copy_in_step_ms = run_e2e(b, host, stages, args.e2e_steps, 3)
+        val, h2d, d2h, copy_ms, gap_ms, copy_in_step_ms, step_ms = run_e2e(b, host, stages, args.e2e_steps, 3)
         del host, stages
         if world > 1:
             t = torch.tensor([val], device=dev, dtype=torch.float64)
@@ -1082,7 +1085,8 @@ def main():
         e2e = {"value": val, "unit": "verified tokens/s", "h2d_bytes_per_step": int(h2d),
                "d2h_bytes_per_step": int(d2h), "steps": args.e2e_steps,
                "input_copy_ms_alone": copy_ms, "input_copy_gbs": h2d / (copy_ms * 1e-3) / 1e9,
-               "device_idle_ms_between_steps": gap_ms, "input_copy_ms_beside_steps": copy_in_step_ms}
+               "device_idle_ms_between_steps": gap_ms, "input_copy_ms_beside_steps": copy_in_step_ms,
+               "device_ms_per_step_beside_copies": step_ms}
 
     if rank != 0:
         if world > 1:
