@@ -20,8 +20,10 @@ def gs(cuda_dev):
     return binding
 
 
-def run_prefill(gs, dev, dims, lengths, src, dst, pool, seed=3, cap=None):
+def run_prefill(gs, dev, dims, lengths, src, dst, pool, seed=3, cap=None, shape_rows=None):
     rows, cu, s0 = sy.prefill_inputs(lengths, dims, seed=seed)
+    if shape_rows is not None:
+        rows = shape_rows(rows)
     R = int(cu[-1])
     cap = R if cap is None else cap
     d = gs.dims(dims.h_qk, dims.h_v, dims.d_k, dims.d_v)
@@ -101,6 +103,51 @@ def test_prefill_head_grouping(gs, cuda_dev, h_qk, h_v):
     ws, wo = check_sequences(rows, cu, o, S0s, [pool[d].cpu().numpy() for d in dst], lengths)
     assert noted("prefill head_grouping: state (rel. Frobenius / 5e-3)", ws / CHUNK_STATE_RTOL) <= 1.0, ws
     assert noted("prefill head_grouping: outputs", wo) <= 1.0, wo
+
+
+def _strong_decay(r):
+    return sy.Rows(r.q, r.k, r.v, torch.full_like(r.g, -20.0), r.beta)
+
+
+def _repeated_keys_no_decay(r):
+    # runs of 8 tokens share one (already unit-norm, bf16) key; g = 0, beta = 1:
+    # the in-chunk matrix A has its largest entries and T = (I + A)^{-1} its
+    # largest cancellations
+    k = r.k.clone()
+    for t in range(0, k.shape[0], 8):
+        k[t:t + 8] = k[t]
+    return sy.Rows(r.q, k, r.v, torch.zeros_like(r.g), torch.ones_like(r.beta))
+
+
+def _tiny_beta(r):
+    return sy.Rows(r.q, r.k, r.v, r.g, torch.full_like(r.beta, 1e-6))
+
+
+@pytest.mark.parametrize("d", [128, 32])
+@pytest.mark.parametrize("shape", [_strong_decay, _repeated_keys_no_decay, _tiny_beta],
+                         ids=["strong_decay", "repeated_keys_no_decay", "tiny_beta"])
+def test_prefill_extreme_gates(gs, cuda_dev, shape, d):
+    """Gates and keys at the edges of their ranges, against the FP64
+    recurrence: g = -20 on every token (the in-chunk exponentials underflow
+    to zero), g = 0 and beta = 1 with keys repeated in runs of 8, and
+    beta = 1e-6; start states from zero and from slots; on the tensor-core
+    kernel (d = 128) and the fp32 one (d = 32)."""
+    dims = sy.Dims(2, 4, d, d)
+    lengths = [130, 64, 7]
+    n = len(lengths)
+    pool = sy.state(sy.generator(23), (2 * n, dims.h_v, dims.d_v, dims.d_k)).to(cuda_dev)
+    init = pool.clone()
+    src = [-1, 1, 2]
+    dst = [n + i for i in range(n)]
+    rows, cu, o, st = run_prefill(gs, cuda_dev, dims, lengths, src, dst, pool, seed=29, shape_rows=shape)
+    assert st == 0
+    S0s = [np.zeros((dims.h_v, d, d)) if x < 0 else init[x].cpu().numpy() for x in src]
+    finals = [pool[j].cpu().numpy() for j in dst]
+    assert all(np.isfinite(f).all() for f in finals)
+    ws, wo = check_sequences(rows, cu, o, S0s, finals, lengths)
+    name = "%s d=%d" % (shape.__name__.strip("_"), d)
+    assert noted("prefill extreme %s: state (rel. Frobenius / 5e-3)" % name, ws / CHUNK_STATE_RTOL) <= 1.0, ws
+    assert noted("prefill extreme %s: outputs" % name, wo) <= 1.0, wo
 
 
 def test_prefill_unused_rows_do_not_leak(gs, cuda_dev):
