@@ -25,24 +25,30 @@ def _pool(gs, num_slots):
     return p
 
 
-def test_replay_loop_matches_checkpoint_loop(gs, cuda_dev):
+def _replay_matches_checkpoints(gs, cuda_dev, dims, k_hi, p_accept, steps, label):
+    """Both decode loops over the same steps: draft counts drawn from
+    0..k_hi (request 2 always asks for k_hi), draft hits Bernoulli with
+    p_accept(step); every step's accepted lengths, tokens and outputs equal,
+    the final slots bit-identical, three requests (one of them request 2)
+    followed by the oracle."""
     from speculative_decoding_hybrid_gb300.step import DecodeLoop, LayerRows, ReplayStep, VerifyStep
-    dims = sy.Dims(4, 8, 128, 128)
     d = gs.dims(dims.h_qk, dims.h_v, dims.d_k, dims.d_v)
-    L, B, num_slots, vocab, steps = 3, 6, 12, 4096, 7
-    cap = B * 4
+    L, B, num_slots, vocab = 3, 6, 12, 4096
+    cap = B * (k_hi + 1)
     init = sy.state(sy.generator(3), (num_slots, L, dims.h_v, dims.d_v, dims.d_k)).to(cuda_dev)
     slots = [5, 5, 0, 3, 7, 1]              # requests 0 and 1 share slot 5
     vs = VerifyStep(d, L, num_slots, cap, B, vocab, cuda_dev, pool=init.clone())
     rs = ReplayStep(d, L, num_slots, cap, B, vocab, cuda_dev, pool=init.clone())
-    lc = DecodeLoop(vs, slots, _pool(gs, num_slots))
-    lr = DecodeLoop(rs, slots, _pool(gs, num_slots))
+    lc = DecodeLoop(vs, slots, _pool(gs, num_slots), k_max=k_hi)
+    lr = DecodeLoop(rs, slots, _pool(gs, num_slots), k_max=k_hi)
     from gpu_util import OracleFollow
-    follow = OracleFollow({r: [init[slots[r], l].cpu().numpy() for l in range(L)] for r in (1, 4)})
+    follow = OracleFollow({r: [init[slots[r], l].cpu().numpy() for l in range(L)] for r in (1, 2, 4)})
     kg = sy.generator(4)
     keep = []
+    max_replayed = 0
     for s in range(steps):
-        ks = torch.randint(0, 4, (B,), generator=kg).tolist()
+        ks = torch.randint(0, k_hi + 1, (B,), generator=kg).tolist()
+        ks[2] = k_hi
         pc = lc.plan_step(ks)
         pr = lr.plan_step(ks)
         assert pc.dec_cu == pr.dec_cu and pc.dec_src == pr.dec_src and pc.dec_dst == pr.dec_dst
@@ -52,7 +58,7 @@ def test_replay_loop_matches_checkpoint_loop(gs, cuda_dev):
         lrows = [LayerRows(r.q, r.k, r.v, r.g, r.beta) for r in rows]
         keep.append(lrows)
         lg, tgt = sy.logits(sy.generator(70 + s), R, vocab, 2.0, cuda_dev)
-        toks = torch.tensor(sum(sy.drafts(sy.generator(90 + s), tgt.tolist(), pc.k, vocab, 0.85), []),
+        toks = torch.tensor(sum(sy.drafts(sy.generator(90 + s), tgt.tolist(), pc.k, vocab, p_accept(s)), []),
                             dtype=torch.int32, device=cuda_dev)
         lc.upload_tables()
         lc.run(lrows, lg, toks)
@@ -60,6 +66,7 @@ def test_replay_loop_matches_checkpoint_loop(gs, cuda_dev):
         lr.upload_tables()
         lr.run(lrows, lg, toks)
         ar, br, orr = (x.clone() for x in lr.readback())
+        max_replayed = max(max_replayed, int(ar.max()) + 1)  # replayed by the next launch or the flush
         assert int(vs.status.item()) == 0 and int(rs.status.item()) == 0
         assert torch.equal(ac, ar) and torch.equal(bc, br) and torch.equal(oc[:R], orr[:R])
         assert torch.equal(vs.o[:, :R], rs.o[:, :R]), "outputs are computed from bit-identical states"
@@ -80,10 +87,26 @@ def test_replay_loop_matches_checkpoint_loop(gs, cuda_dev):
         follow.check_state(r, [rs.pool[lr.slot[r], l].cpu().numpy() for l in range(L)])
     print("replay vs oracle: worst state %.3f, worst output %.3f of their bounds" %
           (follow.worst_state, follow.worst_out))
-    assert noted("fixed-state replay: state", follow.worst_state) <= 1.0
-    assert noted("fixed-state replay: outputs", follow.worst_out) <= 1.0
+    assert noted("fixed-state replay%s: state" % label, follow.worst_state) <= 1.0
+    assert noted("fixed-state replay%s: outputs" % label, follow.worst_out) <= 1.0
     # the shared slot was never written by either path
     assert torch.equal(rs.pool[5], init[5]) and torch.equal(vs.pool[5], init[5])
+    return max_replayed
+
+
+def test_replay_loop_matches_checkpoint_loop(gs, cuda_dev):
+    _replay_matches_checkpoints(gs, cuda_dev, sy.Dims(4, 8, 128, 128), 3, lambda s: 0.85, 7, "")
+
+
+@pytest.mark.parametrize("dims", [sy.Dims(4, 8, 128, 128), sy.Dims(2, 4, 64, 64), sy.Dims(2, 4, 32, 32),
+                                  sy.Dims(2, 2, 16, 16)], ids=["d128", "d64", "d32", "d16"])
+def test_replay_at_the_maximum_draft_count(gs, cuda_dev, dims):
+    """K = 15: a request that accepted all 15 drafts replays 16 rows (the most
+    one launch takes) before its 16 new rows; every other step draws its hits
+    at 0.85, so short and long replays mix."""
+    top = _replay_matches_checkpoints(gs, cuda_dev, dims, 15, lambda s: 1.0 if s % 2 == 0 else 0.85, 5,
+                                      " K=15 d%d" % dims.d_k)
+    assert top == 16, "no step replayed the maximum of 16 rows"
 
 
 def test_replay_refuses_more_accepted_rows_than_existed(gs, cuda_dev):
