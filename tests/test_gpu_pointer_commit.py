@@ -18,12 +18,14 @@ def gs(cuda_dev):
     return binding
 
 
-def test_arena_loop_matches_copy_loop(gs, cuda_dev):
+def _arena_matches_copy(gs, cuda_dev, dims, k_hi, p_accept, steps, label):
+    """The copying loop and the zero-copy loop over the same steps: draft
+    counts from 0..k_hi (request 2 always asks for k_hi), hits Bernoulli with
+    p_accept(step); three requests followed by the FP64 oracle."""
     from speculative_decoding_hybrid_gb300.step import ArenaStep, LayerRows, VerifyStep
-    dims = sy.Dims(4, 8, 128, 128)
     d = gs.dims(dims.h_qk, dims.h_v, dims.d_k, dims.d_v)
-    L, B, num_slots, vocab, steps = 3, 6, 8, 4096, 7
-    cap = B * 4
+    L, B, num_slots, vocab = 3, 6, 8, 4096
+    cap = B * (k_hi + 1)
     init = sy.state(sy.generator(1), (num_slots, L, dims.h_v, dims.d_v, dims.d_k)).to(cuda_dev)
     slots = [5, 0, 3, 7, 1, 6]
     vs = VerifyStep(d, L, num_slots, cap, B, vocab, cuda_dev, pool=init.clone())
@@ -32,10 +34,12 @@ def test_arena_loop_matches_copy_loop(gs, cuda_dev):
     ar.point_at_slots(slots)
     slot_d = torch.tensor(slots, dtype=torch.int32, device=cuda_dev)
     from gpu_util import OracleFollow
-    follow = OracleFollow({r: [init[slots[r], l].cpu().numpy() for l in range(L)] for r in (0, 4)})
+    follow = OracleFollow({r: [init[slots[r], l].cpu().numpy() for l in range(L)] for r in (0, 2, 4)})
     kg = sy.generator(2)
+    max_acc = []
     for s in range(steps):
-        ks = torch.randint(0, 4, (B,), generator=kg).tolist()
+        ks = torch.randint(0, k_hi + 1, (B,), generator=kg).tolist()
+        ks[2] = k_hi
         cu = [0]
         for k in ks:
             cu.append(cu[-1] + k + 1)
@@ -43,7 +47,7 @@ def test_arena_loop_matches_copy_loop(gs, cuda_dev):
         rows = [sy.rows(sy.generator(100 * s + l), R, dims, cuda_dev) for l in range(L)]
         lrows = [LayerRows(r.q, r.k, r.v, r.g, r.beta) for r in rows]
         lg, tgt = sy.logits(sy.generator(7 + s), R, vocab, 2.0, cuda_dev)
-        toks = torch.tensor(sum(sy.drafts(sy.generator(9 + s), tgt.tolist(), ks, vocab, 0.85), []),
+        toks = torch.tensor(sum(sy.drafts(sy.generator(9 + s), tgt.tolist(), ks, vocab, p_accept(s)), []),
                             dtype=torch.int32, device=cuda_dev)
         cu_d = torch.tensor(cu, dtype=torch.int32, device=cuda_dev)
         vs.run(B, cu_d, slot_d, slot_d, lrows, lg, toks)
@@ -58,11 +62,12 @@ def test_arena_loop_matches_copy_loop(gs, cuda_dev):
         follow.step(cu, [[t.cpu() for t in (x.q, x.k, x.v, x.g, x.beta)] for x in rows], lg.cpu(), toks.cpu(), vocab,
                     ar.accept_len[:B].tolist(), ar.o[:, :R])
         for r in follow.S:
-            follow.check_state(r, [ar.arena[int(ar.loc[l, r]):int(ar.loc[l, r]) + ar.S].view(8, 128, 128).cpu()
+            follow.check_state(r, [ar.arena[int(ar.loc[l, r]):int(ar.loc[l, r]) + ar.S].view(dims.h_v, dims.d_v, dims.d_k).cpu()
                                    .numpy() for l in range(L)])
         # every location points at the accepted checkpoint of this transaction's area
         area = ar.txn & 1
         acc = ar.accept_len[:B].tolist()
+        max_acc.append(max(acc))
         for l in range(L):
             for r in range(B):
                 assert int(ar.loc[l, r]) == ar.area_off[area] + l * ar.ckpt_layer_stride + (cu[r] + acc[r]) * ar.S
@@ -74,8 +79,23 @@ def test_arena_loop_matches_copy_loop(gs, cuda_dev):
         assert torch.equal(ar.pool[sl], vs.pool[sl])
     print("zero-copy commit vs oracle: worst state %.3f, worst output %.3f of their bounds" %
           (follow.worst_state, follow.worst_out))
-    assert noted("zero-copy commit: state", follow.worst_state) <= 1.0
-    assert noted("zero-copy commit: outputs", follow.worst_out) <= 1.0
+    assert noted("zero-copy commit%s: state" % label, follow.worst_state) <= 1.0
+    assert noted("zero-copy commit%s: outputs" % label, follow.worst_out) <= 1.0
+    return max(max_acc)
+
+
+def test_arena_loop_matches_copy_loop(gs, cuda_dev):
+    _arena_matches_copy(gs, cuda_dev, sy.Dims(4, 8, 128, 128), 3, lambda s: 0.85, 7, "")
+
+
+@pytest.mark.parametrize("dims", [sy.Dims(4, 8, 128, 128), sy.Dims(2, 4, 64, 64), sy.Dims(2, 4, 32, 32),
+                                  sy.Dims(2, 2, 16, 16)], ids=["d128", "d64", "d32", "d16"])
+def test_arena_loop_at_the_maximum_draft_count(gs, cuda_dev, dims):
+    """K = 15 (16 rows per request, the most one verify launch takes): on the
+    all-hit steps the location points at checkpoint 15 of the request."""
+    top = _arena_matches_copy(gs, cuda_dev, dims, 15, lambda s: 1.0 if s % 2 == 0 else 0.85, 5,
+                              " K=15 d%d" % dims.d_k)
+    assert top == 15, "no step accepted all 15 drafts"
 
 
 def test_commit_at_refuses_stale_tags_and_bad_locations(gs, cuda_dev):
