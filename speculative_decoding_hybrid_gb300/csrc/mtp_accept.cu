@@ -106,27 +106,48 @@ __global__ void __launch_bounds__(kArgThreads) argmax_partial_kernel(const ArgAr
         const uint4 *vp = reinterpret_cast<const uint4 *>(rp + c0);
         const int64_t nvec = (c1 - c0) / 8;
         int64_t i = threadIdx.x;
+        const int lane = threadIdx.x & 31;
         uint32_t best_o = 0, best_i = 0;  // order 0 is below every value: nothing seen yet
-        uint32_t best2 = 0xff80ff80u;     // the prefilter's running maximum (bf16 pair; valid once seen)
-        bool seen = false;
-        for (; i + 3 * kArgThreads < nvec; i += 4 * kArgThreads) {
-            uint4 w[4];
+        // The warp's prefilter: the order of the largest value any of its lanes
+        // has recorded.  A group of 4 kArgThreads vectors (indices above every
+        // earlier group's) whose largest value does not exceed it can neither
+        // beat that value nor win a tie with it, so the whole warp skips the
+        // exact scan; the test is the same for every lane (one warp-wide max),
+        // so the warp never runs the scan for one lane's sake.  The loop runs
+        // while the warp's last lane has a whole group, so it is uniform too,
+        // and the next group's loads go out before this group is examined.
+        uint32_t warp_best = 0;
+        bool have = i - lane + 31 + 3 * kArgThreads < nvec;
+        uint4 w[4];
+        if (have) {
 #pragma unroll
             for (int u = 0; u < 4; ++u) w[u] = __ldcs(vp + i + u * kArgThreads);
-            // Prefilter in the bf16 domain: the chunk can only matter if its
-            // packed maximum differs from the running one (ties of -0 and +0
-            // pass here and are settled by the exact order below).
+        }
+        while (have) {
+            const int64_t inext = i + 4 * kArgThreads;
+            const bool more = inext - lane + 31 + 3 * kArgThreads < nvec;
+            uint4 nx[4];
+            if (more) {
+#pragma unroll
+                for (int u = 0; u < 4; ++u) nx[u] = __ldcs(vp + inext + u * kArgThreads);
+            }
             uint32_t m = bmax2(bmax2(bmax2(w[0].x, w[0].y), bmax2(w[0].z, w[0].w)),
                                bmax2(bmax2(w[1].x, w[1].y), bmax2(w[1].z, w[1].w)));
             m = bmax2(m, bmax2(bmax2(bmax2(w[2].x, w[2].y), bmax2(w[2].z, w[2].w)),
                                bmax2(bmax2(w[3].x, w[3].y), bmax2(w[3].z, w[3].w))));
-            m = bmax2(m, __byte_perm(m, 0u, 0x1032));  // both halves: the chunk's maximum
-            if (!seen || bmax2(m, best2) != best2) {
-                seen = true;
-                best2 = bmax2(m, best2);
+            const uint32_t mo_lo = order17(m & 0xffffu), mo_hi = order17(m >> 16);
+            const uint32_t wm = __reduce_max_sync(0xffffffffu, mo_lo > mo_hi ? mo_lo : mo_hi);
+            if (wm > warp_best) {
+                warp_best = wm;
 #pragma unroll
                 for (int u = 0; u < 4; ++u)
                     scan_vec(w[u], uint32_t(c0 + (i + u * kArgThreads) * 8), vec_max_order(w[u]), best_o, best_i);
+            }
+            i = inext;
+            have = more;
+            if (more) {
+#pragma unroll
+                for (int u = 0; u < 4; ++u) w[u] = nx[u];
             }
         }
         for (; i < nvec; i += kArgThreads) {
