@@ -37,8 +37,8 @@ def run_accept(gs, dev, logits, vocab, tokens, cu, stats=None, cap=None):
     return am.cpu().numpy(), acc.cpu().numpy()[:B], bon.cpu().numpy()[:B], out.cpu().numpy(), int(st.item()), stats
 
 
-def check_against_oracle(gs, dev, logits_cpu, vocab, tokens, cu):
-    am, acc, bon, out, st, stats = run_accept(gs, dev, logits_cpu.to(dev), vocab, tokens, cu)
+def check_against_oracle(gs, dev, logits_cpu, vocab, tokens, cu, cap=None):
+    am, acc, bon, out, st, stats = run_accept(gs, dev, logits_cpu.to(dev), vocab, tokens, cu, cap=cap)
     bits = oracle.bf16_bits(logits_cpu)[:, :vocab]
     am_ref = oracle.argmax_bf16(np.ascontiguousarray(bits))
     R = cu[-1]
@@ -88,6 +88,42 @@ def test_ties_nan_and_split_boundaries(gs, cuda_dev):
     cu = [0, 2, 4, 7]
     toks[1] = 70000           # draft equals row 0's greedy choice
     check_against_oracle(gs, cuda_dev, lg, V, toks, cu)
+
+
+def test_whole_row_scans_adversarial_orders(gs, cuda_dev):
+    """A row capacity of 1,024 gives one CTA per row (no vocabulary split), so
+    every thread streams ~74 vectors through the grouped scan whose exact key
+    search a warp skips when the group's largest value does not beat the
+    largest it has recorded.  Orders that defeat or test that skip: a rising
+    ramp (every group beats the last; bf16 rounding makes plateaus, so the
+    first index of the top plateau must win), a falling ramp, a constant row,
+    the maximum repeated in many groups, the maximum only in the per-lane tail,
+    an equal value earlier than that tail, a NaN after a large value, and
+    -0 / +0 as the top in either order."""
+    V = 151936
+    R = 10
+    lg = (torch.randn((R, V), generator=sy.generator(31)) * 2.0).to(torch.bfloat16)
+    ramp = torch.linspace(-40.0, 40.0, V)
+    lg[0] = ramp.to(torch.bfloat16)
+    lg[1] = ramp.flip(0).to(torch.bfloat16)
+    lg[2] = 1.5
+    for i in range(5003, V, 997):
+        lg[3, i] = 20.0
+    lg[4, V - 1] = 25.0
+    lg[5, V - 2] = 25.0
+    lg[5, 12345] = 25.0
+    lg[6, 300] = 40.0
+    lg[6, 140000] = float("nan")
+    lg[7] = -2.0
+    lg[7, 100000] = -0.0
+    lg[7, 50000] = 0.0
+    lg[8] = -2.0
+    lg[8, 50000] = -0.0
+    lg[8, 100000] = 0.0
+    lg[9] = float("-inf")
+    toks = list(range(R))
+    cu = [0, 4, 10]
+    check_against_oracle(gs, cuda_dev, lg, V, toks, cu, cap=1024)
 
 
 @pytest.mark.parametrize("vocab,stride", [(64, 64), (1001, 1001), (1001, 1008), (5000, 5003), (151936, 151936)])
